@@ -1,0 +1,225 @@
+/*
+ * shadowkv.h -- C ABI of the ShadowKV decode path for GB300 (sm_103a).
+ *
+ * The method is the one of "ShadowKV: KV Cache in Shadows for High-Throughput
+ * Long-Context LLM Inference" as the xllm-io paper review page states it:
+ *   - Algorithm 1 (Pre-filling): A, B <- SVD(K) over the pre-RoPE keys;
+ *     landmarks L <- Reduce(K_RoPE) per chunk of c tokens; S <- cosine of
+ *     each token to its chunk mean; outliers I <- ArgTopK(-Min(S), o);
+ *     V offloaded to the CPU.
+ *   - Algorithm 2 (Decoding): P <- MatMul(Q, L^T); I <- ArgTopK(S2, k);
+ *     in parallel V_sparse <- Gather(V_CPU, I) and
+ *     K_sparse <- MatMul(Gather(A, I), B); attention over
+ *     [K_outlier; RoPE(K_sparse); K_local].
+ *   - The temporal-locality cache (section 核心创新, and the Telegram explainer
+ *     of ShadowKV): chunks selected at the previous step stay on the GPU and
+ *     only the set difference is fetched from host memory.
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are dense, row-major, in the element type given by
+ *     shadowkv_params.dtype (SKV_DTYPE_F32: float, SKV_DTYPE_BF16: bfloat16).
+ *     Index tensors are int32.
+ *   - "device" pointers are CUDA global-memory addresses on the context's
+ *     device; "host" pointers are ordinary CPU addresses.  The caller owns
+ *     every pointer it passes; the library never frees or keeps them past the
+ *     call (prefill copies what it needs).
+ *   - stream is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Work is enqueued on it in order; calls return before the GPU
+ *     finishes unless stated otherwise.  The decode step also uses one
+ *     library-owned side stream, joined back to `stream` before it returns.
+ *   - Every entry point returns an skv_status; on failure
+ *     shadowkv_last_error() (thread-local) describes the cause.  No entry point
+ *     aborts the process, traps the GPU, or falls back to the CPU.
+ *   - Shapes: n = (s - w) / c chunks form the compressed region [0, s - w);
+ *     the last w prompt tokens and every appended token form the exact local
+ *     window.  G = h_q / h_kv query heads share a KV head; query head g uses
+ *     KV head g / G.
+ */
+#ifndef SHADOWKV_H
+#define SHADOWKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum skv_status {
+  SKV_OK = 0,
+  SKV_ERR_INVALID_ARG = 1,   /* bad shape, pointer, option or size */
+  SKV_ERR_OOM = 2,           /* device or pinned-host allocation failed */
+  SKV_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
+  SKV_ERR_DEVICE_CHECK = 4,  /* a kernel found an out-of-range index (status word) */
+  SKV_ERR_TIMEOUT = 5,       /* a bounded device wait gave up */
+  SKV_ERR_STATE = 6,         /* call not valid in the context's state (e.g. max_new reached) */
+  SKV_ERR_UNSUPPORTED = 7    /* a combination the kernels do not implement */
+} skv_status;
+
+enum { SKV_DTYPE_F32 = 0, SKV_DTYPE_BF16 = 1 };
+/* How S2 combines the softmax scores of a KV head's query group (S2 is not
+ * defined on the page): maximum over the group (default) or their sum. */
+enum { SKV_GROUP_MAX = 0, SKV_GROUP_SUM = 1 };
+
+/* Shapes and parameters of one attention layer.  Algorithm 1's r, c, o and
+ * Algorithm 2's k follow the page's notation. */
+typedef struct shadowkv_params {
+  int b;            /* sequences in the batch */
+  int h_q;          /* query heads (multiple of h_kv) */
+  int h_kv;         /* key/value heads */
+  int d;            /* head dimension: 64 or 128 */
+  int s;            /* prompt tokens */
+  int c;            /* chunk size (tokens per landmark) */
+  int r;            /* SVD rank of the pre-RoPE key cache, <= min(s, h_kv*d), <= 256 */
+  int k;            /* chunks selected per KV head per step, 1..min(n - o, 1024) */
+  int o;            /* outlier chunks per KV head, 0..n - 1 */
+  int w;            /* local-window prompt tokens; (s - w) must be a positive multiple of c */
+  int max_new;      /* decode steps the context can append */
+  float rope_theta; /* RoPE base; rotate-half pairing (i, i + d/2) */
+  int dtype;        /* SKV_DTYPE_F32 or SKV_DTYPE_BF16 */
+  int group_reduce; /* SKV_GROUP_MAX or SKV_GROUP_SUM */
+  int svd_iters;    /* subspace iterations of the prefill SVD; 0 = default (3) */
+  int reserved;     /* must be 0 */
+  unsigned long long seed; /* seed of the SVD's random starting basis */
+} shadowkv_params;
+
+typedef struct shadowkv_ctx shadowkv_ctx;   /* opaque, library-owned */
+
+/* Cumulative counters of a context. */
+typedef struct shadowkv_stats {
+  long long steps;       /* decode steps enqueued */
+  long long hits;        /* selected chunks already resident in the cache */
+  long long misses;      /* selected chunks fetched from host memory */
+  long long link_bytes;  /* value bytes read over the host link by the fetch */
+  long long launches;    /* kernels launched by this context */
+} shadowkv_stats;
+
+/* Checks the parameters without touching the GPU. */
+skv_status shadowkv_validate_params(const shadowkv_params* p);
+
+/* Bytes the context will hold on the device and in pinned host memory
+ * (excluding the transient prefill workspace).  Host-only. */
+skv_status shadowkv_footprint(const shadowkv_params* p, size_t* device_bytes,
+                              size_t* host_bytes);
+
+/*
+ * Algorithm 1 (Pre-filling).
+ *   k_pre : device, b x h_kv x s x d, pre-RoPE keys.
+ *   v     : b x h_kv x s x d values; a host pointer if v_on_host != 0, else device.
+ * Computes K_RoPE (position = token index), landmarks L (chunk means of
+ * K_RoPE over [0, s - w)), the per-chunk minimum cosine, the o outlier chunks
+ * per (sequence, KV head) by ArgTopK(-min cos) (ties to the lower index),
+ * the rank-r factors A (b x s x r) and B (b x h_kv x r x d) of the pre-RoPE
+ * keys of each sequence viewed as an s x (h_kv d) matrix, the post-RoPE keys
+ * and values of the outlier chunks and of the local window, and copies V to
+ * library-owned pinned host memory.  On success *out owns everything; k_pre
+ * and v may be freed once `stream` has passed the call (the call synchronizes
+ * `stream` before returning when v is on the host).
+ */
+skv_status shadowkv_prefill(const shadowkv_params* p, const void* k_pre, const void* v,
+                            int v_on_host, void* stream, shadowkv_ctx** out);
+
+/* A compressed layer state supplied by the caller instead of computed by
+ * shadowkv_prefill (checkpoint restore, or a prefill done elsewhere).  All
+ * device pointers, element type p->dtype, except V (see v_on_host). */
+typedef struct shadowkv_state_in {
+  const void* A;               /* b x s x r */
+  const void* B;               /* b x h_kv x r x d */
+  const void* L;               /* b x h_kv x n x d landmarks */
+  const int32_t* outlier_ids;  /* b x h_kv x o, ascending, distinct, < n */
+  const void* K_out;           /* b x h_kv x (o c) x d post-RoPE outlier keys, chunk order of outlier_ids */
+  const void* V_out;           /* b x h_kv x (o c) x d outlier values */
+  const void* K_loc;           /* b x h_kv x w x d post-RoPE local-window keys */
+  const void* V_loc;           /* b x h_kv x w x d */
+  const void* V;               /* b x h_kv x s x d values (host if v_on_host) */
+  int v_on_host;
+} shadowkv_state_in;
+
+/* Builds a context from a given compressed state (no prefill).  Outlier ids
+ * are checked on the device; a bad id makes the call return
+ * SKV_ERR_DEVICE_CHECK.  Synchronizes `stream`. */
+skv_status shadowkv_load_state(const shadowkv_params* p, const shadowkv_state_in* st,
+                               void* stream, shadowkv_ctx** out);
+
+/*
+ * Algorithm 2 (Decoding), one token for every sequence.
+ *   q     : device, b x h_q x d, post-RoPE queries of the new token.
+ *   k_new : device, b x h_kv x d, post-RoPE key of the new token, or NULL.
+ *   v_new : device, b x h_kv x d, its value (NULL iff k_new is NULL).
+ *   out   : device, b x h_q x d, attention output.
+ * With k_new given, the token is appended to the local window first (at most
+ * max_new times; then SKV_ERR_STATE).  Step t (0-based) scores
+ * P = q L^T / sqrt(d) over the non-outlier chunks, forms S2 (group_reduce),
+ * selects the top-k chunks per KV head (ties to the lower index), rebuilds
+ * their keys as RoPE(Gather(A, I) B) at their token positions, takes their
+ * values from the GPU chunk cache (hits of the previous step) or from pinned
+ * host memory (misses, fetched on the side stream while the keys are
+ * rebuilt), and writes softmax(q K^T / sqrt(d)) V over
+ * [outliers; rebuilt chunks; local window].  Asynchronous on `stream`.
+ */
+skv_status shadowkv_decode_step(shadowkv_ctx* ctx, const void* q, const void* k_new,
+                                const void* v_new, void* out, void* stream);
+
+/* Releases everything the context owns (NULL-safe).  Synchronizes the device. */
+void shadowkv_free(shadowkv_ctx* ctx);
+
+/* Text of the last failure of this thread ("" if none). */
+const char* shadowkv_last_error(void);
+
+/* ---------------------------------------------------------------- options */
+enum {
+  SKV_OPT_CACHE = 0,        /* 1 (default): reuse the previous step's chunks; 0: fetch all k */
+  SKV_OPT_TIMING = 1,       /* 1: time each kernel with CUDA events on its stream */
+  SKV_OPT_SPLIT_TOKENS = 2  /* tokens per attention split (multiple of 32, 64..1024; default 256) */
+};
+skv_status shadowkv_set_option(shadowkv_ctx* ctx, int option, long long value);
+
+/* Synchronizes the context's streams and reads the cumulative counters. */
+skv_status shadowkv_get_stats(shadowkv_ctx* ctx, shadowkv_stats* out);
+
+/* Synchronizes and reads the device status word (kernel bounds checks);
+ * SKV_ERR_DEVICE_CHECK if any kernel recorded a violation. */
+skv_status shadowkv_check(shadowkv_ctx* ctx);
+
+/* ------------------------------------------------------ timing / counting */
+/* Kernels are numbered 0..shadowkv_num_kernels()-1 with stable names. */
+int shadowkv_num_kernels(void);
+const char* shadowkv_kernel_name(int id);
+/* With SKV_OPT_TIMING on: total milliseconds and launch count per kernel id
+ * since the last reset (arrays of n entries).  Synchronizes. */
+skv_status shadowkv_kernel_times(shadowkv_ctx* ctx, double* ms, long long* launches, int n);
+skv_status shadowkv_reset_timers(shadowkv_ctx* ctx);
+
+/* ---------------------------------------------------------- introspection */
+enum {
+  SKV_FIELD_A = 0,            /* dtype b x s x r */
+  SKV_FIELD_BT = 1,           /* dtype b x h_kv x d x r  (B transposed per head) */
+  SKV_FIELD_L = 2,            /* dtype b x h_kv x n x d */
+  SKV_FIELD_MIN_COS = 3,      /* f32 b x h_kv x n  (prefill only) */
+  SKV_FIELD_OUTLIER_IDS = 4,  /* i32 b x h_kv x o */
+  SKV_FIELD_K_OUT = 5,        /* dtype b x h_kv x (o c) x d */
+  SKV_FIELD_V_OUT = 6,        /* dtype b x h_kv x (o c) x d */
+  SKV_FIELD_K_LOC = 7,        /* dtype b x h_kv x (w + max_new) x d */
+  SKV_FIELD_V_LOC = 8,        /* dtype b x h_kv x (w + max_new) x d */
+  SKV_FIELD_SEL = 9,          /* i32 b x h_kv x k: last step's chunks, ascending */
+  SKV_FIELD_SEL_SLOT = 10,    /* i32 b x h_kv x k: cache slot holding each selected chunk */
+  SKV_FIELD_HITS = 11,        /* i32 b x h_kv: last step's cache hits */
+  SKV_FIELD_LOGITS = 12,      /* f32 b x h_q x n: last step's q.L/sqrt(d) (outliers included) */
+  SKV_FIELD_K_SPARSE = 13,    /* dtype b x h_kv x (k c) x d: last step's RoPE(Gather(A,I) B) */
+  SKV_FIELD_SLOT_CHUNK = 14,  /* i32 b x h_kv x k: chunk in each cache slot (-1 empty) */
+  SKV_FIELD_SLOT_V = 15,      /* dtype b x h_kv x k x c x d: cached values */
+  SKV_FIELD_V_CPU = 16,       /* dtype b x h_kv x s x d: the pinned host copy of V */
+  SKV_FIELD_SVD_BASIS = 17,   /* f32 b x r x (h_kv d): orthonormal rows spanning the rank-r
+                                 right singular subspace (prefill only) */
+  SKV_FIELD_COUNT = 18
+};
+/* Size in bytes of a field. Host-only. */
+skv_status shadowkv_field_bytes(const shadowkv_ctx* ctx, int field, size_t* bytes);
+/* Copies a field to host memory dst (bytes must equal the field size).
+ * Synchronizes the context's streams. */
+skv_status shadowkv_export(shadowkv_ctx* ctx, int field, void* dst, size_t bytes);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SHADOWKV_H */

@@ -1,0 +1,561 @@
+// C ABI of the ShadowKV library (include/shadowkv.h): parameter checks, the
+// per-context device arena and pinned host copy of V, the decode step's
+// stream/event choreography, per-kernel timing, and state export.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "internal.h"
+
+struct shadowkv_ctx {
+  skv::Ctx c;
+};
+
+namespace {
+
+thread_local std::string g_err;
+
+skv_status fail(skv_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return st;
+}
+
+skv_status cuda_fail(cudaError_t e, const char* what) {
+  if (e == cudaErrorMemoryAllocation)
+    return fail(SKV_ERR_OOM, "%s: %s", what, cudaGetErrorString(e));
+  return fail(SKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define CK(expr)                                      \
+  do {                                                \
+    cudaError_t e_ = (expr);                          \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #expr); \
+  } while (0)
+
+const char* kKernelNames[skv::K_NUM] = {
+    "score", "select", "fetch", "rebuild", "attention", "chunkstats",
+    "outliers", "gather", "gram", "gemm", "orth", "misc"};
+
+constexpr size_t kAlign = 256;
+size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// Byte sizes of every device buffer of a context, in allocation order.
+struct Sizes {
+  size_t A, Bt, L, K_out, V_out, K_loc, V_loc, slot_V, K_sparse;
+  size_t min_cos, logits, score_part, attn_part, basis, rope_tab;
+  size_t out_ids, out_mask, sel, sel_slot, slot_chunk, miss_chunk, miss_slot;
+  size_t miss_count, hits, attn_count, counters, status;
+  size_t total() const {
+    const size_t v[] = {A, Bt, L, K_out, V_out, K_loc, V_loc, slot_V, K_sparse, min_cos, logits,
+                        score_part, attn_part, basis, rope_tab, out_ids, out_mask, sel, sel_slot,
+                        slot_chunk, miss_chunk, miss_slot, miss_count, hits, attn_count, counters,
+                        status};
+    size_t t = 0;
+    for (size_t x : v) t += up(x);
+    return t;
+  }
+};
+
+int n_of(const shadowkv_params& p) { return (p.s - p.w) / p.c; }
+int max_splits_of(const shadowkv_params& p) {
+  const long long T = static_cast<long long>(p.o + p.k) * p.c + p.w + p.max_new;
+  return static_cast<int>((T + 63) / 64);
+}
+
+Sizes sizes_of(const shadowkv_params& p) {
+  const size_t E = p.dtype == SKV_DTYPE_BF16 ? 2 : 4;
+  const size_t b = p.b, h = p.h_kv, hq = p.h_q, d = p.d, s = p.s, r = p.r, c = p.c, k = p.k,
+               o = p.o, n = n_of(p);
+  const size_t cap = static_cast<size_t>(p.w) + p.max_new;
+  const size_t ntile = (n + 127) / 128, nw = (n + 31) / 32;
+  Sizes z{};
+  z.A = b * s * r * E;
+  z.Bt = b * h * d * r * E;
+  z.L = b * h * n * d * E;
+  z.K_out = z.V_out = b * h * o * c * d * E;
+  z.K_loc = z.V_loc = b * h * cap * d * E;
+  z.slot_V = z.K_sparse = b * h * k * c * d * E;
+  z.min_cos = b * h * n * 4;
+  z.logits = b * hq * n * 4;
+  z.score_part = b * hq * ntile * 8;
+  z.attn_part = b * hq * static_cast<size_t>(max_splits_of(p)) * (d + 2) * 4;
+  z.basis = b * r * h * d * 4;
+  z.rope_tab = d / 2 * 8;
+  z.out_ids = b * h * o * 4;
+  z.out_mask = b * h * nw * 4;
+  z.sel = z.sel_slot = z.slot_chunk = z.miss_chunk = z.miss_slot = b * h * k * 4;
+  z.miss_count = z.hits = z.attn_count = b * h * 4;
+  z.counters = 2 * 8;
+  z.status = 4;
+  return z;
+}
+
+skv_status validate(const shadowkv_params* p) {
+  if (!p) return fail(SKV_ERR_INVALID_ARG, "params is NULL");
+  const shadowkv_params& q = *p;
+  if (q.b < 1 || q.h_kv < 1 || q.h_q < 1) return fail(SKV_ERR_INVALID_ARG, "b, h_q, h_kv must be >= 1");
+  if (q.h_q % q.h_kv) return fail(SKV_ERR_INVALID_ARG, "h_q (%d) must be a multiple of h_kv (%d)", q.h_q, q.h_kv);
+  const int G = q.h_q / q.h_kv;
+  if (G != 1 && G != 2 && G != 4 && G != 8)
+    return fail(SKV_ERR_UNSUPPORTED, "h_q / h_kv = %d: supported group sizes are 1, 2, 4, 8", G);
+  if (q.d != 64 && q.d != 128) return fail(SKV_ERR_UNSUPPORTED, "d = %d: supported head dims are 64, 128", q.d);
+  if (q.c < 1) return fail(SKV_ERR_INVALID_ARG, "chunk size c must be >= 1");
+  if (q.w < 0 || q.s <= q.w) return fail(SKV_ERR_INVALID_ARG, "need 0 <= w < s (w=%d, s=%d)", q.w, q.s);
+  if ((q.s - q.w) % q.c)
+    return fail(SKV_ERR_INVALID_ARG, "s - w = %d is not a multiple of c = %d", q.s - q.w, q.c);
+  const int n = n_of(q);
+  if (q.o < 0 || q.o >= n) return fail(SKV_ERR_INVALID_ARG, "need 0 <= o < n (o=%d, n=%d)", q.o, n);
+  if (q.k < 1 || q.k > n - q.o) return fail(SKV_ERR_INVALID_ARG, "need 1 <= k <= n - o (k=%d, n-o=%d)", q.k, n - q.o);
+  if (q.k > 1024) return fail(SKV_ERR_UNSUPPORTED, "k = %d > 1024 chunks per head", q.k);
+  if (q.r < 1 || q.r > std::min(q.s, q.h_kv * q.d))
+    return fail(SKV_ERR_INVALID_ARG, "need 1 <= r <= min(s, h_kv*d) (r=%d)", q.r);
+  if (q.r > 256) return fail(SKV_ERR_UNSUPPORTED, "r = %d > 256", q.r);
+  if (q.max_new < 0) return fail(SKV_ERR_INVALID_ARG, "max_new must be >= 0");
+  if (static_cast<long long>(q.s) + q.max_new >= (1LL << 24))
+    return fail(SKV_ERR_UNSUPPORTED, "s + max_new must be < 2^24 (fp32-exact positions)");
+  if (q.dtype != SKV_DTYPE_F32 && q.dtype != SKV_DTYPE_BF16) return fail(SKV_ERR_INVALID_ARG, "bad dtype %d", q.dtype);
+  if (q.group_reduce != SKV_GROUP_MAX && q.group_reduce != SKV_GROUP_SUM)
+    return fail(SKV_ERR_INVALID_ARG, "bad group_reduce %d", q.group_reduce);
+  if (q.svd_iters < 0 || q.svd_iters > 64) return fail(SKV_ERR_INVALID_ARG, "svd_iters must be in [0, 64]");
+  if (q.reserved != 0) return fail(SKV_ERR_INVALID_ARG, "reserved must be 0");
+  if (!(q.rope_theta > 0.f) || !std::isfinite(q.rope_theta)) return fail(SKV_ERR_INVALID_ARG, "rope_theta must be > 0");
+  if (skv::select_smem_bytes(n, q.k, G) > 220 * 1024)
+    return fail(SKV_ERR_UNSUPPORTED, "n = %d chunks per head exceeds the selection's shared memory", n);
+  return SKV_OK;
+}
+
+// Copies host memory with several threads (pageable -> pinned).
+void parallel_memcpy(void* dst, const void* src, size_t bytes) {
+  const size_t chunk = size_t(64) << 20;
+  if (bytes <= chunk) { std::memcpy(dst, src, bytes); return; }
+  unsigned nt = std::max(1u, std::min(16u, std::thread::hardware_concurrency()));
+  std::vector<std::thread> th;
+  for (unsigned t = 0; t < nt; ++t) {
+    th.emplace_back([=] {
+      const size_t per = (bytes + nt - 1) / nt;
+      const size_t a = per * t, b = std::min(bytes, a + per);
+      if (a < b) std::memcpy(static_cast<char*>(dst) + a, static_cast<const char*>(src) + a, b - a);
+    });
+  }
+  for (auto& x : th) x.join();
+}
+
+void destroy(shadowkv_ctx* h) {
+  if (!h) return;
+  skv::Ctx& c = h->c;
+  cudaSetDevice(c.device);
+  cudaDeviceSynchronize();
+  for (auto& t : c.pending) { cudaEventDestroy(t.a); cudaEventDestroy(t.b); }
+  if (c.open.a) cudaEventDestroy(c.open.a);
+  for (auto e : c.ev_free) cudaEventDestroy(e);
+  if (c.ev_fork) cudaEventDestroy(c.ev_fork);
+  if (c.ev_join) cudaEventDestroy(c.ev_join);
+  if (c.side) cudaStreamDestroy(c.side);
+  if (c.arena) cudaFree(c.arena);
+  if (c.v_cpu) cudaFreeHost(c.v_cpu);
+  delete h;
+}
+
+// Allocates and initialises a context for params p (already validated).
+skv_status create(const shadowkv_params* p, cudaStream_t st, shadowkv_ctx** out) {
+  shadowkv_ctx* h = new (std::nothrow) shadowkv_ctx();
+  if (!h) return fail(SKV_ERR_OOM, "host allocation of the context failed");
+  skv::Ctx& c = h->c;
+  c.p = *p;
+  c.E = p->dtype == SKV_DTYPE_BF16 ? 2 : 4;
+  c.n = n_of(*p);
+  c.G = p->h_q / p->h_kv;
+  c.ntile = (c.n + 127) / 128;
+  c.loc_cap = p->w + p->max_new;
+  c.max_splits = max_splits_of(*p);
+  c.split_tokens = 256;
+  auto bail = [&](skv_status s) { destroy(h); return s; };
+  cudaError_t e = cudaGetDevice(&c.device);
+  if (e != cudaSuccess) return bail(cuda_fail(e, "cudaGetDevice"));
+  e = cudaDeviceGetAttribute(&c.nsm, cudaDevAttrMultiProcessorCount, c.device);
+  if (e != cudaSuccess) return bail(cuda_fail(e, "cudaDeviceGetAttribute"));
+
+  const Sizes z = sizes_of(*p);
+  c.arena_bytes = z.total();
+  e = cudaMalloc(reinterpret_cast<void**>(&c.arena), c.arena_bytes);
+  if (e != cudaSuccess) return bail(cuda_fail(e, "cudaMalloc(context arena)"));
+  char* cur = c.arena;
+  auto take = [&](size_t bytes) { char* q = cur; cur += up(bytes); return static_cast<void*>(q); };
+  c.A = take(z.A); c.Bt = take(z.Bt); c.L = take(z.L);
+  c.K_out = take(z.K_out); c.V_out = take(z.V_out);
+  c.K_loc = take(z.K_loc); c.V_loc = take(z.V_loc);
+  c.slot_V = take(z.slot_V); c.K_sparse = take(z.K_sparse);
+  c.min_cos = static_cast<float*>(take(z.min_cos));
+  c.logits = static_cast<float*>(take(z.logits));
+  c.score_part = static_cast<float2*>(take(z.score_part));
+  c.attn_part = static_cast<float*>(take(z.attn_part));
+  c.basis = static_cast<float*>(take(z.basis));
+  c.rope_tab = static_cast<float2*>(take(z.rope_tab));
+  c.out_ids = static_cast<int32_t*>(take(z.out_ids));
+  c.out_mask = static_cast<uint32_t*>(take(z.out_mask));
+  c.sel = static_cast<int32_t*>(take(z.sel));
+  c.sel_slot = static_cast<int32_t*>(take(z.sel_slot));
+  c.slot_chunk = static_cast<int32_t*>(take(z.slot_chunk));
+  c.miss_chunk = static_cast<int32_t*>(take(z.miss_chunk));
+  c.miss_slot = static_cast<int32_t*>(take(z.miss_slot));
+  c.miss_count = static_cast<int32_t*>(take(z.miss_count));
+  c.hits = static_cast<int32_t*>(take(z.hits));
+  c.attn_count = static_cast<int32_t*>(take(z.attn_count));
+  c.counters = static_cast<unsigned long long*>(take(z.counters));
+  c.status = static_cast<int*>(take(z.status));
+
+  // small state: zeroed; the cache starts empty
+  const size_t small0 = static_cast<size_t>(reinterpret_cast<char*>(c.out_ids) - c.arena);
+  e = cudaMemsetAsync(c.arena + small0, 0, c.arena_bytes - small0, st);
+  if (e != cudaSuccess) return bail(cuda_fail(e, "cudaMemsetAsync"));
+  e = skv::launch_fill_i32(c, c.slot_chunk, -1, z.slot_chunk / 4, st);
+  if (e != cudaSuccess) return bail(cuda_fail(e, "fill slot table"));
+
+  // RoPE frequency table: inv_freq_i / (2 pi) as an fp32 (hi, lo) pair
+  std::vector<float2> tab(p->d / 2);
+  for (int i = 0; i < p->d / 2; ++i) {
+    const double f = std::pow(static_cast<double>(p->rope_theta), -2.0 * i / p->d) / (2.0 * M_PI);
+    const float hi = static_cast<float>(f);
+    tab[i] = make_float2(hi, static_cast<float>(f - static_cast<double>(hi)));
+  }
+  e = cudaMemcpyAsync(c.rope_tab, tab.data(), z.rope_tab, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return bail(cuda_fail(e, "upload RoPE table"));
+
+  // pinned, mapped host copy of V
+  c.v_bytes = static_cast<size_t>(p->b) * p->h_kv * p->s * p->d * c.E;
+  e = cudaHostAlloc(&c.v_cpu, c.v_bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+  if (e != cudaSuccess) { c.v_cpu = nullptr; return bail(cuda_fail(e, "cudaHostAlloc(V)")); }
+  e = cudaHostGetDevicePointer(&c.v_cpu_dev, c.v_cpu, 0);
+  if (e != cudaSuccess) return bail(cuda_fail(e, "cudaHostGetDevicePointer(V)"));
+
+  e = cudaStreamCreateWithFlags(&c.side, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return bail(cuda_fail(e, "create side stream"));
+  e = cudaEventCreateWithFlags(&c.ev_fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c.ev_join, cudaEventDisableTiming);
+  if (e != cudaSuccess) return bail(cuda_fail(e, "create events"));
+  *out = h;
+  return SKV_OK;
+}
+
+skv_status read_status(skv::Ctx& c) {
+  int st = 0;
+  CK(cudaMemcpy(&st, c.status, sizeof(int), cudaMemcpyDeviceToHost));
+  if (st != 0) return fail(SKV_ERR_DEVICE_CHECK, "a kernel reported an out-of-range index (code %d)", st);
+  return SKV_OK;
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    int now = -1;
+    if (prev >= 0 && cudaGetDevice(&now) == cudaSuccess && now != prev) cudaSetDevice(prev);
+  }
+};
+
+}  // namespace
+
+// ------------------------------------------------------------- hooks
+namespace skv {
+int num_sms(const Ctx& c) { return c.nsm; }
+
+static cudaEvent_t pop_event(Ctx& c) {
+  if (!c.ev_free.empty()) {
+    cudaEvent_t e = c.ev_free.back();
+    c.ev_free.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+void kbegin(Ctx& c, int kid, cudaStream_t st) {
+  ++c.launches;
+  if (!c.timing_on) return;
+  c.open.kid = kid;
+  c.open.a = pop_event(c);
+  if (c.open.a) cudaEventRecord(c.open.a, st);
+}
+
+void kend(Ctx& c, int kid, cudaStream_t st) {
+  if (!c.timing_on || !c.open.a || c.open.kid != kid) return;
+  c.open.b = pop_event(c);
+  if (c.open.b) {
+    cudaEventRecord(c.open.b, st);
+    c.pending.push_back(c.open);
+  } else {
+    c.ev_free.push_back(c.open.a);
+  }
+  c.open = Timed{-1, nullptr, nullptr};
+}
+}  // namespace skv
+
+static void drain_timers(skv::Ctx& c) {
+  for (auto& t : c.pending) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(t.b) == cudaSuccess && cudaEventElapsedTime(&ms, t.a, t.b) == cudaSuccess) {
+      c.kms[t.kid] += ms;
+      c.kcount[t.kid] += 1;
+    }
+    c.ev_free.push_back(t.a);
+    c.ev_free.push_back(t.b);
+  }
+  c.pending.clear();
+}
+
+// ============================================================== C ABI
+extern "C" {
+
+const char* shadowkv_last_error(void) { return g_err.c_str(); }
+
+skv_status shadowkv_validate_params(const shadowkv_params* p) { return validate(p); }
+
+skv_status shadowkv_footprint(const shadowkv_params* p, size_t* device_bytes, size_t* host_bytes) {
+  skv_status s = validate(p);
+  if (s != SKV_OK) return s;
+  if (!device_bytes || !host_bytes) return fail(SKV_ERR_INVALID_ARG, "NULL output pointer");
+  *device_bytes = sizes_of(*p).total();
+  *host_bytes = static_cast<size_t>(p->b) * p->h_kv * p->s * p->d * (p->dtype == SKV_DTYPE_BF16 ? 2 : 4);
+  return SKV_OK;
+}
+
+skv_status shadowkv_prefill(const shadowkv_params* p, const void* k_pre, const void* v,
+                            int v_on_host, void* stream, shadowkv_ctx** out) {
+  if (!out) return fail(SKV_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  skv_status s = validate(p);
+  if (s != SKV_OK) return s;
+  if (!k_pre || !v) return fail(SKV_ERR_INVALID_ARG, "k_pre and v must be non-NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  shadowkv_ctx* h = nullptr;
+  s = create(p, st, &h);
+  if (s != SKV_OK) return s;
+  skv::Ctx& c = h->c;
+  const void* v_src = v;
+  cudaError_t e = cudaSuccess;
+  if (v_on_host) {
+    parallel_memcpy(c.v_cpu, v, c.v_bytes);
+    v_src = c.v_cpu_dev;
+  } else {
+    e = cudaMemcpyAsync(c.v_cpu, v, c.v_bytes, cudaMemcpyDeviceToHost, st);
+  }
+  if (e == cudaSuccess) e = skv::prefill_device(c, k_pre, v_src, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) { s = cuda_fail(e, "prefill"); destroy(h); return s; }
+  s = read_status(c);
+  if (s != SKV_OK) { destroy(h); return s; }
+  c.has_min_cos = c.has_basis = true;
+  *out = h;
+  return SKV_OK;
+}
+
+skv_status shadowkv_load_state(const shadowkv_params* p, const shadowkv_state_in* in, void* stream,
+                               shadowkv_ctx** out) {
+  if (!out) return fail(SKV_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  skv_status s = validate(p);
+  if (s != SKV_OK) return s;
+  if (!in || !in->A || !in->B || !in->L || !in->V || (p->o > 0 && (!in->outlier_ids || !in->K_out || !in->V_out)) ||
+      (p->w > 0 && (!in->K_loc || !in->V_loc)))
+    return fail(SKV_ERR_INVALID_ARG, "a required state pointer is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  shadowkv_ctx* h = nullptr;
+  s = create(p, st, &h);
+  if (s != SKV_OK) return s;
+  skv::Ctx& c = h->c;
+  const Sizes z = sizes_of(*p);
+  const size_t E = c.E;
+  const size_t pairs = static_cast<size_t>(p->b) * p->h_kv;
+  cudaError_t e = cudaMemcpyAsync(c.A, in->A, z.A, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(c.L, in->L, z.L, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess && p->o > 0) e = cudaMemcpyAsync(c.out_ids, in->outlier_ids, z.out_ids, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess && p->o > 0) e = cudaMemcpyAsync(c.K_out, in->K_out, z.K_out, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess && p->o > 0) e = cudaMemcpyAsync(c.V_out, in->V_out, z.V_out, cudaMemcpyDeviceToDevice, st);
+  const size_t row = static_cast<size_t>(p->d) * E;
+  if (e == cudaSuccess && p->w > 0)
+    e = cudaMemcpy2DAsync(c.K_loc, row * c.loc_cap, in->K_loc, row * p->w, row * p->w, pairs,
+                          cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess && p->w > 0)
+    e = cudaMemcpy2DAsync(c.V_loc, row * c.loc_cap, in->V_loc, row * p->w, row * p->w, pairs,
+                          cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess) e = skv::launch_transpose_b(c, in->B, st);
+  if (e == cudaSuccess) e = skv::launch_build_mask(c, st);
+  if (e == cudaSuccess) {
+    if (in->v_on_host) parallel_memcpy(c.v_cpu, in->V, c.v_bytes);
+    else e = cudaMemcpyAsync(c.v_cpu, in->V, c.v_bytes, cudaMemcpyDeviceToHost, st);
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) { s = cuda_fail(e, "load_state"); destroy(h); return s; }
+  s = read_status(c);
+  if (s != SKV_OK) { destroy(h); return s; }
+  *out = h;
+  return SKV_OK;
+}
+
+skv_status shadowkv_decode_step(shadowkv_ctx* h, const void* q, const void* k_new, const void* v_new,
+                                void* out, void* stream) {
+  if (!h) return fail(SKV_ERR_INVALID_ARG, "ctx is NULL");
+  if (!q || !out) return fail(SKV_ERR_INVALID_ARG, "q and out must be non-NULL");
+  if ((k_new == nullptr) != (v_new == nullptr)) return fail(SKV_ERR_INVALID_ARG, "k_new and v_new must both be given or both NULL");
+  skv::Ctx& c = h->c;
+  if (k_new && c.n_app >= c.p.max_new)
+    return fail(SKV_ERR_STATE, "local window full: %d tokens appended (max_new)", c.n_app);
+  DeviceGuard g(c.device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int loc_row = c.p.w + c.n_app;
+  const int n_loc = loc_row + (k_new ? 1 : 0);
+  CK(skv::launch_score(c, q, st));
+  CK(skv::launch_select(c, k_new, v_new, loc_row, st));
+  CK(cudaEventRecord(c.ev_fork, st));
+  CK(cudaStreamWaitEvent(c.side, c.ev_fork, 0));
+  CK(skv::launch_fetch(c, c.side));
+  CK(cudaEventRecord(c.ev_join, c.side));
+  CK(skv::launch_rebuild(c, st));
+  CK(cudaStreamWaitEvent(st, c.ev_join, 0));
+  CK(skv::launch_attn(c, q, out, n_loc, st));
+  if (k_new) ++c.n_app;
+  ++c.t;
+  return SKV_OK;
+}
+
+void shadowkv_free(shadowkv_ctx* h) { destroy(h); }
+
+skv_status shadowkv_set_option(shadowkv_ctx* h, int option, long long value) {
+  if (!h) return fail(SKV_ERR_INVALID_ARG, "ctx is NULL");
+  skv::Ctx& c = h->c;
+  switch (option) {
+    case SKV_OPT_CACHE:
+      if (value != 0 && value != 1) return fail(SKV_ERR_INVALID_ARG, "cache option must be 0 or 1");
+      c.cache_on = value == 1;
+      return SKV_OK;
+    case SKV_OPT_TIMING:
+      if (value != 0 && value != 1) return fail(SKV_ERR_INVALID_ARG, "timing option must be 0 or 1");
+      c.timing_on = value == 1;
+      return SKV_OK;
+    case SKV_OPT_SPLIT_TOKENS: {
+      if (value < 64 || value > 1024 || value % 32) return fail(SKV_ERR_INVALID_ARG, "split tokens must be a multiple of 32 in [64, 1024]");
+      c.split_tokens = static_cast<int>(value);
+      return SKV_OK;
+    }
+    default:
+      return fail(SKV_ERR_INVALID_ARG, "unknown option %d", option);
+  }
+}
+
+skv_status shadowkv_get_stats(shadowkv_ctx* h, shadowkv_stats* out) {
+  if (!h || !out) return fail(SKV_ERR_INVALID_ARG, "NULL argument");
+  skv::Ctx& c = h->c;
+  DeviceGuard g(c.device);
+  CK(cudaDeviceSynchronize());
+  unsigned long long cnt[2] = {0, 0};
+  CK(cudaMemcpy(cnt, c.counters, sizeof(cnt), cudaMemcpyDeviceToHost));
+  out->steps = c.t;
+  out->hits = static_cast<long long>(cnt[0]);
+  out->misses = static_cast<long long>(cnt[1]);
+  out->link_bytes = out->misses * static_cast<long long>(c.p.c) * c.p.d * c.E;
+  out->launches = c.launches;
+  return SKV_OK;
+}
+
+skv_status shadowkv_check(shadowkv_ctx* h) {
+  if (!h) return fail(SKV_ERR_INVALID_ARG, "ctx is NULL");
+  DeviceGuard g(h->c.device);
+  CK(cudaDeviceSynchronize());
+  return read_status(h->c);
+}
+
+int shadowkv_num_kernels(void) { return skv::K_NUM; }
+
+const char* shadowkv_kernel_name(int id) {
+  return (id >= 0 && id < skv::K_NUM) ? kKernelNames[id] : "";
+}
+
+skv_status shadowkv_kernel_times(shadowkv_ctx* h, double* ms, long long* launches, int n) {
+  if (!h || n < 0 || (n > 0 && (!ms || !launches))) return fail(SKV_ERR_INVALID_ARG, "bad arguments");
+  skv::Ctx& c = h->c;
+  DeviceGuard g(c.device);
+  drain_timers(c);
+  for (int i = 0; i < n; ++i) {
+    ms[i] = i < skv::K_NUM ? c.kms[i] : 0.0;
+    launches[i] = i < skv::K_NUM ? c.kcount[i] : 0;
+  }
+  return SKV_OK;
+}
+
+skv_status shadowkv_reset_timers(shadowkv_ctx* h) {
+  if (!h) return fail(SKV_ERR_INVALID_ARG, "ctx is NULL");
+  skv::Ctx& c = h->c;
+  DeviceGuard g(c.device);
+  drain_timers(c);
+  for (int i = 0; i < skv::K_NUM; ++i) { c.kms[i] = 0.0; c.kcount[i] = 0; }
+  return SKV_OK;
+}
+
+static void* field_ptr(skv::Ctx& c, int field, size_t* bytes, bool* on_host) {
+  const Sizes z = sizes_of(c.p);
+  *on_host = false;
+  switch (field) {
+    case SKV_FIELD_A: *bytes = z.A; return c.A;
+    case SKV_FIELD_BT: *bytes = z.Bt; return c.Bt;
+    case SKV_FIELD_L: *bytes = z.L; return c.L;
+    case SKV_FIELD_MIN_COS: *bytes = z.min_cos; return c.has_min_cos ? c.min_cos : nullptr;
+    case SKV_FIELD_OUTLIER_IDS: *bytes = z.out_ids; return c.out_ids;
+    case SKV_FIELD_K_OUT: *bytes = z.K_out; return c.K_out;
+    case SKV_FIELD_V_OUT: *bytes = z.V_out; return c.V_out;
+    case SKV_FIELD_K_LOC: *bytes = z.K_loc; return c.K_loc;
+    case SKV_FIELD_V_LOC: *bytes = z.V_loc; return c.V_loc;
+    case SKV_FIELD_SEL: *bytes = z.sel; return c.sel;
+    case SKV_FIELD_SEL_SLOT: *bytes = z.sel_slot; return c.sel_slot;
+    case SKV_FIELD_HITS: *bytes = z.hits; return c.hits;
+    case SKV_FIELD_LOGITS: *bytes = z.logits; return c.logits;
+    case SKV_FIELD_K_SPARSE: *bytes = z.K_sparse; return c.K_sparse;
+    case SKV_FIELD_SLOT_CHUNK: *bytes = z.slot_chunk; return c.slot_chunk;
+    case SKV_FIELD_SLOT_V: *bytes = z.slot_V; return c.slot_V;
+    case SKV_FIELD_V_CPU: *bytes = c.v_bytes; *on_host = true; return c.v_cpu;
+    case SKV_FIELD_SVD_BASIS: *bytes = z.basis; return c.has_basis ? c.basis : nullptr;
+    default: *bytes = 0; return nullptr;
+  }
+}
+
+skv_status shadowkv_field_bytes(const shadowkv_ctx* h, int field, size_t* bytes) {
+  if (!h || !bytes) return fail(SKV_ERR_INVALID_ARG, "NULL argument");
+  if (field < 0 || field >= SKV_FIELD_COUNT) return fail(SKV_ERR_INVALID_ARG, "unknown field %d", field);
+  bool on_host;
+  field_ptr(const_cast<skv::Ctx&>(h->c), field, bytes, &on_host);
+  return SKV_OK;
+}
+
+skv_status shadowkv_export(shadowkv_ctx* h, int field, void* dst, size_t bytes) {
+  if (!h || !dst) return fail(SKV_ERR_INVALID_ARG, "NULL argument");
+  if (field < 0 || field >= SKV_FIELD_COUNT) return fail(SKV_ERR_INVALID_ARG, "unknown field %d", field);
+  skv::Ctx& c = h->c;
+  size_t want = 0;
+  bool on_host = false;
+  void* src = field_ptr(c, field, &want, &on_host);
+  if (!src) return fail(SKV_ERR_STATE, "field %d is not available for this context", field);
+  if (bytes != want) return fail(SKV_ERR_INVALID_ARG, "field %d has %zu bytes, got %zu", field, want, bytes);
+  DeviceGuard g(c.device);
+  CK(cudaDeviceSynchronize());
+  if (on_host) std::memcpy(dst, src, bytes);
+  else CK(cudaMemcpy(dst, src, bytes, cudaMemcpyDeviceToHost));
+  return SKV_OK;
+}
+
+}  // extern "C"

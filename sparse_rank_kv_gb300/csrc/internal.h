@@ -1,0 +1,109 @@
+// Host-side internals of the ShadowKV library: the context and the kernel
+// launchers each .cu file provides to the C ABI in api.cu.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stddef.h>
+#include <string>
+#include <vector>
+
+#include "../../include/shadowkv.h"
+
+namespace skv {
+
+// Kernel ids for timing and launch counting (names in api.cu).
+enum KernelId {
+  K_SCORE = 0,      // landmark scores P = q L^T / sqrt(d) and per-tile softmax stats
+  K_SELECT,         // S2, top-k, cache set difference, local-window append
+  K_FETCH,          // value misses from pinned host memory into cache slots
+  K_REBUILD,        // RoPE(Gather(A, I) B)
+  K_ATTN,           // split-KV attention + last-block combine
+  K_CHUNKSTATS,     // prefill: RoPE, chunk means, min cosine
+  K_OUTLIERS,       // prefill: ArgTopK(-min cos, o) + mask
+  K_GATHER,         // prefill: outlier / local-window rows
+  K_GRAM,           // prefill: Gram matrix partials
+  K_GEMM,           // prefill: basis products
+  K_ORTH,           // prefill: Gram-Schmidt orthonormalisation
+  K_MISC,           // prefill: reductions, transposes, fills
+  K_NUM
+};
+
+struct Timed {
+  int kid;
+  cudaEvent_t a, b;
+};
+
+struct Ctx {
+  shadowkv_params p{};
+  int device = 0;
+  int nsm = 148;      // SMs of the device
+  int E = 2;          // element bytes
+  int n = 0, G = 1;
+  int ntile = 0;      // score tiles per (b, h_kv)
+  int loc_cap = 0;    // w + max_new
+  int split_tokens = 256;
+  int max_splits = 0;
+  bool cache_on = true, timing_on = false;
+  long long t = 0;    // decode steps enqueued
+  int n_app = 0;      // tokens appended to the local window
+  long long launches = 0;
+  bool has_min_cos = false, has_basis = false;
+
+  // device arena
+  char* arena = nullptr;
+  size_t arena_bytes = 0;
+  void *A = nullptr, *Bt = nullptr, *L = nullptr, *K_out = nullptr, *V_out = nullptr;
+  void *K_loc = nullptr, *V_loc = nullptr, *slot_V = nullptr, *K_sparse = nullptr;
+  float *min_cos = nullptr, *logits = nullptr, *attn_part = nullptr, *basis = nullptr;
+  float2 *score_part = nullptr, *rope_tab = nullptr;
+  int32_t *out_ids = nullptr, *sel = nullptr, *sel_slot = nullptr, *slot_chunk = nullptr;
+  int32_t *miss_chunk = nullptr, *miss_slot = nullptr, *miss_count = nullptr, *hits = nullptr;
+  int32_t *attn_count = nullptr;
+  uint32_t* out_mask = nullptr;
+  unsigned long long* counters = nullptr;  // [0] hits, [1] misses
+  int* status = nullptr;
+
+  // pinned host copy of V (mapped)
+  void* v_cpu = nullptr;
+  void* v_cpu_dev = nullptr;
+  size_t v_bytes = 0;
+
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+
+  // timing
+  Timed open{-1, nullptr, nullptr};
+  std::vector<Timed> pending;
+  std::vector<cudaEvent_t> ev_free;
+  double kms[K_NUM] = {};
+  long long kcount[K_NUM] = {};
+};
+
+size_t select_smem_bytes(int n, int k, int G);
+size_t attn_smem_bytes(int G, int D, int S);
+
+// ------------------------------------------------------------ launch hooks
+// Every launcher brackets its kernel with kbegin/kend (api.cu): they count
+// the launch and, with timing on, record CUDA events on the launch stream.
+void kbegin(Ctx& c, int kid, cudaStream_t st);
+void kend(Ctx& c, int kid, cudaStream_t st);
+int num_sms(const Ctx& c);
+
+// ------------------------------------------------------------ launchers
+// decode_kernels.cu
+cudaError_t launch_score(Ctx& c, const void* q, cudaStream_t st);
+cudaError_t launch_select(Ctx& c, const void* k_new, const void* v_new, int loc_row,
+                          cudaStream_t st);
+cudaError_t launch_fetch(Ctx& c, cudaStream_t st);
+cudaError_t launch_attn(Ctx& c, const void* q, void* out, int n_loc, cudaStream_t st);
+cudaError_t launch_build_mask(Ctx& c, cudaStream_t st);
+// rebuild.cu
+cudaError_t launch_rebuild(Ctx& c, cudaStream_t st);
+// prefill_kernels.cu
+// Runs Algorithm 1 on the device.  v is a device pointer, or (v_mapped) the
+// mapped device address of pinned host memory.
+cudaError_t prefill_device(Ctx& c, const void* k_pre, const void* v, cudaStream_t st);
+cudaError_t launch_transpose_b(Ctx& c, const void* B, cudaStream_t st);
+cudaError_t launch_fill_i32(Ctx& c, int32_t* p, int32_t v, size_t n, cudaStream_t st);
+
+}  // namespace skv

@@ -1,0 +1,180 @@
+"""GPU decode path (Algorithm 2) against the CPU oracle, through the C ABI.
+
+Both sides consume the same seeded compressed state (synth.make_state): the
+library through shadowkv_load_state, the oracle directly.  Every step checks
+  a7  the landmark logits P = q L^T / sqrt(d),
+  a8  the selected chunks (tie-aware index rule),
+  a9  the cache hit counts (exact) and, through the output, the fetched values,
+  a10 the rebuilt keys RoPE(Gather(A, I) B),
+  a11 the attention output (per-head relative error bound),
+with the oracle's output computed on the GPU's selection once that selection
+has been shown to be a valid top-k of the oracle's scores.
+"""
+import numpy as np
+import pytest
+import torch
+
+from helpers import TOL, check_selection, head_errors, np64, oracle_state
+from oracle import shadowkv_oracle as O
+from sparse_rank_kv_gb300 import binding, build, synth
+from sparse_rank_kv_gb300.synth import CONFIGS
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+    binding.lib()
+
+
+SMALL = CONFIGS["llama_b1_s32k"].with_(
+    name="small", b=2, h_q=8, h_kv=2, d=128, s=8000 + 64, c=8, r=64, k=37, o=6, w=64,
+    theta=5e5, dtype="bf16", steps=6, seed=11)
+
+
+def run_parity(cfg, steps=None, group="max", cache=True, bsel=None, rows=True, append=True,
+               v_on_host=False, split=None):
+    st = synth.make_state(cfg, device="cuda")
+    if v_on_host:
+        st["v"] = st["v"].cpu()
+    p = binding.make_params(cfg, group_reduce=binding.GROUP_MAX if group == "max" else binding.GROUP_SUM)
+    ctx = binding.load_state(p, st)
+    if not cache:
+        ctx.set_option(binding.OPT_CACHE, 0)
+    if split:
+        ctx.set_option(binding.OPT_SPLIT_TOKENS, split)
+    sl = slice(None) if bsel is None else slice(bsel, bsel + 1)
+    dec = O.OracleDecoder(oracle_state(st, cfg, bsel), h_q=cfg.h_q, k=cfg.k, group_reduce=group)
+    b, h, hq, d, k, c, n = cfg.b, cfg.h_kv, cfg.h_q, cfg.d, cfg.k, cfg.c, cfg.n
+    dt = synth.torch_dtype(cfg.dtype)
+    T = cfg.steps if steps is None else steps
+    outs, worst = [], 0.0
+    for t in range(T):
+        q = st["q"][t].contiguous()
+        kn = st["k_new"][t].contiguous() if append else None
+        vn = st["v_new"][t].contiguous() if append else None
+        out = torch.empty(b, hq, d, dtype=dt, device="cuda")
+        ctx.decode_step(q, kn, vn, out)
+        torch.cuda.synchronize()
+        sel = ctx.export("SEL").view(b, h, k).numpy()[sl]
+        qn = np64(q[sl])
+        P, S2, _ = dec.scores(qn)
+        check_selection(sel, S2, k, what=f"step {t} selection")
+        res = dec.step(qn, np64(kn[sl]) if append else None, np64(vn[sl]) if append else None,
+                       force_sel=sel)
+        err = head_errors(np64(out[sl]), res.out)
+        worst = max(worst, float(err.max()))
+        assert err.max() <= TOL[cfg.dtype], f"step {t}: output error {err.max():.3g}"
+        hits = ctx.export("HITS").view(b, h).numpy()[sl]
+        assert np.array_equal(hits, res.hits), f"step {t}: hits {hits} vs {res.hits}"
+        if rows:
+            lg = ctx.export("LOGITS").view(b, hq, n).numpy()[sl].astype(np.float64)
+            m = ~np.isnan(res.P)
+            scale = np.abs(res.P[m]).max()
+            assert np.abs(lg[m] - res.P[m]).max() <= 2e-6 * scale + 1e-6, f"step {t}: logits"
+            ks = np64(ctx.export("K_SPARSE").view(b, h, k * c, d)[sl])
+            kref = res.K_sparse
+            tol = (1e-5 if cfg.dtype == "f32" else 8e-3) * np.abs(kref).max()
+            assert np.abs(ks - kref).max() <= tol, f"step {t}: rebuilt keys"
+        outs.append(out.clone())
+    ctx.check()
+    stats = ctx.stats()
+    return outs, ctx, stats, worst
+
+
+def test_tiny_fp32_all_steps():
+    _, _, stats, worst = run_parity(CONFIGS["tiny_f32_s1k"])
+    assert stats.steps == 4 and worst <= TOL["f32"]
+
+
+def test_small_bf16_ragged_tiles():
+    # n = 1000 (not a multiple of the 128-landmark score tile), k*c = 296 rows
+    # (not a multiple of the 64-row rebuild tile), ragged attention splits
+    run_parity(SMALL)
+
+
+@pytest.mark.parametrize("G", [1, 2, 8])
+def test_group_sizes(G):
+    run_parity(SMALL.with_(h_q=2 * G, seed=20 + G), steps=3)
+
+
+def test_head_dim_64_bf16():
+    run_parity(SMALL.with_(d=64, theta=1e4, seed=31), steps=3)
+
+
+def test_group_reduce_sum_reading():
+    run_parity(SMALL.with_(seed=32), steps=3, group="sum")
+
+
+def test_no_local_prompt_window_and_no_outliers():
+    run_parity(SMALL.with_(s=8000, w=0, o=0, seed=33), steps=3)
+
+
+def test_decode_without_appending():
+    run_parity(SMALL.with_(seed=34), steps=3, append=False)
+
+
+def test_k_one_and_k_all_candidates():
+    run_parity(SMALL.with_(k=1, seed=35), steps=3)
+    cfg = SMALL.with_(s=600 * 8 + 64, o=4, seed=36)
+    run_parity(cfg.with_(k=cfg.n - cfg.o), steps=3)
+
+
+def test_split_size_variants():
+    run_parity(SMALL.with_(seed=37), steps=2, split=64)
+    run_parity(SMALL.with_(seed=37), steps=2, split=1024)
+
+
+def test_values_from_host_memory():
+    run_parity(SMALL.with_(seed=38), steps=3, v_on_host=True)
+
+
+def test_cache_is_lossless_bit_identical():
+    """The set-difference cache changes only what crosses the host link: the
+    outputs with the cache on and forced off are bit-identical."""
+    cfg = SMALL.with_(steps=8, seed=39)
+    on, _, st_on, _ = run_parity(cfg, rows=False)
+    off, _, st_off, _ = run_parity(cfg, cache=False, rows=False)
+    for a, b in zip(on, off):
+        assert torch.equal(a, b)
+    assert st_off.hits == 0 and st_off.misses == cfg.steps * cfg.b * cfg.h_kv * cfg.k
+    assert st_on.hits > 0 and st_on.hits + st_on.misses == st_off.misses
+
+
+def test_full_size_32k():
+    run_parity(CONFIGS["llama_b1_s32k"])
+
+
+@pytest.mark.parametrize("name,bsel,steps", [
+    ("llama_b8_s128k", 5, 6),
+    ("llama_b48_s60k", 37, 4),
+    ("llama_b2_s256k", 1, 5),
+])
+def test_full_size_sampled_sequence(name, bsel, steps):
+    """The full-size workloads in the benchmark's launch configuration; the
+    oracle recomputes one sequence of the batch."""
+    run_parity(CONFIGS[name], steps=steps, bsel=bsel, rows=False)
+
+
+def test_max_new_is_enforced():
+    cfg = SMALL.with_(steps=2, seed=40)
+    st = synth.make_state(cfg, device="cuda")
+    ctx = binding.load_state(binding.make_params(cfg), st)
+    out = torch.empty(cfg.b, cfg.h_q, cfg.d, dtype=torch.bfloat16, device="cuda")
+    for t in range(2):
+        ctx.decode_step(st["q"][t], st["k_new"][t], st["v_new"][t], out)
+    with pytest.raises(binding.ShadowKVError) as ei:
+        ctx.decode_step(st["q"][0], st["k_new"][0], st["v_new"][0], out)
+    assert ei.value.code == 6
+    ctx.decode_step(st["q"][0], None, None, out)   # no append: still fine
+    ctx.check()
+
+
+def test_bad_outlier_ids_are_reported():
+    cfg = SMALL.with_(seed=41)
+    st = synth.make_state(cfg, device="cuda")
+    st["outlier_ids"][0, 0, 1] = st["outlier_ids"][0, 0, 0]   # duplicate
+    with pytest.raises(binding.ShadowKVError) as ei:
+        binding.load_state(binding.make_params(cfg), st)
+    assert ei.value.code == 4
