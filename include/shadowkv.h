@@ -160,6 +160,12 @@ skv_status shadowkv_load_state(const shadowkv_params* p, const shadowkv_state_in
 skv_status shadowkv_decode_step(shadowkv_ctx* ctx, const void* q, const void* k_new,
                                 const void* v_new, void* out, void* stream);
 
+/* Returns the context to its state right after prefill / load_state: the
+ * appended tokens are dropped (the local window holds the w prompt tokens
+ * again) and the chunk cache is emptied.  Stream-ordered on `stream` after
+ * every earlier decode step of this context. */
+skv_status shadowkv_rewind(shadowkv_ctx* ctx, void* stream);
+
 /* Releases everything the context owns (NULL-safe).  Synchronizes the device. */
 void shadowkv_free(shadowkv_ctx* ctx);
 
@@ -170,7 +176,10 @@ const char* shadowkv_last_error(void);
 enum {
   SKV_OPT_CACHE = 0,        /* 1 (default): reuse the previous step's chunks; 0: fetch all k */
   SKV_OPT_TIMING = 1,       /* 1: time each kernel with CUDA events on its stream */
-  SKV_OPT_SPLIT_TOKENS = 2  /* tokens per attention split (multiple of 32, 64..1024; default 256) */
+  SKV_OPT_SPLIT_TOKENS = 2, /* tokens per attention split (multiple of 32, 64..1024; default 256) */
+  SKV_OPT_SIMT_REBUILD = 3  /* 1: rebuild keys with the CUDA-core kernel even where the tensor-core
+                               (tcgen05) kernel applies (bf16, c a multiple of 8 dividing 128,
+                               r a multiple of 8); for cross-checking the two */
 };
 skv_status shadowkv_set_option(shadowkv_ctx* ctx, int option, long long value);
 

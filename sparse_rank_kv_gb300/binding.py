@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libshadowkv.so")
 
 DTYPE_F32, DTYPE_BF16 = 0, 1
 GROUP_MAX, GROUP_SUM = 0, 1
-OPT_CACHE, OPT_TIMING, OPT_SPLIT_TOKENS = 0, 1, 2
+OPT_CACHE, OPT_TIMING, OPT_SPLIT_TOKENS, OPT_SIMT_REBUILD = 0, 1, 2, 3
 
 FIELDS = {
     "A": 0, "BT": 1, "L": 2, "MIN_COS": 3, "OUTLIER_IDS": 4, "K_OUT": 5, "V_OUT": 6,
@@ -82,6 +82,7 @@ def lib() -> ctypes.CDLL:
             "shadowkv_load_state": (I, [P(Params), P(StateIn), V, P(V)]),
             "shadowkv_decode_step": (I, [V, V, V, V, V, V]),
             "shadowkv_free": (None, [V]),
+            "shadowkv_rewind": (I, [V, V]),
             "shadowkv_last_error": (ctypes.c_char_p, []),
             "shadowkv_set_option": (I, [V, I, ctypes.c_longlong]),
             "shadowkv_get_stats": (I, [V, P(Stats)]),
@@ -177,6 +178,9 @@ class Context:
     def decode_step(self, q, k_new, v_new, out, stream=None):
         _check(lib().shadowkv_decode_step(self._h, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out),
                                           _stream(stream)))
+
+    def rewind(self, stream=None):
+        _check(lib().shadowkv_rewind(self._h, _stream(stream)))
 
     def set_option(self, option: int, value: int):
         _check(lib().shadowkv_set_option(self._h, option, value))

@@ -47,7 +47,7 @@ skv_status cuda_fail(cudaError_t e, const char* what) {
 
 const char* kKernelNames[skv::K_NUM] = {
     "score", "select", "fetch", "rebuild", "attention", "chunkstats",
-    "outliers", "gather", "gram", "gemm", "orth", "misc"};
+    "outliers", "gather", "svd_mx", "svd_ztm", "orth", "misc"};
 
 constexpr size_t kAlign = 256;
 size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -240,6 +240,9 @@ skv_status create(const shadowkv_params* p, cudaStream_t st, shadowkv_ctx** out)
   if (e != cudaSuccess) { c.v_cpu = nullptr; return bail(cuda_fail(e, "cudaHostAlloc(V)")); }
   e = cudaHostGetDevicePointer(&c.v_cpu_dev, c.v_cpu, 0);
   if (e != cudaSuccess) return bail(cuda_fail(e, "cudaHostGetDevicePointer(V)"));
+
+  e = skv::make_rebuild_maps(c);
+  if (e != cudaSuccess) return bail(cuda_fail(e, "encode TMA descriptors"));
 
   e = cudaStreamCreateWithFlags(&c.side, cudaStreamNonBlocking);
   if (e != cudaSuccess) return bail(cuda_fail(e, "create side stream"));
@@ -435,6 +438,17 @@ skv_status shadowkv_decode_step(shadowkv_ctx* h, const void* q, const void* k_ne
   return SKV_OK;
 }
 
+skv_status shadowkv_rewind(shadowkv_ctx* h, void* stream) {
+  if (!h) return fail(SKV_ERR_INVALID_ARG, "ctx is NULL");
+  skv::Ctx& c = h->c;
+  DeviceGuard g(c.device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  CK(cudaStreamWaitEvent(st, c.ev_join, 0));   // the last fetch on the side stream
+  CK(skv::launch_fill_i32(c, c.slot_chunk, -1, static_cast<size_t>(c.p.b) * c.p.h_kv * c.p.k, st));
+  c.n_app = 0;
+  return SKV_OK;
+}
+
 void shadowkv_free(shadowkv_ctx* h) { destroy(h); }
 
 skv_status shadowkv_set_option(shadowkv_ctx* h, int option, long long value) {
@@ -454,6 +468,10 @@ skv_status shadowkv_set_option(shadowkv_ctx* h, int option, long long value) {
       c.split_tokens = static_cast<int>(value);
       return SKV_OK;
     }
+    case SKV_OPT_SIMT_REBUILD:
+      if (value != 0 && value != 1) return fail(SKV_ERR_INVALID_ARG, "option must be 0 or 1");
+      c.force_simt = value == 1;
+      return SKV_OK;
     default:
       return fail(SKV_ERR_INVALID_ARG, "unknown option %d", option);
   }

@@ -16,7 +16,12 @@ enum : int {
   DEV_BAD_SLOT = 2,
   DEV_BAD_OUTLIER = 3,
   DEV_BAD_COUNT = 4,
+  DEV_TIMEOUT = 5,      // a bounded mbarrier wait gave up
 };
+
+// Polls of a bounded mbarrier wait before a kernel gives up (each poll
+// suspends for a hardware-chosen interval; the total is well above a second).
+constexpr uint32_t kWaitLimit = 1u << 26;
 
 __device__ __forceinline__ void flag_error(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
@@ -72,6 +77,17 @@ __device__ __forceinline__ void rope_sincos(int pos, float2 f, float* sn, float*
   const float frac = prod - rintf(prod);
   const float turns = frac + (err + p * f.y);
   sincospif(2.0f * turns, sn, cs);
+}
+
+// Same angle, evaluated with the hardware sine/cosine on the reduced angle in
+// [-pi, pi] (absolute error about 4e-7): the form used by hot epilogues.
+__device__ __forceinline__ void rope_sincos_fast(int pos, float2 f, float* sn, float* cs) {
+  const float p = static_cast<float>(pos);
+  const float prod = p * f.x;
+  const float err = fmaf(p, f.x, -prod);
+  const float frac = prod - rintf(prod);
+  const float turns = frac + (err + p * f.y);
+  __sincosf(turns * 6.283185307179586f, sn, cs);
 }
 
 // ------------------------------------------------------------ reductions

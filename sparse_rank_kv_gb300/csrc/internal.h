@@ -1,6 +1,7 @@
 // Host-side internals of the ShadowKV library: the context and the kernel
 // launchers each .cu file provides to the C ABI in api.cu.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stddef.h>
@@ -21,8 +22,8 @@ enum KernelId {
   K_CHUNKSTATS,     // prefill: RoPE, chunk means, min cosine
   K_OUTLIERS,       // prefill: ArgTopK(-min cos, o) + mask
   K_GATHER,         // prefill: outlier / local-window rows
-  K_GRAM,           // prefill: Gram matrix partials
-  K_GEMM,           // prefill: basis products
+  K_GRAM,           // prefill: M X^T products (range and A)
+  K_GEMM,           // prefill: (M X^T)^T M split-K partials
   K_ORTH,           // prefill: Gram-Schmidt orthonormalisation
   K_MISC,           // prefill: reductions, transposes, fills
   K_NUM
@@ -68,6 +69,11 @@ struct Ctx {
   void* v_cpu_dev = nullptr;
   size_t v_bytes = 0;
 
+  // tensor-core rebuild: TMA descriptors of A (b*s x r) and B^T (b*h_kv*d x r)
+  CUtensorMap mapA{}, mapBt{};
+  bool tc_rebuild = false;      // shapes and dtype allow the tcgen05 kernel
+  bool force_simt = false;      // test hook: use the CUDA-core kernel anyway
+
   cudaStream_t side = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
 
@@ -99,6 +105,8 @@ cudaError_t launch_attn(Ctx& c, const void* q, void* out, int n_loc, cudaStream_
 cudaError_t launch_build_mask(Ctx& c, cudaStream_t st);
 // rebuild.cu
 cudaError_t launch_rebuild(Ctx& c, cudaStream_t st);
+bool tc_rebuild_supported(const shadowkv_params& p);
+cudaError_t make_rebuild_maps(Ctx& c);   // encodes mapA / mapBt
 // prefill_kernels.cu
 // Runs Algorithm 1 on the device.  v is a device pointer, or (v_mapped) the
 // mapped device address of pinned host memory.

@@ -6,12 +6,13 @@
 //   k_gather_rows    post-RoPE keys and values of the outlier chunks and of
 //                    the local window, kept exactly on the GPU (step 5)
 //   SVD (step 1)     rank-r right singular subspace of each sequence's
-//                    s x (h_kv d) pre-RoPE key matrix M: Gram G = M^T M,
-//                    subspace iteration on G from a seeded random basis,
-//                    one refinement pass on M itself (M^T (M X)) that undoes
-//                    the Gram's squared conditioning, then A = M X and
-//                    B = X^T split per KV head.  Since only the product A B
-//                    matters, X is any orthonormal basis of that subspace.
+//                    s x (h_kv d) pre-RoPE key matrix M by randomized
+//                    subspace iteration: a seeded Gaussian basis X, then
+//                    X <- orth((M X^T)^T M) a few times (M^T M applied one
+//                    factor at a time, so fp32 never sees its squared
+//                    condition number), then A = M X^T and B = X split per
+//                    KV head.  Only the product A B is unique, so X is any
+//                    orthonormal basis of that subspace.
 #include "common.cuh"
 #include "internal.h"
 
@@ -428,78 +429,60 @@ static cudaError_t prefill_svd(Ctx& c, const T* K, cudaStream_t st) {
   const int s = c.p.s, d = c.p.d, h = c.p.h_kv, r = c.p.r, D = h * d;
   const int dshift = d == 128 ? 7 : 6;
   const int nsm = num_sms(c);
-  const int tiles_sym = (D / 64) * (D / 64 + 1) / 2;
-  int nz_g = (4 * nsm + tiles_sym - 1) / tiles_sym;
-  nz_g = max(1, min(nz_g, s / 256));
   const int tiles_y = ((r + 63) / 64) * (D / 64);
   int nz_y = (4 * nsm + tiles_y - 1) / tiles_y;
   nz_y = max(1, min(nz_y, s / 256));
   const int iters = c.p.svd_iters > 0 ? c.p.svd_iters : 3;
 
-  // one sequence's workspace
-  const size_t n_gpart = static_cast<size_t>(nz_g) * D * D, n_g = static_cast<size_t>(D) * D;
+  // one sequence's workspace: basis X, next basis Y (r x D), Z = M X^T
+  // (s x r), and the split-K partials of Z^T M
   const size_t n_x = static_cast<size_t>(r) * D, n_z = static_cast<size_t>(s) * r;
   const size_t n_ypart = static_cast<size_t>(nz_y) * r * D;
   float* ws = nullptr;
-  SKV_TRY(cudaMalloc(&ws, sizeof(float) * (n_gpart + n_g + 2 * n_x + n_z + n_ypart)));
-  float* Gp = ws;
-  float* Gm = Gp + n_gpart;
-  float* X = Gm + n_g;
+  SKV_TRY(cudaMalloc(&ws, sizeof(float) * (2 * n_x + n_z + n_ypart)));
+  float* X = ws;
   float* Y = X + n_x;
   float* Z = Y + n_x;
   float* Yp = Z + n_z;
+  const int tper_y = ((s + nz_y - 1) / nz_y + 15) / 16 * 16;
   cudaError_t err = cudaSuccess;
   for (int bb = 0; bb < c.p.b && err == cudaSuccess; ++bb) {
     const HeadSplit<T> M{K + static_cast<size_t>(bb) * h * s * d, s, dshift};
-    const int tper_g = ((s + nz_g - 1) / nz_g + 15) / 16 * 16;
-    kbegin(c, K_GRAM, st);
-    k_gemm_tn<<<dim3(D / 64, D / 64, nz_g), 256, 0, st>>>(M, M, Gp, D, D, s, tper_g, D, n_g, 1);
-    kend(c, K_GRAM, st);
-    kbegin(c, K_MISC, st);
-    k_reduce_splits<<<grid_for(n_g, 256, 4096), 256, 0, st>>>(Gp, Gm, nz_g, D, D, n_g, 1);
-    kend(c, K_MISC, st);
     kbegin(c, K_MISC, st);
     k_random_basis<<<grid_for(n_x, 256, 1024), 256, 0, st>>>(X, r, D, c.p.seed, bb);
     kend(c, K_MISC, st);
     kbegin(c, K_ORTH, st);
     k_mgs<<<1, 1024, 0, st>>>(X, r, D, 2);
     kend(c, K_ORTH, st);
+    // subspace iteration on M^T M, one factor at a time: Y = (M X^T)^T M
     for (int it = 0; it < iters; ++it) {
-      kbegin(c, K_GEMM, st);   // Y = X G (rows of X times the symmetric G)
-      k_gemm_nt<<<dim3(D / 64, (r + 63) / 64), 256, 0, st>>>(RowF{X, D}, RowF{Gm, D}, Y, r, D, D, D);
+      kbegin(c, K_GRAM, st);
+      k_gemm_nt<<<dim3((r + 63) / 64, (s + 63) / 64), 256, 0, st>>>(M, RowF{X, D}, Z, s, r, D, r);
+      kend(c, K_GRAM, st);
+      kbegin(c, K_GEMM, st);
+      k_gemm_tn<<<dim3(D / 64, (r + 63) / 64, nz_y), 256, 0, st>>>(RowF{Z, r}, M, Yp, r, D, s,
+                                                                   tper_y, D, n_x, 0);
       kend(c, K_GEMM, st);
+      kbegin(c, K_MISC, st);
+      k_reduce_splits<<<grid_for(n_x, 256, 4096), 256, 0, st>>>(Yp, Y, nz_y, r, D, n_x, 0);
+      kend(c, K_MISC, st);
       kbegin(c, K_ORTH, st);
       k_mgs<<<1, 1024, 0, st>>>(Y, r, D, 2);
       kend(c, K_ORTH, st);
       float* t = X; X = Y; Y = t;
     }
-    // refinement on M: Y = (M X^T)^T M, i.e. X (M^T M) without forming G
-    kbegin(c, K_GEMM, st);
-    k_gemm_nt<<<dim3((r + 63) / 64, (s + 63) / 64), 256, 0, st>>>(M, RowF{X, D}, Z, s, r, D, r);
-    kend(c, K_GEMM, st);
-    const int tper_y = ((s + nz_y - 1) / nz_y + 15) / 16 * 16;
-    kbegin(c, K_GEMM, st);
-    k_gemm_tn<<<dim3(D / 64, (r + 63) / 64, nz_y), 256, 0, st>>>(RowF{Z, r}, M, Yp, r, D, s, tper_y, D,
-                                                                 n_x, 0);
-    kend(c, K_GEMM, st);
-    kbegin(c, K_MISC, st);
-    k_reduce_splits<<<grid_for(n_x, 256, 4096), 256, 0, st>>>(Yp, Y, nz_y, r, D, n_x, 0);
-    kend(c, K_MISC, st);
-    kbegin(c, K_ORTH, st);
-    k_mgs<<<1, 1024, 0, st>>>(Y, r, D, 2);
-    kend(c, K_ORTH, st);
     // A = M X^T, B^T per head, and the basis for export
-    kbegin(c, K_GEMM, st);
+    kbegin(c, K_GRAM, st);
     k_gemm_nt<<<dim3((r + 63) / 64, (s + 63) / 64), 256, 0, st>>>(
-        M, RowF{Y, D}, static_cast<T*>(c.A) + static_cast<size_t>(bb) * s * r, s, r, D, r);
-    kend(c, K_GEMM, st);
+        M, RowF{X, D}, static_cast<T*>(c.A) + static_cast<size_t>(bb) * s * r, s, r, D, r);
+    kend(c, K_GRAM, st);
     kbegin(c, K_MISC, st);
     k_basis_to_bt<T><<<grid_for(n_x, 256, 1024), 256, 0, st>>>(
-        Y, static_cast<T*>(c.Bt) + static_cast<size_t>(bb) * n_x, r, D);
+        X, static_cast<T*>(c.Bt) + static_cast<size_t>(bb) * n_x, r, D);
     kend(c, K_MISC, st);
     err = cudaGetLastError();
     if (err == cudaSuccess)
-      err = cudaMemcpyAsync(c.basis + static_cast<size_t>(bb) * n_x, Y, sizeof(float) * n_x,
+      err = cudaMemcpyAsync(c.basis + static_cast<size_t>(bb) * n_x, X, sizeof(float) * n_x,
                             cudaMemcpyDeviceToDevice, st);
   }
   cudaError_t e2 = cudaStreamSynchronize(st);
