@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libshadowkv.so")
 
 DTYPE_F32, DTYPE_BF16 = 0, 1
 GROUP_MAX, GROUP_SUM = 0, 1
-OPT_CACHE, OPT_TIMING, OPT_SPLIT_TOKENS, OPT_SIMT_REBUILD = 0, 1, 2, 3
+OPT_CACHE, OPT_TIMING, OPT_SPLIT_TOKENS, OPT_CUDA_CORES = 0, 1, 2, 3
 
 FIELDS = {
     "A": 0, "BT": 1, "L": 2, "MIN_COS": 3, "OUTLIER_IDS": 4, "K_OUT": 5, "V_OUT": 6,

@@ -72,7 +72,7 @@ struct Sizes {
 int n_of(const shadowkv_params& p) { return (p.s - p.w) / p.c; }
 int max_splits_of(const shadowkv_params& p) {
   const long long T = static_cast<long long>(p.o + p.k) * p.c + p.w + p.max_new;
-  return static_cast<int>((T + 63) / 64);
+  return static_cast<int>((T + 31) / 32);   // the smallest split is 32 tokens
 }
 
 Sizes sizes_of(const shadowkv_params& p) {
@@ -90,7 +90,7 @@ Sizes sizes_of(const shadowkv_params& p) {
   z.slot_V = z.K_sparse = b * h * k * c * d * E;
   z.min_cos = b * h * n * 4;
   z.logits = b * hq * n * 4;
-  z.score_part = b * hq * ntile * 8;
+  z.score_part = b * hq * ntile * 4 * 8;   // 4 softmax partials per 128-landmark tile
   z.attn_part = b * hq * static_cast<size_t>(max_splits_of(p)) * (d + 2) * 4;
   z.basis = b * r * h * d * 4;
   z.rope_tab = d / 2 * 8;
@@ -181,7 +181,7 @@ skv_status create(const shadowkv_params* p, cudaStream_t st, shadowkv_ctx** out)
   c.ntile = (c.n + 127) / 128;
   c.loc_cap = p->w + p->max_new;
   c.max_splits = max_splits_of(*p);
-  c.split_tokens = 256;
+  c.split_tokens = 128;
   auto bail = [&](skv_status s) { destroy(h); return s; };
   cudaError_t e = cudaGetDevice(&c.device);
   if (e != cudaSuccess) return bail(cuda_fail(e, "cudaGetDevice"));
@@ -242,6 +242,7 @@ skv_status create(const shadowkv_params* p, cudaStream_t st, shadowkv_ctx** out)
   if (e != cudaSuccess) return bail(cuda_fail(e, "cudaHostGetDevicePointer(V)"));
 
   e = skv::make_rebuild_maps(c);
+  if (e == cudaSuccess) e = skv::make_score_map(c);
   if (e != cudaSuccess) return bail(cuda_fail(e, "encode TMA descriptors"));
 
   e = cudaStreamCreateWithFlags(&c.side, cudaStreamNonBlocking);
@@ -464,11 +465,14 @@ skv_status shadowkv_set_option(shadowkv_ctx* h, int option, long long value) {
       c.timing_on = value == 1;
       return SKV_OK;
     case SKV_OPT_SPLIT_TOKENS: {
-      if (value < 64 || value > 1024 || value % 32) return fail(SKV_ERR_INVALID_ARG, "split tokens must be a multiple of 32 in [64, 1024]");
+      if (value < 32 || value > 256 || value % 32)
+        return fail(SKV_ERR_INVALID_ARG, "split tokens must be a multiple of 32 in [32, 256]");
+      if (skv::attn_smem_bytes(c.E, c.G, c.p.d, static_cast<int>(value)) > 227 * 1024)
+        return fail(SKV_ERR_UNSUPPORTED, "split of %lld tokens does not fit in shared memory", value);
       c.split_tokens = static_cast<int>(value);
       return SKV_OK;
     }
-    case SKV_OPT_SIMT_REBUILD:
+    case SKV_OPT_CUDA_CORES:
       if (value != 0 && value != 1) return fail(SKV_ERR_INVALID_ARG, "option must be 0 or 1");
       c.force_simt = value == 1;
       return SKV_OK;

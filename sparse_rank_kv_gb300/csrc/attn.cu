@@ -1,0 +1,274 @@
+// Sparse attention of ShadowKV's decode step (Algorithm 2 step 4):
+// out = softmax(q K^T / sqrt(d)) V over [outliers; RoPE(K_sparse); local],
+// split-KV over the token list with the G query heads of a KV head sharing
+// every K/V row.
+//
+// Block (pair, split) owns tokens [split*S, min(T, split*S + S)).  All its
+// K and V rows are copied to shared memory with cp.async at once (the copies
+// of one block are all in flight together); K rows are stored with their
+// 16-byte chunks XOR-swizzled by the row index so that the one-row-per-thread
+// dot products read shared memory without bank conflicts.  Logits and
+// probabilities stay in shared memory.  Each block writes a partial
+// (max, sum, sum p v) per head; the last block of the pair (atomic ticket)
+// combines the splits in split order, so the result does not depend on which
+// block finishes last.
+#include "common.cuh"
+#include "internal.h"
+
+namespace skv {
+
+constexpr int kAt = 256;   // threads per attention block
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
+               "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+template <typename T, int D>
+struct AttnLayout {
+  static constexpr int RB = D * static_cast<int>(sizeof(T));  // bytes per K/V row
+  static constexpr int NCH = RB / 16;                          // 16-byte chunks per row
+  static constexpr int V = 16 / static_cast<int>(sizeof(T));   // elements per chunk
+};
+
+size_t attn_smem_bytes(int E, int G, int D, int S) {
+  const size_t rb = static_cast<size_t>(D) * E;
+  const size_t pv = static_cast<size_t>(kAt / (D / 2)) * G * D;   // PV partial sums
+  const size_t kv = 2 * static_cast<size_t>(S) * rb;
+  return kv + sizeof(float) * (static_cast<size_t>(G) * D + static_cast<size_t>(G) * S) +
+         (pv * sizeof(float) > kv ? pv * sizeof(float) - kv : 0);
+}
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kAt)
+k_attn(const T* __restrict__ K_out, const T* __restrict__ V_out, const T* __restrict__ K_sp,
+       const T* __restrict__ slot_V, const int32_t* __restrict__ sel_slot,
+       const T* __restrict__ K_loc, const T* __restrict__ V_loc, const T* __restrict__ q,
+       T* __restrict__ out, float* __restrict__ part, int32_t* __restrict__ ticket, int n_out,
+       int n_sp, int n_loc, int loc_cap, int c, int k, int S, int nsplit, int max_splits,
+       float scale_log2) {
+  using Lay = AttnLayout<T, D>;
+  constexpr int RB = Lay::RB, NCH = Lay::NCH, V = Lay::V;
+  constexpr int NDP = D / 2;          // dimension pairs
+  constexpr int TG = kAt / NDP;       // token groups in P V
+  extern __shared__ __align__(16) unsigned char sm[];
+  unsigned char* Ks = sm;
+  unsigned char* Vs = sm + static_cast<size_t>(S) * RB;
+  float* qs = reinterpret_cast<float*>(Vs + static_cast<size_t>(S) * RB);
+  float* ps = qs + G * D;
+  float* pvred = reinterpret_cast<float*>(sm);   // reuses K/V after the logits
+  __shared__ float red[kAt / 32][G];
+  __shared__ float hm[G], hl[G];
+  __shared__ int last;
+
+  const int pair = blockIdx.x, split = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int T_all = n_out + n_sp + n_loc;
+  const int t0 = split * S, cnt = min(T_all, t0 + S) - t0;
+
+  // ---- copy the split's K and V rows to shared memory
+  for (int idx = tid; idx < cnt * NCH; idx += kAt) {
+    const int i = idx / NCH, ch = idx - i * NCH;
+    int t = t0 + i;
+    const T *kr, *vr;
+    if (t < n_out) {
+      kr = K_out + (static_cast<size_t>(pair) * n_out + t) * D;
+      vr = V_out + (static_cast<size_t>(pair) * n_out + t) * D;
+    } else if ((t -= n_out) < n_sp) {
+      kr = K_sp + (static_cast<size_t>(pair) * n_sp + t) * D;
+      const int slot = sel_slot[static_cast<size_t>(pair) * k + t / c];
+      vr = slot_V + ((static_cast<size_t>(pair) * k + slot) * c + (t % c)) * D;
+    } else {
+      t -= n_sp;
+      kr = K_loc + (static_cast<size_t>(pair) * loc_cap + t) * D;
+      vr = V_loc + (static_cast<size_t>(pair) * loc_cap + t) * D;
+    }
+    cp_async16(Ks + static_cast<size_t>(i) * RB + ((ch ^ (i & (NCH - 1))) << 4), kr + ch * V);
+    cp_async16(Vs + static_cast<size_t>(i) * RB + (ch << 4), vr + ch * V);
+  }
+  for (int i = tid; i < G * D; i += kAt)
+    qs[i] = Ty<T>::to_f(q[static_cast<size_t>(pair) * G * D + i]) * scale_log2;
+  cp_async_wait_all();
+  __syncthreads();
+
+  // ---- logits (log2 domain): two threads per token, one half of d each
+  float lmax[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) lmax[g] = -INFINITY;
+  const int hsel = tid & 1;
+  for (int i0 = 0; i0 < cnt; i0 += kAt / 2) {
+    const int i = i0 + (tid >> 1);
+    float acc[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) acc[g] = 0.f;
+    if (i < cnt) {
+      const unsigned char* row = Ks + static_cast<size_t>(i) * RB;
+#pragma unroll
+      for (int j = 0; j < NCH / 2; ++j) {
+        const int ch = hsel * (NCH / 2) + j;
+        float x[V];
+        Ty<T>::load16(reinterpret_cast<const T*>(row + ((ch ^ (i & (NCH - 1))) << 4)), x);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float* qg = qs + g * D + ch * V;
+#pragma unroll
+          for (int e = 0; e < V; ++e) acc[g] = fmaf(x[e], qg[e], acc[g]);
+        }
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      acc[g] += __shfl_xor_sync(0xffffffffu, acc[g], 1);
+      if (i < cnt) {
+        if (hsel == 0) ps[g * S + i] = acc[g];
+        lmax[g] = fmaxf(lmax[g], acc[g]);
+      }
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const float m = warp_max(lmax[g]);
+    if (lane == 0) red[warp][g] = m;
+  }
+  __syncthreads();
+  if (tid < G) {
+    float m = -INFINITY;
+    for (int w = 0; w < kAt / 32; ++w) m = fmaxf(m, red[w][tid]);
+    hm[tid] = m;
+  }
+  __syncthreads();
+  float lsum[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) lsum[g] = 0.f;
+  for (int i = tid; i < cnt; i += kAt) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float p = exp2f(ps[g * S + i] - hm[g]);
+      ps[g * S + i] = p;
+      lsum[g] += p;
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const float z = warp_sum(lsum[g]);
+    if (lane == 0) red[warp][g] = z;
+  }
+  __syncthreads();
+  if (tid < G) {
+    float z = 0.f;
+    for (int w = 0; w < kAt / 32; ++w) z += red[w][tid];
+    hl[tid] = z;
+  }
+
+  // ---- P V: thread owns dimensions (2 dp, 2 dp + 1) for tokens tg, tg + TG, ...
+  const int dp = tid % NDP, tg = tid / NDP;
+  float acc[G][2];
+#pragma unroll
+  for (int g = 0; g < G; ++g) acc[g][0] = acc[g][1] = 0.f;
+  for (int i = tg; i < cnt; i += TG) {
+    float v0, v1;
+    if constexpr (sizeof(T) == 2) {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(Vs + static_cast<size_t>(i) * RB + dp * 4);
+      v0 = __uint_as_float(w << 16);
+      v1 = __uint_as_float(w & 0xffff0000u);
+    } else {
+      const float2 w = *reinterpret_cast<const float2*>(Vs + static_cast<size_t>(i) * RB + dp * 8);
+      v0 = w.x;
+      v1 = w.y;
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float p = ps[g * S + i];
+      acc[g][0] = fmaf(p, v0, acc[g][0]);
+      acc[g][1] = fmaf(p, v1, acc[g][1]);
+    }
+  }
+  __syncthreads();   // K/V no longer read: reuse for the token-group sums
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    pvred[(tg * G + g) * D + 2 * dp] = acc[g][0];
+    pvred[(tg * G + g) * D + 2 * dp + 1] = acc[g][1];
+  }
+  __syncthreads();
+  const size_t pbase = static_cast<size_t>(pair) * G * max_splits;
+  for (int idx = tid; idx < G * D; idx += kAt) {
+    const int g = idx / D, dd = idx - g * D;
+    float sacc = 0.f;
+#pragma unroll
+    for (int z = 0; z < TG; ++z) sacc += pvred[(z * G + g) * D + dd];
+    float* pp = part + ((pbase + static_cast<size_t>(g) * max_splits + split) * (D + 2));
+    pp[dd] = sacc;
+    if (dd == 0) { pp[D] = hm[g]; pp[D + 1] = hl[g]; }
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) last = (atomicAdd(&ticket[pair], 1) == nsplit - 1);
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  for (int idx = tid; idx < G * D; idx += kAt) {
+    const int g = idx / D, dd = idx - g * D;
+    const float* pp = part + (pbase + static_cast<size_t>(g) * max_splits) * (D + 2);
+    float M = -INFINITY;
+    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(pp + sp * (D + 2) + D));
+    float num = 0.f, den = 0.f;
+    for (int sp = 0; sp < nsplit; ++sp) {
+      const float* q2 = pp + sp * (D + 2);
+      const float wgt = exp2f(__ldcg(q2 + D) - M);
+      num = fmaf(wgt, __ldcg(q2 + dd), num);
+      den = fmaf(wgt, __ldcg(q2 + D + 1), den);
+    }
+    out[(static_cast<size_t>(pair) * G + g) * D + dd] = Ty<T>::from_f(num / den);
+  }
+  if (tid == 0) ticket[pair] = 0;
+}
+
+template <typename T, int D, int G>
+static cudaError_t attn_t(Ctx& c, const void* q, void* out, int n_loc, cudaStream_t st) {
+  const int S = c.split_tokens;
+  const int n_out = c.p.o * c.p.c, n_sp = c.p.k * c.p.c;
+  const int T_all = n_out + n_sp + n_loc;
+  const int nsplit = (T_all + S - 1) / S;
+  if (nsplit > c.max_splits) return cudaErrorInvalidValue;
+  const size_t smem = attn_smem_bytes(sizeof(T), G, D, S);
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  auto kern = k_attn<T, D, G>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
+  kern<<<dim3(c.p.b * c.p.h_kv, nsplit), kAt, smem, st>>>(
+      static_cast<const T*>(c.K_out), static_cast<const T*>(c.V_out),
+      static_cast<const T*>(c.K_sparse), static_cast<const T*>(c.slot_V), c.sel_slot,
+      static_cast<const T*>(c.K_loc), static_cast<const T*>(c.V_loc), static_cast<const T*>(q),
+      static_cast<T*>(out), c.attn_part, c.attn_count, n_out, n_sp, n_loc, c.loc_cap, c.p.c,
+      c.p.k, S, nsplit, c.max_splits, scale_log2);
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+static cudaError_t attn_d(Ctx& c, const void* q, void* out, int n_loc, cudaStream_t st) {
+  switch (c.G) {
+    case 1: return attn_t<T, D, 1>(c, q, out, n_loc, st);
+    case 2: return attn_t<T, D, 2>(c, q, out, n_loc, st);
+    case 4: return attn_t<T, D, 4>(c, q, out, n_loc, st);
+    default: return attn_t<T, D, 8>(c, q, out, n_loc, st);
+  }
+}
+
+cudaError_t launch_attn(Ctx& c, const void* q, void* out, int n_loc, cudaStream_t st) {
+  kbegin(c, K_ATTN, st);
+  cudaError_t e;
+  if (c.p.dtype == SKV_DTYPE_BF16)
+    e = c.p.d == 128 ? attn_d<bf16, 128>(c, q, out, n_loc, st) : attn_d<bf16, 64>(c, q, out, n_loc, st);
+  else
+    e = c.p.d == 128 ? attn_d<float, 128>(c, q, out, n_loc, st) : attn_d<float, 64>(c, q, out, n_loc, st);
+  kend(c, K_ATTN, st);
+  return e;
+}
+
+}  // namespace skv

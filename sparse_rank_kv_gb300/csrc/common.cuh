@@ -19,9 +19,9 @@ enum : int {
   DEV_TIMEOUT = 5,      // a bounded mbarrier wait gave up
 };
 
-// Polls of a bounded mbarrier wait before a kernel gives up (each poll
-// suspends for a hardware-chosen interval; the total is well above a second).
-constexpr uint32_t kWaitLimit = 1u << 26;
+// Nanoseconds a bounded mbarrier wait lasts before a kernel gives up and
+// reports DEV_TIMEOUT (every legitimate wait is microseconds).
+constexpr unsigned long long kWaitLimit = 2000000000ull;
 
 __device__ __forceinline__ void flag_error(int* status, int code) {
   if (status) atomicCAS(status, 0, code);

@@ -5,8 +5,7 @@
 //             local-window append of the new token
 //   k_fetch   Gather(V_CPU, I) for the chunks that missed the cache, read
 //             zero-copy from pinned host memory on the side stream
-//   k_attn    split-KV attention over [outliers; RoPE(K_sparse); local]
-//             with the split combine done by the last block of each head
+// (the attention kernel is in attn.cu, the key rebuild in rebuild.cu)
 #include "common.cuh"
 #include "internal.h"
 
@@ -14,7 +13,6 @@ namespace skv {
 
 constexpr int kScoreTile = 128;      // landmarks per score tile (one per thread)
 constexpr int kSelectThreads = 1024;
-constexpr int kAttnThreads = 128;
 constexpr int kFetchWarps = 8;
 
 // ------------------------------------------------------------------ score
@@ -27,8 +25,6 @@ k_score(const T* __restrict__ L, const T* __restrict__ q, const uint32_t* __rest
         float* __restrict__ P, float2* __restrict__ part, int n, int ntile, int total_tiles,
         float scale) {
   __shared__ __align__(16) float qs[G * D];
-  __shared__ float red[kScoreTile / 32][G];
-  __shared__ float bmax[G];
   constexpr int V = Ty<T>::kVec;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int cur = -1;
@@ -61,32 +57,13 @@ k_score(const T* __restrict__ L, const T* __restrict__ q, const uint32_t* __rest
       for (int g = 0; g < G; ++g) P[(static_cast<size_t>(pair) * G + g) * n + j] = acc[g];
     }
     const bool valid = j < n && !((mask[static_cast<size_t>(pair) * ((n + 31) >> 5) + (j >> 5)] >> (j & 31)) & 1u);
-    // tile max and sum of exp over valid rows, per head
+    // per-warp (32-row) max and sum of exp over the valid rows, per head
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       const float m = warp_max(valid ? acc[g] : -INFINITY);
-      if (lane == 0) red[warp][g] = m;
-    }
-    __syncthreads();
-    if (tid < G) {
-      float m = -INFINITY;
-      for (int w = 0; w < kScoreTile / 32; ++w) m = fmaxf(m, red[w][tid]);
-      bmax[tid] = m;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float m = bmax[g];
       const float e = warp_sum(valid ? __expf(acc[g] - m) : 0.f);
-      if (lane == 0) red[warp][g] = e;
+      if (lane == 0) part[((static_cast<size_t>(pair) * G + g) * ntile + ti) * 4 + warp] = make_float2(m, e);
     }
-    __syncthreads();
-    if (tid < G) {
-      float z = 0.f;
-      for (int w = 0; w < kScoreTile / 32; ++w) z += red[w][tid];
-      part[(static_cast<size_t>(pair) * G + tid) * ntile + ti] = make_float2(bmax[tid], z);
-    }
-    __syncthreads();
   }
 }
 
@@ -128,14 +105,15 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part,
       V_loc[dst] = v_new[static_cast<size_t>(pair) * D + i];
     }
   }
-  // log-sum-exp of each query head over the candidate chunks
+  // log-sum-exp of each query head over the candidate chunks (4 partials
+  // of 32 landmarks per 128-landmark score tile)
   for (int g = warp; g < G; g += nthr / 32) {
-    const float2* pp = part + (static_cast<size_t>(pair) * G + g) * ntile;
+    const float2* pp = part + (static_cast<size_t>(pair) * G + g) * ntile * 4;
     float m = -INFINITY;
-    for (int t = lane; t < ntile; t += 32) m = fmaxf(m, pp[t].x);
+    for (int t = lane; t < 4 * ntile; t += 32) m = fmaxf(m, pp[t].x);
     m = warp_max(m);
     float z = 0.f;
-    for (int t = lane; t < ntile; t += 32) {
+    for (int t = lane; t < 4 * ntile; t += 32) {
       const float2 v = pp[t];
       if (v.y > 0.f) z += v.y * __expf(v.x - m);
     }
@@ -262,158 +240,6 @@ k_fetch(const T* __restrict__ vcpu, T* __restrict__ slot_V, const int32_t* __res
   }
 }
 
-// -------------------------------------------------------------- attention
-// Block (pair, split) covers tokens [split*S, min(T, split*S + S)) of the
-// concatenation [outliers (n_out); rebuilt chunks (n_sp); local (n_loc)].
-// Logits and probabilities stay in shared memory; the block writes its
-// partial (max, sum, sum p v) per query head; the last block of the pair
-// (atomic ticket) combines all splits in split order.
-template <typename T, int D, int G>
-__global__ void __launch_bounds__(kAttnThreads)
-k_attn(const T* __restrict__ K_out, const T* __restrict__ V_out, const T* __restrict__ K_sp,
-       const T* __restrict__ slot_V, const int32_t* __restrict__ sel_slot,
-       const T* __restrict__ K_loc, const T* __restrict__ V_loc, const T* __restrict__ q,
-       T* __restrict__ out, float* __restrict__ part, int32_t* __restrict__ ticket, int n_out,
-       int n_sp, int n_loc, int loc_cap, int c, int k, int S, int nsplit, int max_splits,
-       float scale_log2) {
-  extern __shared__ __align__(16) float sm[];
-  float* qs = sm;               // G*D
-  float* ps = qs + G * D;       // G*S
-  __shared__ float red[kAttnThreads / 32][G];
-  __shared__ float hm[G], hl[G];
-  __shared__ int last;
-  constexpr int V = Ty<T>::kVec;
-  const int pair = blockIdx.x, split = blockIdx.y;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int T_all = n_out + n_sp + n_loc;
-  const int t0 = split * S, t1 = min(T_all, t0 + S), cnt = t1 - t0;
-
-  for (int i = tid; i < G * D; i += kAttnThreads)
-    qs[i] = Ty<T>::to_f(q[static_cast<size_t>(pair) * G * D + i]) * scale_log2;
-  __syncthreads();
-
-  auto key_row = [&](int t) -> const T* {
-    if (t < n_out) return K_out + (static_cast<size_t>(pair) * n_out + t) * D;
-    t -= n_out;
-    if (t < n_sp) return K_sp + (static_cast<size_t>(pair) * n_sp + t) * D;
-    t -= n_sp;
-    return K_loc + (static_cast<size_t>(pair) * loc_cap + t) * D;
-  };
-  auto val_row = [&](int t) -> const T* {
-    if (t < n_out) return V_out + (static_cast<size_t>(pair) * n_out + t) * D;
-    t -= n_out;
-    if (t < n_sp) {
-      const int slot = sel_slot[static_cast<size_t>(pair) * k + t / c];
-      return slot_V + ((static_cast<size_t>(pair) * k + slot) * c + (t % c)) * D;
-    }
-    t -= n_sp;
-    return V_loc + (static_cast<size_t>(pair) * loc_cap + t) * D;
-  };
-
-  // logits (log2 domain)
-  float lmax[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) lmax[g] = -INFINITY;
-  for (int i = tid; i < cnt; i += kAttnThreads) {
-    const T* row = key_row(t0 + i);
-    float acc[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) acc[g] = 0.f;
-#pragma unroll 4
-    for (int d0 = 0; d0 < D; d0 += V) {
-      float x[V];
-      Ty<T>::load16(row + d0, x);
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-#pragma unroll
-        for (int e = 0; e < V; ++e) acc[g] = fmaf(x[e], qs[g * D + d0 + e], acc[g]);
-      }
-    }
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      ps[g * S + i] = acc[g];
-      lmax[g] = fmaxf(lmax[g], acc[g]);
-    }
-  }
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    const float m = warp_max(lmax[g]);
-    if (lane == 0) red[warp][g] = m;
-  }
-  __syncthreads();
-  if (tid < G) {
-    float m = -INFINITY;
-    for (int w = 0; w < kAttnThreads / 32; ++w) m = fmaxf(m, red[w][tid]);
-    hm[tid] = m;
-  }
-  __syncthreads();
-  float lsum[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) lsum[g] = 0.f;
-  for (int i = tid; i < cnt; i += kAttnThreads) {
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float p = exp2f(ps[g * S + i] - hm[g]);
-      ps[g * S + i] = p;
-      lsum[g] += p;
-    }
-  }
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    const float z = warp_sum(lsum[g]);
-    if (lane == 0) red[warp][g] = z;
-  }
-  __syncthreads();
-  if (tid < G) {
-    float z = 0.f;
-    for (int w = 0; w < kAttnThreads / 32; ++w) z += red[w][tid];
-    hl[tid] = z;
-  }
-  __syncthreads();
-
-  // P V: thread owns output dimension tid
-  const size_t pbase = static_cast<size_t>(pair) * G * max_splits;
-  if (tid < D) {
-    float acc[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) acc[g] = 0.f;
-    for (int i = 0; i < cnt; ++i) {
-      const float v = Ty<T>::to_f(val_row(t0 + i)[tid]);
-#pragma unroll
-      for (int g = 0; g < G; ++g) acc[g] = fmaf(ps[g * S + i], v, acc[g]);
-    }
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float* pp = part + ((pbase + static_cast<size_t>(g) * max_splits + split) * (D + 2));
-      pp[tid] = acc[g];
-      if (tid == 0) { pp[D] = hm[g]; pp[D + 1] = hl[g]; }
-    }
-  }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) last = (atomicAdd(&ticket[pair], 1) == nsplit - 1);
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  if (tid < D) {
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float* pp = part + (pbase + static_cast<size_t>(g) * max_splits) * (D + 2);
-      float M = -INFINITY;
-      for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(pp + sp * (D + 2) + D));
-      float num = 0.f, den = 0.f;
-      for (int sp = 0; sp < nsplit; ++sp) {
-        const float* q2 = pp + sp * (D + 2);
-        const float wgt = exp2f(__ldcg(q2 + D) - M);
-        num = fmaf(wgt, __ldcg(q2 + tid), num);
-        den = fmaf(wgt, __ldcg(q2 + D + 1), den);
-      }
-      out[(static_cast<size_t>(pair) * G + g) * D + tid] = Ty<T>::from_f(num / den);
-    }
-  }
-  if (tid == 0) ticket[pair] = 0;
-}
-
 // --------------------------------------------------------- outlier mask
 // Rebuilds the per-(batch, KV head) outlier bitmap from outlier_ids and
 // checks that the ids are ascending, distinct and < n.
@@ -458,6 +284,11 @@ static void score_d(Ctx& c, const void* q, cudaStream_t st) {
 
 cudaError_t launch_score(Ctx& c, const void* q, cudaStream_t st) {
   kbegin(c, K_SCORE, st);
+  const cudaError_t et = launch_score_tc(c, q, st);
+  if (et != cudaErrorNotSupported) {
+    kend(c, K_SCORE, st);
+    return et;
+  }
   if (c.p.dtype == SKV_DTYPE_BF16) {
     if (c.p.d == 128) score_d<bf16, 128>(c, q, st); else score_d<bf16, 64>(c, q, st);
   } else {
@@ -516,53 +347,6 @@ cudaError_t launch_fetch(Ctx& c, cudaStream_t st) {
         c.miss_slot, c.miss_count, c.p.s, c.n, c.p.c, c.p.d, c.p.k, c.status);
   kend(c, K_FETCH, st);
   return cudaGetLastError();
-}
-
-size_t attn_smem_bytes(int G, int D, int S) {
-  return sizeof(float) * (static_cast<size_t>(G) * D + static_cast<size_t>(G) * S);
-}
-
-template <typename T, int D, int G>
-static cudaError_t attn_t(Ctx& c, const void* q, void* out, int n_loc, cudaStream_t st) {
-  const int S = c.split_tokens;
-  const int n_out = c.p.o * c.p.c, n_sp = c.p.k * c.p.c;
-  const int T_all = n_out + n_sp + n_loc;
-  const int nsplit = (T_all + S - 1) / S;
-  if (nsplit > c.max_splits) return cudaErrorInvalidValue;
-  const size_t smem = attn_smem_bytes(G, D, S);
-  auto kern = k_attn<T, D, G>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
-  kern<<<dim3(c.p.b * c.p.h_kv, nsplit), kAttnThreads, smem, st>>>(
-      static_cast<const T*>(c.K_out), static_cast<const T*>(c.V_out),
-      static_cast<const T*>(c.K_sparse), static_cast<const T*>(c.slot_V), c.sel_slot,
-      static_cast<const T*>(c.K_loc), static_cast<const T*>(c.V_loc), static_cast<const T*>(q),
-      static_cast<T*>(out), c.attn_part, c.attn_count, n_out, n_sp, n_loc, c.loc_cap, c.p.c,
-      c.p.k, S, nsplit, c.max_splits, scale_log2);
-  return cudaGetLastError();
-}
-
-template <typename T, int D>
-static cudaError_t attn_d(Ctx& c, const void* q, void* out, int n_loc, cudaStream_t st) {
-  switch (c.G) {
-    case 1: return attn_t<T, D, 1>(c, q, out, n_loc, st);
-    case 2: return attn_t<T, D, 2>(c, q, out, n_loc, st);
-    case 4: return attn_t<T, D, 4>(c, q, out, n_loc, st);
-    default: return attn_t<T, D, 8>(c, q, out, n_loc, st);
-  }
-}
-
-cudaError_t launch_attn(Ctx& c, const void* q, void* out, int n_loc, cudaStream_t st) {
-  kbegin(c, K_ATTN, st);
-  cudaError_t e;
-  if (c.p.dtype == SKV_DTYPE_BF16)
-    e = c.p.d == 128 ? attn_d<bf16, 128>(c, q, out, n_loc, st) : attn_d<bf16, 64>(c, q, out, n_loc, st);
-  else
-    e = c.p.d == 128 ? attn_d<float, 128>(c, q, out, n_loc, st) : attn_d<float, 64>(c, q, out, n_loc, st);
-  kend(c, K_ATTN, st);
-  return e;
 }
 
 cudaError_t launch_build_mask(Ctx& c, cudaStream_t st) {

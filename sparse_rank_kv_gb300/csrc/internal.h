@@ -42,7 +42,7 @@ struct Ctx {
   int n = 0, G = 1;
   int ntile = 0;      // score tiles per (b, h_kv)
   int loc_cap = 0;    // w + max_new
-  int split_tokens = 256;
+  int split_tokens = 128;
   int max_splits = 0;
   bool cache_on = true, timing_on = false;
   long long t = 0;    // decode steps enqueued
@@ -71,8 +71,10 @@ struct Ctx {
 
   // tensor-core rebuild: TMA descriptors of A (b*s x r) and B^T (b*h_kv*d x r)
   CUtensorMap mapA{}, mapBt{};
-  bool tc_rebuild = false;      // shapes and dtype allow the tcgen05 kernel
-  bool force_simt = false;      // test hook: use the CUDA-core kernel anyway
+  CUtensorMap mapL{};           // landmarks (b*h_kv*n x d) for the tensor-core score kernel
+  bool tc_rebuild = false;      // shapes and dtype allow the tcgen05 rebuild
+  bool tc_score = false;        // ... and the tcgen05 landmark scores
+  bool force_simt = false;      // test hook: use the CUDA-core kernels anyway
 
   cudaStream_t side = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
@@ -86,7 +88,7 @@ struct Ctx {
 };
 
 size_t select_smem_bytes(int n, int k, int G);
-size_t attn_smem_bytes(int G, int D, int S);
+size_t attn_smem_bytes(int E, int G, int D, int S);
 
 // ------------------------------------------------------------ launch hooks
 // Every launcher brackets its kernel with kbegin/kend (api.cu): they count
@@ -101,6 +103,11 @@ cudaError_t launch_score(Ctx& c, const void* q, cudaStream_t st);
 cudaError_t launch_select(Ctx& c, const void* k_new, const void* v_new, int loc_row,
                           cudaStream_t st);
 cudaError_t launch_fetch(Ctx& c, cudaStream_t st);
+// score_tc.cu (cudaErrorNotSupported: use the CUDA-core score kernel)
+cudaError_t launch_score_tc(Ctx& c, const void* q, cudaStream_t st);
+bool tc_score_supported(const shadowkv_params& p);
+cudaError_t make_score_map(Ctx& c);
+// attn.cu
 cudaError_t launch_attn(Ctx& c, const void* q, void* out, int n_loc, cudaStream_t st);
 cudaError_t launch_build_mask(Ctx& c, cudaStream_t st);
 // rebuild.cu

@@ -1,0 +1,253 @@
+// Landmark scores of ShadowKV's decode step on the tensor cores (Algorithm 2
+// step 1): P = MatMul(Q, L^T) / sqrt(d) for every landmark of every
+// (batch, KV head), with the G query heads of the KV head as the N side of
+// the MMA (padded to 16 with zeros).  The landmark stream is the largest HBM
+// read of a decode step, so this kernel is built to keep HBM busy:
+//
+//   persistent: one CTA per SM, each owning a contiguous range of 128-row
+//               landmark tiles (a tile never spans two KV heads)
+//   warp 0    : TMA producer -- per tile, d/32 boxes of 128 landmark rows x
+//               32 columns and d/32 boxes of the head's q (16 rows; rows past
+//               G are zero-filled by TMA) into a 5-stage shared-memory ring,
+//               K-major with the 64-byte swizzle
+//   warp 1    : tcgen05.mma (M=128, N=16, K=16) x (d/16) per tile into one of
+//               two TMEM accumulators; commits free the ring slot and publish
+//               the accumulator
+//   warps 2-5 : epilogue -- one landmark row per thread (TMEM lane), scale,
+//               store the G logits, and per 32-row warp the running max and
+//               sum of exp over the non-outlier rows (softmax partials)
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace skv {
+
+constexpr int kScTile = 128;
+constexpr int kScStages = 5;
+constexpr int kScThreads = 192;
+
+__host__ __device__ constexpr int sc_stage_bytes(int D) { return (D / 32) * (kScTile + 16) * 64; }
+__host__ __device__ constexpr int sc_smem_bytes(int D) {
+  return 1024 /* alignment slack */ + 1024 /* header */ + kScStages * sc_stage_bytes(D);
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kScThreads, 1)
+k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUtensorMap mapQ,
+           const uint32_t* __restrict__ mask, float* __restrict__ P, float2* __restrict__ part, int n,
+           int ntile, int total_tiles, float scale, int* __restrict__ status) {
+  constexpr int KB = D / 32;
+  constexpr int A_BYTES = KB * kScTile * 64;
+  constexpr int STAGE = sc_stage_bytes(D);
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kScStages;
+  uint64_t* tfull = empty + kScStages;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  unsigned char* stages = smem + 1024;
+
+  const int t_begin = static_cast<int>(static_cast<long long>(total_tiles) * blockIdx.x / gridDim.x);
+  const int t_end = static_cast<int>(static_cast<long long>(total_tiles) * (blockIdx.x + 1) / gridDim.x);
+  const int ntl = t_end - t_begin;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    tc::prefetch_tensormap(&mapL);
+    tc::prefetch_tensormap(&mapQ);
+    for (int s = 0; s < kScStages; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(&tfull[a], 1);
+      tc::mbar_init(&tempty[a], 128);
+    }
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, 32);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int i = 0; i < ntl; ++i) {
+        const int s = i % kScStages;
+        const uint32_t ph = (i / kScStages) & 1;
+        if (!tc::mbar_wait(&empty[s], ph ^ 1, kWaitLimit)) {
+          flag_error(status, DEV_TIMEOUT);
+          break;
+        }
+        const int tile = t_begin + i;
+        const int pair = tile / ntile, ti = tile - pair * ntile;
+        unsigned char* st = stages + s * STAGE;
+        tc::mbar_expect_tx(&full[s], STAGE);
+#pragma unroll
+        for (int kb = 0; kb < KB; ++kb)
+          tc::tma_load_2d(st + kb * (kScTile * 64), &mapL, &full[s], kb * 32, pair * n + ti * kScTile);
+#pragma unroll
+        for (int kb = 0; kb < KB; ++kb)
+          tc::tma_load_3d(st + A_BYTES + kb * (16 * 64), &mapQ, &full[s], kb * 32, 0, pair);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(kScTile, 16);
+      for (int i = 0; i < ntl; ++i) {
+        const int s = i % kScStages;
+        const uint32_t ph = (i / kScStages) & 1;
+        const int a = i & 1;
+        const uint32_t tph = (i >> 1) & 1;
+        if (!tc::mbar_wait(&full[s], ph, kWaitLimit) || !tc::mbar_wait(&tempty[a], tph ^ 1, kWaitLimit)) {
+          flag_error(status, DEV_TIMEOUT);
+          break;
+        }
+        tc::fence_after();
+        const uint32_t a0 = tc::smem_u32(stages + s * STAGE);
+        const uint32_t b0 = a0 + A_BYTES;
+#pragma unroll
+        for (int kb = 0; kb < KB; ++kb) {
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks) {
+            tc::mma_bf16(tmem + a * 16, tc::desc_k_sw64(a0 + kb * (kScTile * 64) + ks * 32, 512),
+                         tc::desc_k_sw64(b0 + kb * (16 * 64) + ks * 32, 512), idesc, (kb | ks) != 0);
+          }
+        }
+        tc::mma_commit(&empty[s]);
+        tc::mma_commit(&tfull[a]);
+      }
+    }
+  } else {
+    const int q4 = warp & 3;               // TMEM lane quarter of this warp
+    const int row = q4 * 32 + lane;
+    const int nw = (n + 31) >> 5;
+    for (int i = 0; i < ntl; ++i) {
+      const int a = i & 1;
+      const uint32_t tph = (i >> 1) & 1;
+      const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(&tfull[a], tph, kWaitLimit));
+      if (!ok) {
+        if (lane == 0) flag_error(status, DEV_TIMEOUT);
+        break;
+      }
+      tc::fence_after();
+      float acc[8];
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + a * 16;
+      if constexpr (G <= 4) tc::tmem_ld4(taddr, acc);
+      else tc::tmem_ld8(taddr, acc);
+      tc::fence_before();
+      tc::mbar_arrive(&tempty[a]);
+      const int tile = t_begin + i;
+      const int pair = tile / ntile, ti = tile - pair * ntile;
+      const int j = ti * kScTile + row;
+      const bool valid = j < n && !((mask[static_cast<size_t>(pair) * nw + (j >> 5)] >> (j & 31)) & 1u);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float x = acc[g] * scale;
+        if (j < n) P[(static_cast<size_t>(pair) * G + g) * n + j] = x;
+        const float m = warp_max(valid ? x : -INFINITY);
+        const float e = warp_sum(valid ? __expf(x - m) : 0.f);
+        if (lane == 0) part[((static_cast<size_t>(pair) * G + g) * ntile + ti) * 4 + q4] = make_float2(m, e);
+      }
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 1) tc::tmem_dealloc(tmem, 32);
+}
+
+bool tc_score_supported(const shadowkv_params& p) {
+  return p.dtype == SKV_DTYPE_BF16 && (p.d == 64 || p.d == 128);
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+cudaError_t make_score_map(Ctx& c) {
+  c.tc_score = false;
+  if (!tc_score_supported(c.p)) return cudaSuccess;
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t rows = static_cast<cuuint64_t>(c.p.b) * c.p.h_kv * c.n;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(c.p.d), rows};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(c.p.d) * 2};
+  const cuuint32_t box[2] = {32, kScTile};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(&c.mapL, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.L, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  c.tc_score = true;
+  return cudaSuccess;
+}
+
+// The queries live in the caller's buffer, so their descriptor is encoded for
+// every step: a 3D view {d, G, b*h_kv} read in boxes of 32 x 16 x 1, the rows
+// past G being zero-filled.
+static cudaError_t encode_q(const Ctx& c, const void* q, CUtensorMap* map) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  if (reinterpret_cast<uintptr_t>(q) % 16) return cudaErrorMisalignedAddress;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(c.p.d), static_cast<cuuint64_t>(c.G),
+                              static_cast<cuuint64_t>(c.p.b) * c.p.h_kv};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(c.p.d) * 2,
+                                 static_cast<cuuint64_t>(c.p.d) * 2 * c.G};
+  const cuuint32_t box[3] = {32, 16, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int D, int G>
+static cudaError_t score_tc_t(Ctx& c, const CUtensorMap& mq, cudaStream_t st) {
+  const int smem = sc_smem_bytes(D);
+  auto kern = k_score_tc<D, G>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int total = c.p.b * c.p.h_kv * c.ntile;
+  const int grid = total < c.nsm ? total : c.nsm;
+  kern<<<grid, kScThreads, smem, st>>>(c.mapL, mq, c.out_mask, c.logits, c.score_part, c.n, c.ntile,
+                                        total, 1.0f / sqrtf(static_cast<float>(D)), c.status);
+  return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t score_tc_d(Ctx& c, const CUtensorMap& mq, cudaStream_t st) {
+  switch (c.G) {
+    case 1: return score_tc_t<D, 1>(c, mq, st);
+    case 2: return score_tc_t<D, 2>(c, mq, st);
+    case 4: return score_tc_t<D, 4>(c, mq, st);
+    default: return score_tc_t<D, 8>(c, mq, st);
+  }
+}
+
+// Returns cudaErrorNotSupported when the tensor-core kernel does not apply
+// (the caller then uses the CUDA-core kernel).
+cudaError_t launch_score_tc(Ctx& c, const void* q, cudaStream_t st) {
+  if (!c.tc_score || c.force_simt) return cudaErrorNotSupported;
+  CUtensorMap mq;
+  if (encode_q(c, q, &mq) != cudaSuccess) return cudaErrorNotSupported;
+  return c.p.d == 128 ? score_tc_d<128>(c, mq, st) : score_tc_d<64>(c, mq, st);
+}
+
+}  // namespace skv

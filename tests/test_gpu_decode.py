@@ -73,7 +73,7 @@ def run_parity(cfg, steps=None, group="max", cache=True, bsel=None, rows=True, a
             lg = ctx.export("LOGITS").view(b, hq, n).numpy()[sl].astype(np.float64)
             m = ~np.isnan(res.P)
             scale = np.abs(res.P[m]).max()
-            assert np.abs(lg[m] - res.P[m]).max() <= 2e-6 * scale + 1e-6, f"step {t}: logits"
+            assert np.abs(lg[m] - res.P[m]).max() <= 1e-5 * scale + 1e-6, f"step {t}: logits"
             ks = np64(ctx.export("K_SPARSE").view(b, h, k * c, d)[sl])
             kref = res.K_sparse
             tol = (1e-5 if cfg.dtype == "f32" else 8e-3) * np.abs(kref).max()
@@ -89,21 +89,25 @@ def run_parity(cfg, steps=None, group="max", cache=True, bsel=None, rows=True, a
     SMALL.with_(r=48, seed=43),                       # last K block half out of range
     SMALL.with_(c=16, k=20, seed=44),                 # 16-row chunk boxes
     SMALL.with_(d=64, theta=1e4, seed=45),            # N = 64
-], ids=["r64", "r48", "c16", "d64"])
-def test_tensor_core_rebuild_matches_cuda_core_rebuild(cfg):
-    """The tcgen05 kernel and the fp32 CUDA-core kernel compute the same
-    RoPE(Gather(A, I) B): both round an fp32 result to bf16."""
+    SMALL.with_(h_q=16, seed=48),                     # G = 8 (x8 TMEM loads)
+    SMALL.with_(h_q=2, seed=49),                      # G = 1
+], ids=["r64", "r48", "c16", "d64", "g8", "g1"])
+def test_tensor_core_kernels_match_cuda_core_kernels(cfg):
+    """The tcgen05 kernels and the fp32 CUDA-core kernels compute the same
+    landmark logits (fp32 sums of exact bf16 products) and the same
+    RoPE(Gather(A, I) B) (both round an fp32 result to bf16)."""
     st = synth.make_state(cfg, device="cuda")
     got = []
     for simt in (0, 1):
         ctx = binding.load_state(binding.make_params(cfg), st)
-        ctx.set_option(binding.OPT_SIMT_REBUILD, simt)
+        ctx.set_option(binding.OPT_CUDA_CORES, simt)
         out = torch.empty(cfg.b, cfg.h_q, cfg.d, dtype=torch.bfloat16, device="cuda")
         ctx.decode_step(st["q"][0], st["k_new"][0], st["v_new"][0], out)
         torch.cuda.synchronize()
         ctx.check()
-        got.append((ctx.export("K_SPARSE").float(), out.float().cpu()))
-    (k_tc, o_tc), (k_simt, o_simt) = got
+        got.append((ctx.export("K_SPARSE").float(), out.float().cpu(), ctx.export("LOGITS")))
+    (k_tc, o_tc, l_tc), (k_simt, o_simt, l_simt) = got
+    assert (l_tc - l_simt).abs().max() <= 1e-5 * l_simt.abs().max()
     assert (k_tc - k_simt).abs().max() <= 2.0 ** -7 * k_simt.abs().max()
     assert (o_tc - o_simt).abs().max() <= 1e-2 * o_simt.abs().max()
 
@@ -147,8 +151,8 @@ def test_k_one_and_k_all_candidates():
 
 
 def test_split_size_variants():
-    run_parity(SMALL.with_(seed=37), steps=2, split=64)
-    run_parity(SMALL.with_(seed=37), steps=2, split=1024)
+    run_parity(SMALL.with_(seed=37), steps=2, split=32)
+    run_parity(SMALL.with_(seed=37), steps=2, split=256)
 
 
 def test_values_from_host_memory():
