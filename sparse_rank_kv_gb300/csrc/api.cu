@@ -467,7 +467,7 @@ skv_status shadowkv_set_option(shadowkv_ctx* h, int option, long long value) {
     case SKV_OPT_SPLIT_TOKENS: {
       if (value < 32 || value > 256 || value % 32)
         return fail(SKV_ERR_INVALID_ARG, "split tokens must be a multiple of 32 in [32, 256]");
-      if (skv::attn_smem_bytes(c.E, c.G, c.p.d, static_cast<int>(value)) > 227 * 1024)
+      if (skv::attn_smem_bytes(c.E, c.G, c.p.d, static_cast<int>(value), c.max_splits) > 227 * 1024)
         return fail(SKV_ERR_UNSUPPORTED, "split of %lld tokens does not fit in shared memory", value);
       c.split_tokens = static_cast<int>(value);
       return SKV_OK;

@@ -17,7 +17,8 @@
 
 namespace skv {
 
-constexpr int kAt = 256;   // threads per attention block
+constexpr int kAt = 256;        // threads per attention block
+constexpr int kMaxSplit = 256;  // largest split (tokens)
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
@@ -35,12 +36,16 @@ struct AttnLayout {
   static constexpr int V = 16 / static_cast<int>(sizeof(T));   // elements per chunk
 };
 
-size_t attn_smem_bytes(int E, int G, int D, int S) {
+// Shared memory: K and V rows [S][D] each, q [G][D] and p [G][S] in fp32, and
+// the split weights of the combine [G][max_splits]; the P V partial sums
+// [kAt/(D/2)][G][D] reuse the K/V space (extended if they are larger).
+size_t attn_smem_bytes(int E, int G, int D, int S, int max_splits) {
   const size_t rb = static_cast<size_t>(D) * E;
-  const size_t pv = static_cast<size_t>(kAt / (D / 2)) * G * D;   // PV partial sums
+  const size_t pv = static_cast<size_t>(kAt / (D / 2)) * G * D * sizeof(float);
   const size_t kv = 2 * static_cast<size_t>(S) * rb;
-  return kv + sizeof(float) * (static_cast<size_t>(G) * D + static_cast<size_t>(G) * S) +
-         (pv * sizeof(float) > kv ? pv * sizeof(float) - kv : 0);
+  return (kv > pv ? kv : pv) +
+         sizeof(float) * (static_cast<size_t>(G) * D + static_cast<size_t>(G) * S +
+                          static_cast<size_t>(G) * max_splits);
 }
 
 template <typename T, int D, int G>
@@ -49,7 +54,7 @@ k_attn(const T* __restrict__ K_out, const T* __restrict__ V_out, const T* __rest
        const T* __restrict__ slot_V, const int32_t* __restrict__ sel_slot,
        const T* __restrict__ K_loc, const T* __restrict__ V_loc, const T* __restrict__ q,
        T* __restrict__ out, float* __restrict__ part, int32_t* __restrict__ ticket, int n_out,
-       int n_sp, int n_loc, int loc_cap, int c, int k, int S, int nsplit, int max_splits,
+       int n_sp, int n_loc, int loc_cap, int c, int c_shift, int k, int S, int nsplit, int max_splits,
        float scale_log2) {
   using Lay = AttnLayout<T, D>;
   constexpr int RB = Lay::RB, NCH = Lay::NCH, V = Lay::V;
@@ -58,21 +63,34 @@ k_attn(const T* __restrict__ K_out, const T* __restrict__ V_out, const T* __rest
   extern __shared__ __align__(16) unsigned char sm[];
   unsigned char* Ks = sm;
   unsigned char* Vs = sm + static_cast<size_t>(S) * RB;
-  float* qs = reinterpret_cast<float*>(Vs + static_cast<size_t>(S) * RB);
+  constexpr int PVB = (kAt / (D / 2)) * G * D * 4;   // bytes of the P V partial sums
+  const int kvb = 2 * S * RB;
+  float* qs = reinterpret_cast<float*>(sm + (kvb > PVB ? kvb : PVB));
   float* ps = qs + G * D;
+  float* wts = ps + G * S;                       // [G][max_splits], combine only
   float* pvred = reinterpret_cast<float*>(sm);   // reuses K/V after the logits
   __shared__ float red[kAt / 32][G];
   __shared__ float hm[G], hl[G];
   __shared__ int last;
+  __shared__ int s_slot[kMaxSplit + 1];   // cache slots of the split's rebuilt chunks
 
   const int pair = blockIdx.x, split = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int T_all = n_out + n_sp + n_loc;
   const int t0 = split * S, cnt = min(T_all, t0 + S) - t0;
+  // chunk range of the split's part of the rebuilt segment
+  const int sp0 = max(t0, n_out) - n_out, sp1 = min(t0 + cnt, n_out + n_sp) - n_out;
+  const int ch0 = sp0 / c;
+  if (sp1 > sp0)
+    for (int i = tid; i <= (sp1 - 1) / c - ch0; i += kAt) s_slot[i] = sel_slot[static_cast<size_t>(pair) * k + ch0 + i];
+  __syncthreads();
 
-  // ---- copy the split's K and V rows to shared memory
-  for (int idx = tid; idx < cnt * NCH; idx += kAt) {
-    const int i = idx / NCH, ch = idx - i * NCH;
+  // ---- copy the split's K and V rows to shared memory: LPR lanes per row,
+  // one 16-byte chunk each, so every warp instruction covers whole rows
+  constexpr int LPR = NCH < 32 ? NCH : 32;
+  constexpr int RPI = kAt / LPR;
+  const int lc = tid % LPR;
+  for (int i = tid / LPR; i < cnt; i += RPI) {
     int t = t0 + i;
     const T *kr, *vr;
     if (t < n_out) {
@@ -80,15 +98,21 @@ k_attn(const T* __restrict__ K_out, const T* __restrict__ V_out, const T* __rest
       vr = V_out + (static_cast<size_t>(pair) * n_out + t) * D;
     } else if ((t -= n_out) < n_sp) {
       kr = K_sp + (static_cast<size_t>(pair) * n_sp + t) * D;
-      const int slot = sel_slot[static_cast<size_t>(pair) * k + t / c];
-      vr = slot_V + ((static_cast<size_t>(pair) * k + slot) * c + (t % c)) * D;
+      const int cq = c_shift >= 0 ? (t >> c_shift) : t / c;
+      const int slot = s_slot[cq - ch0];
+      vr = slot_V + ((static_cast<size_t>(pair) * k + slot) * c + (t - cq * c)) * D;
     } else {
       t -= n_sp;
       kr = K_loc + (static_cast<size_t>(pair) * loc_cap + t) * D;
       vr = V_loc + (static_cast<size_t>(pair) * loc_cap + t) * D;
     }
-    cp_async16(Ks + static_cast<size_t>(i) * RB + ((ch ^ (i & (NCH - 1))) << 4), kr + ch * V);
-    cp_async16(Vs + static_cast<size_t>(i) * RB + (ch << 4), vr + ch * V);
+    unsigned char* krow = Ks + static_cast<size_t>(i) * RB;
+    unsigned char* vrow = Vs + static_cast<size_t>(i) * RB;
+#pragma unroll
+    for (int ch = lc; ch < NCH; ch += LPR) {
+      cp_async16(krow + ((ch ^ (i & (NCH - 1))) << 4), kr + ch * V);
+      cp_async16(vrow + (ch << 4), vr + ch * V);
+    }
   }
   for (int i = tid; i < G * D; i += kAt)
     qs[i] = Ty<T>::to_f(q[static_cast<size_t>(pair) * G * D + i]) * scale_log2;
@@ -102,9 +126,9 @@ k_attn(const T* __restrict__ K_out, const T* __restrict__ V_out, const T* __rest
   const int hsel = tid & 1;
   for (int i0 = 0; i0 < cnt; i0 += kAt / 2) {
     const int i = i0 + (tid >> 1);
-    float acc[G];
+    float2 acc2[G];
 #pragma unroll
-    for (int g = 0; g < G; ++g) acc[g] = 0.f;
+    for (int g = 0; g < G; ++g) acc2[g] = make_float2(0.f, 0.f);
     if (i < cnt) {
       const unsigned char* row = Ks + static_cast<size_t>(i) * RB;
 #pragma unroll
@@ -114,14 +138,17 @@ k_attn(const T* __restrict__ K_out, const T* __restrict__ V_out, const T* __rest
         Ty<T>::load16(reinterpret_cast<const T*>(row + ((ch ^ (i & (NCH - 1))) << 4)), x);
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          const float* qg = qs + g * D + ch * V;
+          const float2* qg = reinterpret_cast<const float2*>(qs + g * D + ch * V);
 #pragma unroll
-          for (int e = 0; e < V; ++e) acc[g] = fmaf(x[e], qg[e], acc[g]);
+          for (int e = 0; e < V / 2; ++e)
+            acc2[g] = __ffma2_rn(make_float2(x[2 * e], x[2 * e + 1]), qg[e], acc2[g]);
         }
       }
     }
+    float acc[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
+      acc[g] = acc2[g].x + acc2[g].y;
       acc[g] += __shfl_xor_sync(0xffffffffu, acc[g], 1);
       if (i < cnt) {
         if (hsel == 0) ps[g * S + i] = acc[g];
@@ -166,33 +193,28 @@ k_attn(const T* __restrict__ K_out, const T* __restrict__ V_out, const T* __rest
 
   // ---- P V: thread owns dimensions (2 dp, 2 dp + 1) for tokens tg, tg + TG, ...
   const int dp = tid % NDP, tg = tid / NDP;
-  float acc[G][2];
+  float2 acc[G];
 #pragma unroll
-  for (int g = 0; g < G; ++g) acc[g][0] = acc[g][1] = 0.f;
+  for (int g = 0; g < G; ++g) acc[g] = make_float2(0.f, 0.f);
+#pragma unroll 4
   for (int i = tg; i < cnt; i += TG) {
-    float v0, v1;
+    float2 v;
     if constexpr (sizeof(T) == 2) {
       const uint32_t w = *reinterpret_cast<const uint32_t*>(Vs + static_cast<size_t>(i) * RB + dp * 4);
-      v0 = __uint_as_float(w << 16);
-      v1 = __uint_as_float(w & 0xffff0000u);
+      v = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
     } else {
-      const float2 w = *reinterpret_cast<const float2*>(Vs + static_cast<size_t>(i) * RB + dp * 8);
-      v0 = w.x;
-      v1 = w.y;
+      v = *reinterpret_cast<const float2*>(Vs + static_cast<size_t>(i) * RB + dp * 8);
     }
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       const float p = ps[g * S + i];
-      acc[g][0] = fmaf(p, v0, acc[g][0]);
-      acc[g][1] = fmaf(p, v1, acc[g][1]);
+      acc[g] = __ffma2_rn(make_float2(p, p), v, acc[g]);
     }
   }
   __syncthreads();   // K/V no longer read: reuse for the token-group sums
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-    pvred[(tg * G + g) * D + 2 * dp] = acc[g][0];
-    pvred[(tg * G + g) * D + 2 * dp + 1] = acc[g][1];
-  }
+  for (int g = 0; g < G; ++g)
+    *reinterpret_cast<float2*>(&pvred[(tg * G + g) * D + 2 * dp]) = acc[g];
   __syncthreads();
   const size_t pbase = static_cast<size_t>(pair) * G * max_splits;
   for (int idx = tid; idx < G * D; idx += kAt) {
@@ -210,19 +232,35 @@ k_attn(const T* __restrict__ K_out, const T* __restrict__ V_out, const T* __rest
   __syncthreads();
   if (!last) return;
   __threadfence();
+  // combine: weight of split sp for head g = 2^(m_sp - M) / sum_sp' 2^(m_sp' - M) l_sp'
+  for (int idx = tid; idx < G * nsplit; idx += kAt) {
+    const int g = idx / nsplit, sp = idx - g * nsplit;
+    wts[idx] = __ldcg(part + (pbase + static_cast<size_t>(g) * max_splits + sp) * (D + 2) + D);
+  }
+  __syncthreads();
+  if (tid < G) {
+    float M = -INFINITY, den = 0.f;
+    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, wts[tid * nsplit + sp]);
+    for (int sp = 0; sp < nsplit; ++sp) {
+      const float l = __ldcg(part + (pbase + static_cast<size_t>(tid) * max_splits + sp) * (D + 2) + D + 1);
+      den = fmaf(exp2f(wts[tid * nsplit + sp] - M), l, den);
+    }
+    hm[tid] = M;
+    hl[tid] = 1.f / den;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < G * nsplit; idx += kAt) {
+    const int g = idx / nsplit;
+    wts[idx] = exp2f(wts[idx] - hm[g]) * hl[g];
+  }
+  __syncthreads();
   for (int idx = tid; idx < G * D; idx += kAt) {
     const int g = idx / D, dd = idx - g * D;
-    const float* pp = part + (pbase + static_cast<size_t>(g) * max_splits) * (D + 2);
-    float M = -INFINITY;
-    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(pp + sp * (D + 2) + D));
-    float num = 0.f, den = 0.f;
-    for (int sp = 0; sp < nsplit; ++sp) {
-      const float* q2 = pp + sp * (D + 2);
-      const float wgt = exp2f(__ldcg(q2 + D) - M);
-      num = fmaf(wgt, __ldcg(q2 + dd), num);
-      den = fmaf(wgt, __ldcg(q2 + D + 1), den);
-    }
-    out[(static_cast<size_t>(pair) * G + g) * D + dd] = Ty<T>::from_f(num / den);
+    const float* pp = part + (pbase + static_cast<size_t>(g) * max_splits) * (D + 2) + dd;
+    float num = 0.f;
+#pragma unroll 8
+    for (int sp = 0; sp < nsplit; ++sp) num = fmaf(wts[g * nsplit + sp], __ldcg(pp + sp * (D + 2)), num);
+    out[(static_cast<size_t>(pair) * G + g) * D + dd] = Ty<T>::from_f(num);
   }
   if (tid == 0) ticket[pair] = 0;
 }
@@ -234,7 +272,7 @@ static cudaError_t attn_t(Ctx& c, const void* q, void* out, int n_loc, cudaStrea
   const int T_all = n_out + n_sp + n_loc;
   const int nsplit = (T_all + S - 1) / S;
   if (nsplit > c.max_splits) return cudaErrorInvalidValue;
-  const size_t smem = attn_smem_bytes(sizeof(T), G, D, S);
+  const size_t smem = attn_smem_bytes(sizeof(T), G, D, S, c.max_splits);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
   auto kern = k_attn<T, D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -246,7 +284,8 @@ static cudaError_t attn_t(Ctx& c, const void* q, void* out, int n_loc, cudaStrea
       static_cast<const T*>(c.K_sparse), static_cast<const T*>(c.slot_V), c.sel_slot,
       static_cast<const T*>(c.K_loc), static_cast<const T*>(c.V_loc), static_cast<const T*>(q),
       static_cast<T*>(out), c.attn_part, c.attn_count, n_out, n_sp, n_loc, c.loc_cap, c.p.c,
-      c.p.k, S, nsplit, c.max_splits, scale_log2);
+      (c.p.c & (c.p.c - 1)) == 0 ? __builtin_ctz(static_cast<unsigned>(c.p.c)) : -1, c.p.k, S, nsplit,
+      c.max_splits, scale_log2);
   return cudaGetLastError();
 }
 

@@ -141,32 +141,89 @@ __device__ __forceinline__ uint32_t order_key(float x) {
 }
 
 // ------------------------------------------------------------ top-k select
-// Block-wide selection of the k largest keys among keys[0..n) (shared
-// memory), ties broken toward the lower index; key 0 marks an excluded entry
-// and is never chosen when at least k keys are non-zero.  The chosen indices
-// are written to out[0..k) in ascending order (shared or global memory).
-// `scratch` holds >= 256 + 40 ints of shared memory.  Radix select on the
-// 32-bit key, 8 bits per pass from the top, then an order-preserving
-// compaction.  All threads of the block must call it.
-__device__ __forceinline__ void block_topk(const uint32_t* keys, int n, int k, int* out, int* scratch) {
-  int* hist = scratch;          // 256
-  int* tmp = scratch + 256;     // 33 for the scans
-  int* bcast = scratch + 256 + 34;  // 2: digit, remaining need
-  const int tid = threadIdx.x, lane = tid & 31, nthr = blockDim.x;
+constexpr int kTopkCand = 4096;   // boundary-bin candidates kept after the first pass
+
+// Shared memory (ints) block_topk needs besides the keys.
+__host__ __device__ constexpr int topk_scratch_ints(int nthreads) {
+  // max of the radix path's needs and (values + block_kth scratch + scans)
+  return (nthreads / 32) * 256 + 256 + 64 + kTopkCand > 4 * nthreads + (nthreads / 32) * 256 + 256 + 48
+             ? (nthreads / 32) * 256 + 256 + 64 + kTopkCand
+             : 4 * nthreads + (nthreads / 32) * 256 + 256 + 48;
+}
+
+// Radix version of block_topk below (same contract, no bitmap): radix select
+// on r = key - kmin (kmin: smallest non-zero key), 8-bit digits
+// taken from the highest bit in which keys can differ downward, so no pass is
+// spent on bits every key shares.  Each warp counts into a private 256-bin
+// histogram (no cross-warp contention on popular bins).  After the first
+// digit is fixed, the keys in its bin are compacted into a candidate list
+// (if there are at most kTopkCand of them) and the remaining digits are
+// resolved on that list only.  A final order-preserving compaction writes the
+// chosen indices.  All threads of the block must call it; blockDim.x must be
+// a multiple of 32.
+__device__ __forceinline__ void block_topk_radix(const uint32_t* keys, int n, int k, int* out, int* scratch) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthr = blockDim.x;
+  const int nwarps = nthr >> 5;
+  int* whist = scratch;                       // [nwarps][256]
+  int* hist = scratch + nwarps * 256;         // [256]
+  int* tmp = hist + 256;                      // 33 ints for the scans
+  int* bc = tmp + 40;                         // broadcast slots
+  int* cand = tmp + 64;                       // [kTopkCand] indices
+  // smallest and largest non-zero key
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+  for (int j = tid; j < n; j += nthr) {
+    const uint32_t key = keys[j];
+    if (key) { kmin = min(kmin, key); kmax = max(kmax, key); }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+  }
+  if (lane == 0) { whist[warp] = static_cast<int>(kmin); whist[32 + warp] = static_cast<int>(kmax); }
+  __syncthreads();
+  if (tid < 32) {
+    uint32_t m = tid < nwarps ? static_cast<uint32_t>(whist[tid]) : 0xffffffffu;
+    uint32_t M = tid < nwarps ? static_cast<uint32_t>(whist[32 + tid]) : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      m = min(m, __shfl_xor_sync(0xffffffffu, m, o));
+      M = max(M, __shfl_xor_sync(0xffffffffu, M, o));
+    }
+    if (tid == 0) { bc[2] = static_cast<int>(m); bc[3] = static_cast<int>(M); }
+  }
+  __syncthreads();
+  kmin = static_cast<uint32_t>(bc[2]);
+  kmax = static_cast<uint32_t>(bc[3]);
+  const uint32_t span = kmax - kmin;          // every r = key - kmin is <= span
+  int hb = span ? 32 - __clz(span) : 1;       // r < 2^hb
   uint32_t prefix = 0, pmask = 0;
   int need = k;
-  const int n_pad = ((n + nthr - 1) / nthr) * nthr;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += nthr) hist[i] = 0;
-    __syncthreads();
-    for (int j = tid; j < n_pad; j += nthr) {
-      int bin = 256;
-      if (j < n) {
+  int ncand = -1;                             // -1: scan all keys
+  while (hb > 0) {
+    const int width = hb < 8 ? hb : 8;
+    const int shift = hb - width;
+    const uint32_t dmask = (1u << width) - 1u;
+    int* wh = whist + warp * 256;
+    for (int i = lane; i < 256; i += 32) wh[i] = 0;
+    __syncwarp();
+    if (ncand < 0) {
+      for (int j = tid; j < n; j += nthr) {
         const uint32_t key = keys[j];
-        if ((key & pmask) == prefix) bin = (key >> shift) & 255;
+        const uint32_t r = key - kmin;
+        if (key && (r & pmask) == prefix) atomicAdd(&wh[(r >> shift) & dmask], 1);
       }
-      const unsigned grp = __match_any_sync(0xffffffffu, bin);
-      if (bin < 256 && lane == __ffs(grp) - 1) atomicAdd(&hist[bin], __popc(grp));
+    } else {
+      for (int c = tid; c < ncand; c += nthr) {
+        const uint32_t r = keys[cand[c]] - kmin;
+        if ((r & pmask) == prefix) atomicAdd(&wh[(r >> shift) & dmask], 1);
+      }
+    }
+    __syncthreads();
+    for (int i = tid; i < 256; i += nthr) {
+      int acc = 0;
+      for (int w = 0; w < nwarps; ++w) acc += whist[w * 256 + i];
+      hist[i] = acc;
     }
     __syncthreads();
     if (tid < 32) {
@@ -177,12 +234,12 @@ __device__ __forceinline__ void block_topk(const uint32_t* keys, int n, int k, i
       int incl = sum;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        int y = __shfl_up_sync(0xffffffffu, incl, o);
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
       }
       const int excl = incl - sum;
       const unsigned hit = __ballot_sync(0xffffffffu, incl >= need);
-      const int first = __ffs(hit) - 1;  // need <= total count by construction
+      const int first = __ffs(hit) - 1;   // need <= number of candidates by construction
       if (lane == first) {
         int acc = excl, digit = 255 - 8 * lane;
 #pragma unroll
@@ -190,19 +247,40 @@ __device__ __forceinline__ void block_topk(const uint32_t* keys, int n, int k, i
           if (acc + cnt[i] >= need) { digit = 255 - 8 * lane - i; break; }
           acc += cnt[i];
         }
-        bcast[0] = digit;
-        bcast[1] = need - acc;
+        bc[0] = digit;
+        bc[1] = need - acc;
+        bc[4] = cnt[digit == 255 - 8 * lane ? 0 : (255 - 8 * lane - digit)];   // keys in the bin
       }
     }
     __syncthreads();
-    prefix |= static_cast<uint32_t>(bcast[0]) << shift;
-    pmask |= 255u << shift;
-    need = bcast[1];
+    prefix |= static_cast<uint32_t>(bc[0]) << shift;
+    pmask |= dmask << shift;
+    need = bc[1];
+    const int inbin = bc[4];
+    hb = shift;
     __syncthreads();
+    if (ncand < 0 && hb > 0 && inbin <= kTopkCand) {
+      // compact the bin's keys into the candidate list (order not needed)
+      const int per = (n + nthr - 1) / nthr;
+      const int j0 = tid * per, j1 = min(n, j0 + per);
+      int mine = 0;
+      for (int j = j0; j < j1; ++j) {
+        const uint32_t key = keys[j];
+        mine += key && ((key - kmin) & pmask) == prefix;
+      }
+      int tot;
+      int pos = block_exclusive_scan(mine, tmp, &tot);
+      for (int j = j0; j < j1; ++j) {
+        const uint32_t key = keys[j];
+        if (key && ((key - kmin) & pmask) == prefix) cand[pos++] = j;
+      }
+      ncand = tot;
+      __syncthreads();
+    }
   }
-  // prefix is the k-th largest key; take every key above it and the first
-  // `need` keys equal to it (lowest indices first).
-  const uint32_t T = prefix;
+  // kmin + prefix is the k-th largest key; take every key above it and the
+  // first `need` keys equal to it (lowest indices first).
+  const uint32_t T = kmin + prefix;
   const int per = (n + nthr - 1) / nthr;
   const int j0 = tid * per, j1 = min(n, j0 + per);
   int gt = 0, eq = 0;
@@ -221,6 +299,249 @@ __device__ __forceinline__ void block_topk(const uint32_t* keys, int n, int k, i
     bool take = key > T;
     if (key == T && taken < eq_take) { take = true; ++taken; }
     if (take) out[pos++] = j;
+  }
+  __syncthreads();
+}
+
+// Rounds a shared-memory int pointer up to a 16-byte boundary (the top-k
+// scratch holds 64-bit entries).
+__device__ __forceinline__ int* align16(int* p) {
+  return reinterpret_cast<int*>((reinterpret_cast<uintptr_t>(p) + 15) & ~static_cast<uintptr_t>(15));
+}
+
+// The k-th largest (1-based) of the values v[0..cnt) (shared memory, all
+// non-zero, cnt <= 4 * blockDim.x, 1 <= kth <= cnt).  Returns it in *T and in
+// *need how many of the values equal to it are within the top kth.  Radix
+// select from the highest bit in which the values differ, 8 bits per pass,
+// each thread holding up to 4 values in registers and each warp counting into
+// its own 256-bin histogram.  All threads of the block must call it.
+__device__ __forceinline__ void block_kth(const uint32_t* v, int cnt, int kth, int* scratch, uint32_t* T,
+                                          int* need_out) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthr = blockDim.x;
+  const int nwarps = nthr >> 5;
+  int* whist = scratch;                     // [nwarps][256]
+  int* hist = scratch + nwarps * 256;       // [256]
+  int* bc = hist + 256;                     // broadcast slots
+  uint32_t x[4];
+  uint32_t lo = 0xffffffffu, hi = 0u;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int i = tid + q * nthr;
+    x[q] = i < cnt ? v[i] : 0u;
+    if (x[q]) { lo = min(lo, x[q]); hi = max(hi, x[q]); }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  if (lane == 0) { whist[warp] = static_cast<int>(lo); whist[32 + warp] = static_cast<int>(hi); }
+  __syncthreads();
+  if (tid < 32) {
+    uint32_t m = tid < nwarps ? static_cast<uint32_t>(whist[tid]) : 0xffffffffu;
+    uint32_t M = tid < nwarps ? static_cast<uint32_t>(whist[32 + tid]) : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      m = min(m, __shfl_xor_sync(0xffffffffu, m, o));
+      M = max(M, __shfl_xor_sync(0xffffffffu, M, o));
+    }
+    if (tid == 0) { bc[2] = static_cast<int>(m); bc[3] = static_cast<int>(M); }
+  }
+  __syncthreads();
+  const uint32_t vmin = static_cast<uint32_t>(bc[2]);
+  const uint32_t span = static_cast<uint32_t>(bc[3]) - vmin;
+  int hb = span ? 32 - __clz(span) : 1;
+  uint32_t prefix = 0, pmask = 0;
+  int need = kth;
+  while (hb > 0) {
+    const int width = hb < 8 ? hb : 8;
+    const int shift = hb - width;
+    const uint32_t dmask = (1u << width) - 1u;
+    int* wh = whist + warp * 256;
+    for (int i = lane; i < 256; i += 32) wh[i] = 0;
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t r = x[q] - vmin;
+      if (x[q] && (r & pmask) == prefix) atomicAdd(&wh[(r >> shift) & dmask], 1);
+    }
+    __syncthreads();
+    for (int i = tid; i < 256; i += nthr) {
+      int acc = 0;
+      for (int w = 0; w < nwarps; ++w) acc += whist[w * 256 + i];
+      hist[i] = acc;
+    }
+    __syncthreads();
+    if (tid < 32) {
+      int cnt8[8], sum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) { cnt8[i] = hist[255 - 8 * lane - i]; sum += cnt8[i]; }
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned hit = __ballot_sync(0xffffffffu, incl >= need);
+      const int first = __ffs(hit) - 1;
+      if (lane == first) {
+        int acc = incl - sum, digit = 255 - 8 * lane;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (acc + cnt8[i] >= need) { digit = 255 - 8 * lane - i; break; }
+          acc += cnt8[i];
+        }
+        bc[0] = digit;
+        bc[1] = need - acc;
+      }
+    }
+    __syncthreads();
+    prefix |= static_cast<uint32_t>(bc[0]) << shift;
+    pmask |= dmask << shift;
+    need = bc[1];
+    hb = shift;
+    __syncthreads();
+  }
+  *T = vmin + prefix;
+  *need_out = need;
+}
+
+// Block-wide selection of the k largest keys among keys[0..n) (shared
+// memory), ties broken toward the lower index; key 0 marks an excluded entry
+// and is never chosen when at least k keys are non-zero.  On return out[0..k)
+// holds the chosen indices in ascending order, bits[0..ceil(n/32)) is their
+// bitmap and wpref[w] the number of chosen indices below 32 w (all three in
+// shared memory).  `scratch` holds topk_scratch_ints(blockDim.x) ints and is
+// 16-byte aligned.
+//
+// The k-th largest key T is found on small sets only: 1024 evenly spaced
+// keys give a threshold T0 a little below the k-th largest (its rank in the
+// sample leaves about 1.5k + margin keys above it in expectation); the keys
+// >= T0 (normally a few hundred) are gathered and T is their k-th largest.
+// A final pass marks every key above T and, in index order, the first keys
+// equal to T that the top k needs.  If the sample misjudges (fewer than k or
+// more than 4 blockDim.x survivors) the radix select over all keys decides
+// instead.  All threads of the block must call it.
+constexpr int kTopkSample = 1024;
+__device__ __forceinline__ void block_topk(const uint32_t* keys, int n, int k, int* out, int* scratch,
+                                           uint32_t* bits, int* wpref) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthr = blockDim.x;
+  const int nwarps = nthr >> 5;
+  const int nw = (n + 31) >> 5;
+  const int cap = 4 * nthr;
+  uint32_t* vals = reinterpret_cast<uint32_t*>(scratch);   // cap values
+  int* ks = scratch + cap;                                  // block_kth scratch
+  int* tmp = ks + (nthr / 32) * 256 + 256 + 8;              // 40 ints for the scans
+  int* cnt_slot = tmp + 36;                                 // survivor counter
+  // each warp owns a contiguous range of 32-key rows; lanes read consecutive
+  // keys, so shared-memory reads are conflict-free
+  const int rows = (n + 31) >> 5;
+  const int rpw = (rows + nwarps - 1) / nwarps;
+  const int r0 = warp * rpw, r1 = min(rows, r0 + rpw);
+  uint32_t T = 0;
+  int need = 0;
+  bool ok = true;
+  if (tid == 0) *cnt_slot = 0;
+  __syncthreads();
+  uint32_t T0 = 1u;                  // keys >= T0 are gathered (all non-zero keys when n <= cap)
+  if (n > cap) {
+    const int S = kTopkSample;
+    // non-zero samples of evenly spaced keys (order irrelevant)
+    for (int s2 = tid; s2 < ((S + 31) & ~31); s2 += nthr) {
+      const uint32_t x = s2 < S ? keys[static_cast<int>((static_cast<long long>(s2) * n) / S)] : 0u;
+      const unsigned m = __ballot_sync(0xffffffffu, x != 0u);
+      int base = 0;
+      if (lane == 0 && m) base = atomicAdd(cnt_slot, __popc(m));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      if (x) vals[base + __popc(m & ((1u << lane) - 1u))] = x;
+    }
+    __syncthreads();
+    const int tot = *cnt_slot;
+    // rank r (0-based) among the samples: expected survivors ~ (r + 1) n / S
+    int r = static_cast<int>((3LL * k * S + 2LL * n - 1) / (2LL * n)) + 12;
+    if (r > tot - 1) r = tot - 1;
+    T0 = 0xffffffffu;                // no non-zero sample: no survivor, radix decides
+    int dummy;
+    if (tot > 0) block_kth(vals, tot, r + 1, ks, &T0, &dummy);
+    __syncthreads();
+    if (tid == 0) *cnt_slot = 0;
+    __syncthreads();
+  }
+  // gather the survivors (keys >= T0, non-zero) while they fit in `vals`
+  for (int row = r0; row < r1; ++row) {
+    const int j = row * 32 + lane;
+    const uint32_t key = j < n ? keys[j] : 0u;
+    const bool keep = key != 0u && key >= T0;
+    const unsigned m = __ballot_sync(0xffffffffu, keep);
+    int base = 0;
+    if (lane == 0 && m) base = atomicAdd(cnt_slot, __popc(m));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    const int pos = base + __popc(m & ((1u << lane) - 1u));
+    if (keep && pos < cap) vals[pos] = key;
+  }
+  __syncthreads();
+  const int nsurv = *cnt_slot;
+  ok = nsurv >= k && nsurv <= cap;
+  if (ok) block_kth(vals, nsurv, k, ks, &T, &need);
+  for (int w = tid; w < nw; w += nthr) bits[w] = 0u;
+  __syncthreads();
+  if (ok) {
+    // every key above T; the keys equal to T in index order until `need`
+    int eq = 0;
+    for (int row = r0; row < r1; ++row) {
+      const int j = row * 32 + lane;
+      const uint32_t key = j < n ? keys[j] : 0u;
+      const unsigned gt = __ballot_sync(0xffffffffu, key > T);
+      if (lane == 0) bits[row] = gt;
+      eq += __popc(__ballot_sync(0xffffffffu, key == T));
+    }
+    // warp totals of equal keys -> exclusive prefix over warps
+    if (lane == 0) tmp[warp] = eq;
+    __syncthreads();
+    if (warp == 0) {
+      int v = lane < nwarps ? tmp[lane] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      __syncwarp();
+      if (lane < nwarps) tmp[lane] = incl - v;
+    }
+    __syncthreads();
+    int before = tmp[warp];
+    for (int row = r0; row < r1 && before < need; ++row) {
+      const int j = row * 32 + lane;
+      const uint32_t key = j < n ? keys[j] : 0u;
+      const unsigned e = __ballot_sync(0xffffffffu, key == T);
+      const int rank = before + __popc(e & ((1u << lane) - 1u));
+      const unsigned take = __ballot_sync(0xffffffffu, key == T && rank < need);
+      if (lane == 0) bits[row] |= take;
+      before += __popc(e);
+    }
+  } else {
+    block_topk_radix(keys, n, k, out, scratch);
+    for (int i = tid; i < k; i += nthr) atomicOr(&bits[out[i] >> 5], 1u << (out[i] & 31));
+  }
+  __syncthreads();
+  // prefix popcounts per word, then the ascending list from the bitmap
+  {
+    const int per = (nw + nthr - 1) / nthr;
+    const int w0 = tid * per, w1 = min(nw, w0 + per);
+    int cnt = 0;
+    for (int w = w0; w < w1; ++w) cnt += __popc(bits[w]);
+    int tot;
+    int ex = block_exclusive_scan(cnt, tmp, &tot);
+    for (int w = w0; w < w1; ++w) {
+      wpref[w] = ex;
+      uint32_t b = bits[w];
+      while (b) {
+        const int bit = __ffs(b) - 1;
+        out[ex++] = w * 32 + bit;
+        b &= b - 1;
+      }
+    }
   }
   __syncthreads();
 }

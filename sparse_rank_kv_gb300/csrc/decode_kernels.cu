@@ -70,10 +70,10 @@ k_score(const T* __restrict__ L, const T* __restrict__ q, const uint32_t* __rest
 // ----------------------------------------------------------------- select
 // One block per (batch, KV head).  Shared memory: keys[n], then the cache
 // bookkeeping arrays.
-template <typename T, int D>
+template <typename T, int D, int G>
 __global__ void __launch_bounds__(kSelectThreads)
 k_select(const float* __restrict__ P, const float2* __restrict__ part,
-         const uint32_t* __restrict__ mask, int G, int n, int ntile, int k, int group_reduce,
+         const uint32_t* __restrict__ mask, int n, int ntile, int k, int group_reduce,
          int cache_on, int32_t* __restrict__ sel, int32_t* __restrict__ sel_slot,
          int32_t* __restrict__ slot_chunk, int32_t* __restrict__ miss_chunk,
          int32_t* __restrict__ miss_slot, int32_t* __restrict__ miss_count,
@@ -90,9 +90,9 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part,
   int* s_hit = s_slot + k;
   int* s_keep = s_hit + k;
   int* s_free = s_keep + k;
-  int* scratch = s_free + k;   // 300 ints
-  float* lse = reinterpret_cast<float*>(scratch + 300);  // G floats
-  int* tmp = scratch + 256;
+  int* scratch = align16(s_free + k);   // topk_scratch_ints(kSelectThreads) ints, 16-byte aligned
+  float* lse = reinterpret_cast<float*>(scratch + topk_scratch_ints(kSelectThreads));  // G floats
+  int* tmp = scratch;          // block scans after the top-k
 
   const int pair = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthr = blockDim.x;
@@ -123,6 +123,45 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part,
   __syncthreads();
   // selection keys: S2 per chunk, 0 for outliers
   const uint32_t* mk = mask + static_cast<size_t>(pair) * nw;
+  auto key_of = [&](float sc_max, float sc_sum, bool excluded) -> uint32_t {
+    if (excluded) return 0u;
+    return group_reduce == 0 ? order_key(sc_max) : __float_as_uint(sc_sum) + 1u;
+  };
+  if ((n & 3) == 0) {
+    // 16-byte loads of 4 consecutive chunks per head; a batch of IT x G loads
+    // is issued before any key of the batch is computed
+    constexpr int IT = G >= 8 ? 1 : 8 / G;
+    const float4* P4 = reinterpret_cast<const float4*>(P + static_cast<size_t>(pair) * G * n);
+    const int n4 = n >> 2;
+    for (int jb = 0; jb < n4; jb += IT * nthr) {
+      float4 v[IT][G];
+#pragma unroll
+      for (int it = 0; it < IT; ++it) {
+        const int j4 = jb + it * nthr + tid;
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+          v[it][g] = j4 < n4 ? __ldcg(P4 + static_cast<size_t>(g) * n4 + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int it = 0; it < IT; ++it) {
+        const int j4 = jb + it * nthr + tid;
+        if (j4 >= n4) continue;
+        const uint32_t mbits = mk[j4 >> 3] >> ((j4 & 7) * 4);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float smax = -INFINITY, ssum = 0.f;
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const float pv = e == 0 ? v[it][g].x : e == 1 ? v[it][g].y : e == 2 ? v[it][g].z : v[it][g].w;
+            const float x = pv - lse[g];
+            smax = fmaxf(smax, x);
+            if (group_reduce) ssum += __expf(x);
+          }
+          keys[4 * j4 + e] = key_of(smax, ssum, (mbits >> e) & 1u);
+        }
+      }
+    }
+  } else
   for (int j = tid; j < n; j += nthr) {
     uint32_t key = 0;
     if (!((mk[j >> 5] >> (j & 31)) & 1u)) {
@@ -141,22 +180,8 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part,
     keys[j] = key;
   }
   __syncthreads();
-  block_topk(keys, n, k, s_sel, scratch);
-
-  // bitmap of the selection and prefix popcounts per 32-chunk word
-  for (int i = tid; i < nw; i += nthr) words[i] = 0u;
-  __syncthreads();
-  for (int i = tid; i < k; i += nthr) atomicOr(&words[s_sel[i] >> 5], 1u << (s_sel[i] & 31));
-  __syncthreads();
-  {
-    const int per = (nw + nthr - 1) / nthr;
-    const int w0 = tid * per, w1 = min(nw, w0 + per);
-    int cnt = 0;
-    for (int w = w0; w < w1; ++w) cnt += __popc(words[w]);
-    int tot;
-    int ex = block_exclusive_scan(cnt, tmp, &tot);
-    for (int w = w0; w < w1; ++w) { wpref[w] = ex; ex += __popc(words[w]); }
-  }
+  // the selection (ascending), its bitmap and per-word prefix popcounts
+  block_topk(keys, n, k, s_sel, scratch, words, wpref);
   for (int i = tid; i < k; i += nthr) s_hit[i] = 0;
   __syncthreads();
   // slots whose chunk is selected again keep it (hits)
@@ -300,24 +325,34 @@ cudaError_t launch_score(Ctx& c, const void* q, cudaStream_t st) {
 
 size_t select_smem_bytes(int n, int k, int G) {
   const int nw = (n + 31) / 32;
-  return sizeof(uint32_t) * (static_cast<size_t>(n) + 2 * nw) + sizeof(int) * (5 * static_cast<size_t>(k) + 300) +
-         sizeof(float) * G + 16;
+  return sizeof(uint32_t) * (static_cast<size_t>(n) + 2 * nw) +
+         sizeof(int) * (5 * static_cast<size_t>(k) + topk_scratch_ints(kSelectThreads)) + sizeof(float) * G + 16;
 }
 
-template <typename T, int D>
+template <typename T, int D, int G>
 static cudaError_t select_t(Ctx& c, const void* k_new, const void* v_new, int loc_row,
                             cudaStream_t st) {
   const size_t smem = select_smem_bytes(c.n, c.p.k, c.G);
-  auto kern = k_select<T, D>;
+  auto kern = k_select<T, D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   kern<<<c.p.b * c.p.h_kv, kSelectThreads, smem, st>>>(
-      c.logits, c.score_part, c.out_mask, c.G, c.n, c.ntile, c.p.k, c.p.group_reduce,
+      c.logits, c.score_part, c.out_mask, c.n, c.ntile, c.p.k, c.p.group_reduce,
       c.cache_on ? 1 : 0, c.sel, c.sel_slot, c.slot_chunk, c.miss_chunk, c.miss_slot,
       c.miss_count, c.hits, c.counters, static_cast<const T*>(k_new), static_cast<const T*>(v_new),
       static_cast<T*>(c.K_loc), static_cast<T*>(c.V_loc), loc_row, c.loc_cap, c.status);
   return cudaGetLastError();
+}
+
+template <typename T, int D>
+static cudaError_t select_g(Ctx& c, const void* k_new, const void* v_new, int loc_row, cudaStream_t st) {
+  switch (c.G) {
+    case 1: return select_t<T, D, 1>(c, k_new, v_new, loc_row, st);
+    case 2: return select_t<T, D, 2>(c, k_new, v_new, loc_row, st);
+    case 4: return select_t<T, D, 4>(c, k_new, v_new, loc_row, st);
+    default: return select_t<T, D, 8>(c, k_new, v_new, loc_row, st);
+  }
 }
 
 cudaError_t launch_select(Ctx& c, const void* k_new, const void* v_new, int loc_row,
@@ -325,11 +360,11 @@ cudaError_t launch_select(Ctx& c, const void* k_new, const void* v_new, int loc_
   kbegin(c, K_SELECT, st);
   cudaError_t e;
   if (c.p.dtype == SKV_DTYPE_BF16)
-    e = c.p.d == 128 ? select_t<bf16, 128>(c, k_new, v_new, loc_row, st)
-                     : select_t<bf16, 64>(c, k_new, v_new, loc_row, st);
+    e = c.p.d == 128 ? select_g<bf16, 128>(c, k_new, v_new, loc_row, st)
+                     : select_g<bf16, 64>(c, k_new, v_new, loc_row, st);
   else
-    e = c.p.d == 128 ? select_t<float, 128>(c, k_new, v_new, loc_row, st)
-                     : select_t<float, 64>(c, k_new, v_new, loc_row, st);
+    e = c.p.d == 128 ? select_g<float, 128>(c, k_new, v_new, loc_row, st)
+                     : select_g<float, 64>(c, k_new, v_new, loc_row, st);
   kend(c, K_SELECT, st);
   return e;
 }

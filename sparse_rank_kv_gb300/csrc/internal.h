@@ -88,7 +88,7 @@ struct Ctx {
 };
 
 size_t select_smem_bytes(int n, int k, int G);
-size_t attn_smem_bytes(int E, int G, int D, int S);
+size_t attn_smem_bytes(int E, int G, int D, int S, int max_splits);
 
 // ------------------------------------------------------------ launch hooks
 // Every launcher brackets its kernel with kbegin/kend (api.cu): they count

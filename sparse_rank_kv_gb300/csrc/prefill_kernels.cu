@@ -89,14 +89,17 @@ k_chunkstats(const T* __restrict__ K, const float2* __restrict__ rope_tab, T* __
 __global__ void __launch_bounds__(1024)
 k_outlier_select(const float* __restrict__ mcos, int32_t* __restrict__ out_ids, int n, int o) {
   extern __shared__ __align__(16) unsigned char smem[];
+  const int nw = (n + 31) >> 5;
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
-  int* s_out = reinterpret_cast<int*>(keys + n);
-  int* scratch = s_out + o;
+  uint32_t* bits = keys + n;
+  int* wpref = reinterpret_cast<int*>(bits + nw);
+  int* s_out = wpref + nw;
+  int* scratch = align16(s_out + o);
   const int pair = blockIdx.x;
   for (int j = threadIdx.x; j < n; j += blockDim.x)
     keys[j] = order_key(-mcos[static_cast<size_t>(pair) * n + j]);
   __syncthreads();
-  block_topk(keys, n, o, s_out, scratch);
+  block_topk(keys, n, o, s_out, scratch, bits, wpref);
   for (int i = threadIdx.x; i < o; i += blockDim.x) out_ids[static_cast<size_t>(pair) * o + i] = s_out[i];
 }
 
@@ -398,7 +401,7 @@ static cudaError_t prefill_stats(Ctx& c, const T* K, const T* V, cudaStream_t st
   kend(c, K_CHUNKSTATS, st);
   SKV_TRY(cudaGetLastError());
   if (o > 0) {
-    const size_t smem = sizeof(uint32_t) * n + sizeof(int) * (o + 300) + 16;
+    const size_t smem = sizeof(uint32_t) * (n + 2 * ((n + 31) / 32)) + sizeof(int) * (o + topk_scratch_ints(1024)) + 16;
     SKV_TRY(cudaFuncSetAttribute(k_outlier_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem)));
     kbegin(c, K_OUTLIERS, st);

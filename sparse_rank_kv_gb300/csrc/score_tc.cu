@@ -11,11 +11,14 @@
 //               G are zero-filled by TMA) into a 5-stage shared-memory ring,
 //               K-major with the 64-byte swizzle
 //   warp 1    : tcgen05.mma (M=128, N=16, K=16) x (d/16) per tile into one of
-//               two TMEM accumulators; commits free the ring slot and publish
+//               four TMEM accumulators; commits free the ring slot and publish
 //               the accumulator
-//   warps 2-5 : epilogue -- one landmark row per thread (TMEM lane), scale,
-//               store the G logits, and per 32-row warp the running max and
-//               sum of exp over the non-outlier rows (softmax partials)
+//   warps 2-9 : epilogue, two warpgroups taking alternate tiles (four TMEM
+//               accumulators let the MMAs run ahead) -- one landmark row per
+//               thread (TMEM lane), scale, store the G logits, and per 32-row
+//               warp the max and sum of exp over the non-outlier rows (softmax
+//               partials); the outlier-mask word of the group's next tile is
+//               loaded before waiting on the current one
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -26,7 +29,8 @@ namespace skv {
 
 constexpr int kScTile = 128;
 constexpr int kScStages = 5;
-constexpr int kScThreads = 192;
+constexpr int kScThreads = 320;
+constexpr int kScAcc = 4;        // TMEM accumulators of 16 columns
 
 __host__ __device__ constexpr int sc_stage_bytes(int D) { return (D / 32) * (kScTile + 16) * 64; }
 __host__ __device__ constexpr int sc_smem_bytes(int D) {
@@ -47,8 +51,8 @@ k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUt
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kScStages;
   uint64_t* tfull = empty + kScStages;
-  uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* tempty = tfull + kScAcc;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + kScAcc);
   unsigned char* stages = smem + 1024;
 
   const int t_begin = static_cast<int>(static_cast<long long>(total_tiles) * blockIdx.x / gridDim.x);
@@ -63,14 +67,14 @@ k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUt
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < kScAcc; ++a) {
       tc::mbar_init(&tfull[a], 1);
       tc::mbar_init(&tempty[a], 128);
     }
     tc::fence_mbar_init();
   }
   if (warp == 1) {
-    tc::tmem_alloc(tmem_slot, 32);
+    tc::tmem_alloc(tmem_slot, 16 * kScAcc);
     tc::tmem_relinquish();
   }
   tc::fence_before();
@@ -105,8 +109,8 @@ k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUt
       for (int i = 0; i < ntl; ++i) {
         const int s = i % kScStages;
         const uint32_t ph = (i / kScStages) & 1;
-        const int a = i & 1;
-        const uint32_t tph = (i >> 1) & 1;
+        const int a = i % kScAcc;
+        const uint32_t tph = (i / kScAcc) & 1;
         if (!tc::mbar_wait(&full[s], ph, kWaitLimit) || !tc::mbar_wait(&tempty[a], tph ^ 1, kWaitLimit)) {
           flag_error(status, DEV_TIMEOUT);
           break;
@@ -128,11 +132,21 @@ k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUt
     }
   } else {
     const int q4 = warp & 3;               // TMEM lane quarter of this warp
+    const int eg = (warp - 2) >> 2;        // epilogue warpgroup: tiles eg, eg + 2, ...
     const int row = q4 * 32 + lane;
     const int nw = (n + 31) >> 5;
-    for (int i = 0; i < ntl; ++i) {
-      const int a = i & 1;
-      const uint32_t tph = (i >> 1) & 1;
+    auto mask_word = [&](int i) -> uint32_t {
+      if (i >= ntl) return 0u;
+      const int tile = t_begin + i;
+      const int pair = tile / ntile, ti = tile - pair * ntile;
+      const int w = ti * (kScTile / 32) + q4;
+      return w < nw ? __ldg(&mask[static_cast<size_t>(pair) * nw + w]) : 0u;
+    };
+    uint32_t mword = mask_word(eg);
+    for (int i = eg; i < ntl; i += 2) {
+      const uint32_t mnext = mask_word(i + 2);
+      const int a = i % kScAcc;
+      const uint32_t tph = (i / kScAcc) & 1;
       const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(&tfull[a], tph, kWaitLimit));
       if (!ok) {
         if (lane == 0) flag_error(status, DEV_TIMEOUT);
@@ -148,7 +162,7 @@ k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUt
       const int tile = t_begin + i;
       const int pair = tile / ntile, ti = tile - pair * ntile;
       const int j = ti * kScTile + row;
-      const bool valid = j < n && !((mask[static_cast<size_t>(pair) * nw + (j >> 5)] >> (j & 31)) & 1u);
+      const bool valid = j < n && !((mword >> lane) & 1u);
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         const float x = acc[g] * scale;
@@ -157,11 +171,12 @@ k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUt
         const float e = warp_sum(valid ? __expf(x - m) : 0.f);
         if (lane == 0) part[((static_cast<size_t>(pair) * G + g) * ntile + ti) * 4 + q4] = make_float2(m, e);
       }
+      mword = mnext;
     }
   }
   tc::fence_before();
   __syncthreads();
-  if (warp == 1) tc::tmem_dealloc(tmem, 32);
+  if (warp == 1) tc::tmem_dealloc(tmem, 16 * kScAcc);
 }
 
 bool tc_score_supported(const shadowkv_params& p) {

@@ -213,3 +213,14 @@ def test_bad_outlier_ids_are_reported():
                          ids=["r48", "c16"])
 def test_rebuild_shape_variants_against_oracle(cfg):
     run_parity(cfg, steps=3)
+
+
+def test_selection_with_massive_ties():
+    """Most landmarks equal: the sampled threshold admits far more than 2048
+    survivors, so the radix select decides; ties go to the lower index."""
+    cfg = CONFIGS["llama_b1_s32k"].with_(b=1, steps=3, seed=60)
+    st = synth.make_state(cfg, device="cuda")
+    hot = st["L"][:, :, :20].clone()
+    st["L"].zero_()
+    st["L"][:, :, 100:120] = hot
+    run_parity(cfg, steps=3)
