@@ -192,6 +192,36 @@ skv_status shadowkv_get_stats(shadowkv_ctx* ctx, shadowkv_stats* out);
  * SKV_ERR_DEVICE_CHECK if any kernel recorded a violation. */
 skv_status shadowkv_check(shadowkv_ctx* ctx);
 
+/* ----------------------------------------------- attention without allocation
+ * (no counterpart in the paper: a service for callers that cannot allocate)
+ *
+ * Some callers cannot call cudaMalloc: an inference engine that hands every
+ * byte of device memory to its own pool at start-up, or code that records a
+ * decode loop into a CUDA graph and must not allocate inside it.  This entry
+ * point runs the library's split-KV GQA attention kernel on keys and values
+ * the caller already holds and allocates nothing: its scratch (the per-split
+ * partial results and the per-head completion tickets) lives in one static
+ * device array of SKV_NOALLOC_SCRATCH_BYTES that the library image carries,
+ * so every GPU that loads the library holds that array until the process
+ * exits.
+ *   p        : b, h_q, h_kv, d and dtype are used (h_q / h_kv in {1,2,4,8},
+ *              d in {64, 128}); the other fields are ignored.
+ *   q        : device, b x h_q x d, post-RoPE queries.
+ *   K, V     : device, b x h_kv x n_tokens x d, post-RoPE keys and values.
+ *   out      : device, b x h_q x d; out = softmax(q K^T / sqrt(d)) V, query
+ *              head g reading KV head g / G.
+ * Needs b * h_q * ceil(n_tokens / 128) * (d + 2) * 4 bytes of partials plus
+ * 256 bytes of tickets; larger problems return SKV_ERR_UNSUPPORTED.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call shares the one array and clears the
+ * tickets it needs, so calls whose GPU work overlaps (different streams, or
+ * different host threads on the same device without ordering) race; order
+ * them on one stream.  Asynchronous on `stream`. */
+#define SKV_NOALLOC_SCRATCH_BYTES (8u << 20)
+skv_status shadowkv_attention_noalloc(const shadowkv_params* p, const void* q, const void* K,
+                                      const void* V, int n_tokens, void* out, void* stream);
+
 /* ------------------------------------------------------ timing / counting */
 /* Kernels are numbered 0..shadowkv_num_kernels()-1 with stable names. */
 int shadowkv_num_kernels(void);

@@ -93,6 +93,7 @@ def lib() -> ctypes.CDLL:
             "shadowkv_reset_timers": (I, [V]),
             "shadowkv_field_bytes": (I, [V, I, P(S)]),
             "shadowkv_export": (I, [V, I, V, S]),
+            "shadowkv_attention_noalloc": (I, [P(Params), V, V, V, I, V, V]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -228,6 +229,14 @@ def prefill(p: Params, k_pre: torch.Tensor, v: torch.Tensor, stream=None) -> Con
     _check(lib().shadowkv_prefill(ctypes.byref(p), _ptr(k_pre), _ptr(v), int(not v.is_cuda),
                                   _stream(stream), ctypes.byref(h)))
     return Context(h, p)
+
+
+def attention_noalloc(p: Params, q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, out: torch.Tensor,
+                      stream=None) -> None:
+    """softmax(q K^T / sqrt(d)) V over K, V (b, h_kv, n_tokens, d) on the device,
+    with the library's static scratch instead of any allocation."""
+    _check(lib().shadowkv_attention_noalloc(ctypes.byref(p), _ptr(q), _ptr(K), _ptr(V),
+                                            int(K.shape[2]), _ptr(out), _stream(stream)))
 
 
 def load_state(p: Params, st: dict, stream=None) -> Context:

@@ -324,6 +324,13 @@ static void drain_timers(skv::Ctx& c) {
   c.pending.clear();
 }
 
+namespace skv {
+skv_status set_error(skv_status st, const char* msg) {
+  g_err = msg;
+  return st;
+}
+}  // namespace skv
+
 // ============================================================== C ABI
 extern "C" {
 

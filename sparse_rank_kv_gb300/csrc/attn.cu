@@ -12,6 +12,9 @@
 // (max, sum, sum p v) per head; the last block of the pair (atomic ticket)
 // combines the splits in split order, so the result does not depend on which
 // block finishes last.
+#include <cstdio>
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -311,3 +314,110 @@ cudaError_t launch_attn(Ctx& c, const void* q, void* out, int n_loc, cudaStream_
 }
 
 }  // namespace skv
+
+// ============================================= attention without allocation
+// Scratch of shadowkv_attention_noalloc: split partials, then 256 bytes of
+// tickets.  One copy per device, alive until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SKV_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device (the symbol's host-side name is not a device address).
+cudaError_t noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+template <typename T, int D, int G>
+cudaError_t noalloc_launch(const shadowkv_params& p, const void* q, const void* K, const void* V,
+                           int n_tokens, void* out, float* part, int32_t* ticket, int nsplit,
+                           cudaStream_t st) {
+  constexpr int S = 128;
+  const size_t smem = skv::attn_smem_bytes(sizeof(T), G, D, S, nsplit);
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  auto kern = skv::k_attn<T, D, G>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
+  // every token is one plain segment: no rebuilt chunks, no local window
+  kern<<<dim3(p.b * p.h_kv, nsplit), skv::kAt, smem, st>>>(
+      static_cast<const T*>(K), static_cast<const T*>(V), static_cast<const T*>(K),
+      static_cast<const T*>(V), nullptr, static_cast<const T*>(K), static_cast<const T*>(V),
+      static_cast<const T*>(q), static_cast<T*>(out), part, ticket, n_tokens, 0, 0, 0, 1, 0, 1, S,
+      nsplit, nsplit, scale_log2);
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t noalloc_g(const shadowkv_params& p, const void* q, const void* K, const void* V,
+                      int n_tokens, void* out, float* part, int32_t* ticket, int nsplit,
+                      cudaStream_t st) {
+  switch (p.h_q / p.h_kv) {
+    case 1: return noalloc_launch<T, D, 1>(p, q, K, V, n_tokens, out, part, ticket, nsplit, st);
+    case 2: return noalloc_launch<T, D, 2>(p, q, K, V, n_tokens, out, part, ticket, nsplit, st);
+    case 4: return noalloc_launch<T, D, 4>(p, q, K, V, n_tokens, out, part, ticket, nsplit, st);
+    default: return noalloc_launch<T, D, 8>(p, q, K, V, n_tokens, out, part, ticket, nsplit, st);
+  }
+}
+}  // namespace
+
+extern "C" skv_status shadowkv_attention_noalloc(const shadowkv_params* p, const void* q,
+                                                 const void* K, const void* V, int n_tokens,
+                                                 void* out, void* stream) {
+  using skv::set_error;
+  if (!p || !q || !K || !V || !out) return set_error(SKV_ERR_INVALID_ARG, "NULL argument");
+  if (p->b < 1 || p->h_kv < 1 || p->h_q < 1 || p->h_q % p->h_kv)
+    return set_error(SKV_ERR_INVALID_ARG, "need b, h_kv >= 1 and h_q a multiple of h_kv");
+  const int G = p->h_q / p->h_kv;
+  if (G != 1 && G != 2 && G != 4 && G != 8)
+    return set_error(SKV_ERR_UNSUPPORTED, "h_q / h_kv must be 1, 2, 4 or 8");
+  if (p->d != 64 && p->d != 128) return set_error(SKV_ERR_UNSUPPORTED, "d must be 64 or 128");
+  if (p->dtype != SKV_DTYPE_F32 && p->dtype != SKV_DTYPE_BF16)
+    return set_error(SKV_ERR_INVALID_ARG, "bad dtype");
+  if (n_tokens < 1) return set_error(SKV_ERR_INVALID_ARG, "n_tokens must be >= 1");
+  const int nsplit = (n_tokens + 127) / 128;
+  const size_t part_bytes = static_cast<size_t>(p->b) * p->h_q * nsplit * (p->d + 2) * sizeof(float);
+  const size_t ticket_bytes = static_cast<size_t>(p->b) * p->h_kv * sizeof(int32_t);
+  const size_t part_room = (static_cast<size_t>(SKV_NOALLOC_SCRATCH_BYTES) - 256) & ~static_cast<size_t>(255);
+  if (part_bytes > part_room || ticket_bytes > 256) {
+    char msg[200];
+    snprintf(msg, sizeof(msg),
+             "attention_noalloc needs %zu bytes of partials and %zu of tickets; the static scratch "
+             "holds %zu and 256",
+             part_bytes, ticket_bytes, part_room);
+    return set_error(SKV_ERR_UNSUPPORTED, msg);
+  }
+  void* base = nullptr;
+  cudaError_t e = noalloc_scratch(&base);
+  if (e != cudaSuccess) return set_error(SKV_ERR_CUDA, cudaGetErrorString(e));
+  float* part = static_cast<float*>(base);
+  int32_t* ticket = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(base) + part_room);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  e = cudaMemsetAsync(ticket, 0, ticket_bytes, st);   // the kernel's tickets start at zero
+  if (e == cudaSuccess) {
+    if (p->dtype == SKV_DTYPE_BF16)
+      e = p->d == 128 ? noalloc_g<skv::bf16, 128>(*p, q, K, V, n_tokens, out, part, ticket, nsplit, st)
+                      : noalloc_g<skv::bf16, 64>(*p, q, K, V, n_tokens, out, part, ticket, nsplit, st);
+    else
+      e = p->d == 128 ? noalloc_g<float, 128>(*p, q, K, V, n_tokens, out, part, ticket, nsplit, st)
+                      : noalloc_g<float, 64>(*p, q, K, V, n_tokens, out, part, ticket, nsplit, st);
+  }
+  if (e != cudaSuccess) return set_error(SKV_ERR_CUDA, cudaGetErrorString(e));
+  return SKV_OK;
+}

@@ -90,6 +90,9 @@ struct Ctx {
 size_t select_smem_bytes(int n, int k, int G);
 size_t attn_smem_bytes(int E, int G, int D, int S, int max_splits);
 
+// Records the text of a failure for shadowkv_last_error (api.cu).
+skv_status set_error(skv_status st, const char* msg);
+
 // ------------------------------------------------------------ launch hooks
 // Every launcher brackets its kernel with kbegin/kend (api.cu): they count
 // the launch and, with timing on, record CUDA events on the launch stream.
