@@ -311,7 +311,7 @@ def run_ours(args, cfg):
         score_ms, score_n = kt["score"]
         score_bytes = E * cfg.b * cfg.h_kv * cfg.n * cfg.d
         achieved = score_bytes / (score_ms / score_n * 1e-3) / 1e9
-        traffic = traffic_from_profile("score_kernel_b8_s128k.md", "decode_kernels.cu")
+        traffic = traffic_from_profile("score_kernel_b8_s128k.md", "score_tc.cu")
         per_kernel = {k_: {"ms_per_step": v[0] / K, "launches": v[1]} for k_, v in kt.items() if v[1]}
         value = ws * cfg.b / (ms_step * 1e-3)
         result = {

@@ -97,7 +97,8 @@ Sizes sizes_of(const shadowkv_params& p) {
   z.out_ids = b * h * o * 4;
   z.out_mask = b * h * nw * 4;
   z.sel = z.sel_slot = z.slot_chunk = z.miss_chunk = z.miss_slot = b * h * k * 4;
-  z.miss_count = z.hits = z.attn_count = b * h * 4;
+  z.hits = z.attn_count = b * h * 4;
+  z.miss_count = 2 * 4;   // compact miss-list length per step parity
   z.counters = 2 * 8;
   z.status = 4;
   return z;
@@ -124,6 +125,8 @@ skv_status validate(const shadowkv_params* p) {
     return fail(SKV_ERR_INVALID_ARG, "need 1 <= r <= min(s, h_kv*d) (r=%d)", q.r);
   if (q.r > 256) return fail(SKV_ERR_UNSUPPORTED, "r = %d > 256", q.r);
   if (q.max_new < 0) return fail(SKV_ERR_INVALID_ARG, "max_new must be >= 0");
+  if (static_cast<long long>(q.b) * q.h_kv * n >= (1LL << 31))
+    return fail(SKV_ERR_UNSUPPORTED, "b * h_kv * n must be < 2^31 (32-bit chunk ids)");
   if (static_cast<long long>(q.s) + q.max_new >= (1LL << 24))
     return fail(SKV_ERR_UNSUPPORTED, "s + max_new must be < 2^24 (fp32-exact positions)");
   if (q.dtype != SKV_DTYPE_F32 && q.dtype != SKV_DTYPE_BF16) return fail(SKV_ERR_INVALID_ARG, "bad dtype %d", q.dtype);

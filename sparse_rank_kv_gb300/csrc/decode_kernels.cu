@@ -76,7 +76,7 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part,
          const uint32_t* __restrict__ mask, int n, int ntile, int k, int group_reduce,
          int cache_on, int32_t* __restrict__ sel, int32_t* __restrict__ sel_slot,
          int32_t* __restrict__ slot_chunk, int32_t* __restrict__ miss_chunk,
-         int32_t* __restrict__ miss_slot, int32_t* __restrict__ miss_count,
+         int32_t* __restrict__ miss_slot, int32_t* __restrict__ miss_total, int par,
          int32_t* __restrict__ hits, unsigned long long* __restrict__ counters,
          const T* __restrict__ k_new, const T* __restrict__ v_new, T* __restrict__ K_loc,
          T* __restrict__ V_loc, int loc_row, int loc_cap, int* __restrict__ status) {
@@ -208,12 +208,20 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part,
   if (is_free) s_free[frank] = tid;
   __syncthreads();
   if (nmiss != nfree) flag_error(status, DEV_BAD_COUNT);
+  // reserve this head's range of the step's compact miss list; the block of
+  // head 0 also clears the other step parity's counter for the next step
+  __shared__ int s_base;
+  if (tid == 0) {
+    s_base = atomicAdd(&miss_total[par], min(nmiss, nfree));
+    if (pair == 0) miss_total[par ^ 1] = 0;
+  }
+  __syncthreads();
   if (is_miss && mrank < nfree) {
     const int slot = s_free[mrank];
     s_slot[tid] = slot;
     sc_row[slot] = s_sel[tid];
-    miss_chunk[static_cast<size_t>(pair) * k + mrank] = s_sel[tid];
-    miss_slot[static_cast<size_t>(pair) * k + mrank] = slot;
+    miss_chunk[s_base + mrank] = pair * n + s_sel[tid];
+    miss_slot[s_base + mrank] = pair * k + slot;
   }
   __syncthreads();
   for (int i = tid; i < k; i += nthr) {
@@ -221,7 +229,6 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part,
     sel_slot[static_cast<size_t>(pair) * k + i] = s_slot[i];
   }
   if (tid == 0) {
-    miss_count[pair] = min(nmiss, nfree);
     hits[pair] = k - nmiss;
     atomicAdd(&counters[0], static_cast<unsigned long long>(k - nmiss));
     atomicAdd(&counters[1], static_cast<unsigned long long>(nmiss));
@@ -229,38 +236,48 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part,
 }
 
 // ------------------------------------------------------------------ fetch
-// Warp per missed chunk: c*d elements copied from pinned host memory (read
-// through its mapped device address) into the chunk's cache slot.
+// The step's misses form one compact list (entries pair * n + chunk and
+// pair * k + slot, count miss_total[par]).  A small fixed grid (one block per
+// SM) walks it, a warp per chunk: c*d elements read from pinned host memory
+// through its mapped device address into the chunk's cache slot.  Keeping
+// the grid small leaves the SMs to the key rebuild running alongside.
 template <typename T>
 __global__ void __launch_bounds__(kFetchWarps * 32)
 k_fetch(const T* __restrict__ vcpu, T* __restrict__ slot_V, const int32_t* __restrict__ miss_chunk,
-        const int32_t* __restrict__ miss_slot, const int32_t* __restrict__ miss_count, int s,
-        int n, int c, int d, int k, int* __restrict__ status) {
-  const int pair = blockIdx.x;
-  const int m = blockIdx.y * kFetchWarps + (threadIdx.x >> 5);
+        const int32_t* __restrict__ miss_slot, const int32_t* __restrict__ miss_total, int par, int s,
+        int n, int c, int d, int k, int npairs, int* __restrict__ status) {
   const int lane = threadIdx.x & 31;
-  if (m >= miss_count[pair]) return;
-  const int chunk = miss_chunk[static_cast<size_t>(pair) * k + m];
-  const int slot = miss_slot[static_cast<size_t>(pair) * k + m];
-  if (chunk < 0 || chunk >= n || slot < 0 || slot >= k) {
-    if (lane == 0) flag_error(status, DEV_BAD_SLOT);
-    return;
+  const int w0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  int total = miss_total[par];
+  if (total > npairs * k) {
+    if (w0 == 0 && lane == 0) flag_error(status, DEV_BAD_COUNT);
+    total = npairs * k;
   }
-  const uint4* src = reinterpret_cast<const uint4*>(vcpu + (static_cast<size_t>(pair) * s + static_cast<size_t>(chunk) * c) * d);
-  uint4* dst = reinterpret_cast<uint4*>(slot_V + ((static_cast<size_t>(pair) * k + slot) * c) * d);
   const int nvec = c * d * static_cast<int>(sizeof(T)) / 16;
-  constexpr int U = 4;
-  for (int base = 0; base < nvec; base += 32 * U) {
-    uint4 buf[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int i = base + u * 32 + lane;
-      if (i < nvec) buf[u] = src[i];
+  for (int m = w0; m < total; m += nwarps) {
+    const int pc = miss_chunk[m], ps = miss_slot[m];
+    const int pair = pc / n, chunk = pc - pair * n;
+    const int slot = ps - pair * k;
+    if (pair < 0 || pair >= npairs || chunk < 0 || slot < 0 || slot >= k) {
+      if (lane == 0) flag_error(status, DEV_BAD_SLOT);
+      continue;
     }
+    const uint4* src = reinterpret_cast<const uint4*>(vcpu + (static_cast<size_t>(pair) * s + static_cast<size_t>(chunk) * c) * d);
+    uint4* dst = reinterpret_cast<uint4*>(slot_V + ((static_cast<size_t>(pair) * k + slot) * c) * d);
+    constexpr int U = 4;
+    for (int base = 0; base < nvec; base += 32 * U) {
+      uint4 buf[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int i = base + u * 32 + lane;
-      if (i < nvec) dst[i] = buf[u];
+      for (int u = 0; u < U; ++u) {
+        const int i = base + u * 32 + lane;
+        if (i < nvec) buf[u] = src[i];
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = base + u * 32 + lane;
+        if (i < nvec) dst[i] = buf[u];
+      }
     }
   }
 }
@@ -340,7 +357,8 @@ static cudaError_t select_t(Ctx& c, const void* k_new, const void* v_new, int lo
   kern<<<c.p.b * c.p.h_kv, kSelectThreads, smem, st>>>(
       c.logits, c.score_part, c.out_mask, c.n, c.ntile, c.p.k, c.p.group_reduce,
       c.cache_on ? 1 : 0, c.sel, c.sel_slot, c.slot_chunk, c.miss_chunk, c.miss_slot,
-      c.miss_count, c.hits, c.counters, static_cast<const T*>(k_new), static_cast<const T*>(v_new),
+      c.miss_count, static_cast<int>(c.t & 1), c.hits, c.counters, static_cast<const T*>(k_new),
+      static_cast<const T*>(v_new),
       static_cast<T*>(c.K_loc), static_cast<T*>(c.V_loc), loc_row, c.loc_cap, c.status);
   return cudaGetLastError();
 }
@@ -371,15 +389,16 @@ cudaError_t launch_select(Ctx& c, const void* k_new, const void* v_new, int loc_
 
 cudaError_t launch_fetch(Ctx& c, cudaStream_t st) {
   kbegin(c, K_FETCH, st);
-  dim3 grid(c.p.b * c.p.h_kv, (c.p.k + kFetchWarps - 1) / kFetchWarps);
+  const int par = static_cast<int>(c.t & 1);
+  const int npairs = c.p.b * c.p.h_kv;
   if (c.p.dtype == SKV_DTYPE_BF16)
-    k_fetch<bf16><<<grid, kFetchWarps * 32, 0, st>>>(
+    k_fetch<bf16><<<c.nsm, kFetchWarps * 32, 0, st>>>(
         static_cast<const bf16*>(c.v_cpu_dev), static_cast<bf16*>(c.slot_V), c.miss_chunk,
-        c.miss_slot, c.miss_count, c.p.s, c.n, c.p.c, c.p.d, c.p.k, c.status);
+        c.miss_slot, c.miss_count, par, c.p.s, c.n, c.p.c, c.p.d, c.p.k, npairs, c.status);
   else
-    k_fetch<float><<<grid, kFetchWarps * 32, 0, st>>>(
+    k_fetch<float><<<c.nsm, kFetchWarps * 32, 0, st>>>(
         static_cast<const float*>(c.v_cpu_dev), static_cast<float*>(c.slot_V), c.miss_chunk,
-        c.miss_slot, c.miss_count, c.p.s, c.n, c.p.c, c.p.d, c.p.k, c.status);
+        c.miss_slot, c.miss_count, par, c.p.s, c.n, c.p.c, c.p.d, c.p.k, npairs, c.status);
   kend(c, K_FETCH, st);
   return cudaGetLastError();
 }

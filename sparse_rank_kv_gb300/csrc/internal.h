@@ -58,6 +58,8 @@ struct Ctx {
   float *min_cos = nullptr, *logits = nullptr, *attn_part = nullptr, *basis = nullptr;
   float2 *score_part = nullptr, *rope_tab = nullptr;
   int32_t *out_ids = nullptr, *sel = nullptr, *sel_slot = nullptr, *slot_chunk = nullptr;
+  // step's compact miss list (pair*n + chunk, pair*k + slot) and its length
+  // per step parity in miss_count[0..1]
   int32_t *miss_chunk = nullptr, *miss_slot = nullptr, *miss_count = nullptr, *hits = nullptr;
   int32_t *attn_count = nullptr;
   uint32_t* out_mask = nullptr;

@@ -91,164 +91,272 @@ k_rebuild_simt(const T* __restrict__ A, const T* __restrict__ Bt, const int32_t*
 
 
 // ------------------------------------------------------------ tcgen05 path
-// One CTA per (batch, KV head, 128-row tile of the k*c selected rows).
-//   warp 0   : TMA loads -- the tile's selected chunks of A (one c x 32 box
-//              per chunk and 32-column K block) and the head's B^T, all into
-//              K-major 64-byte-swizzled shared memory: [K block][row][64 B]
-//   thread 0 : ceil(r/32) x 2 tcgen05.mma (M=128, N=d, K=16) into a TMEM
-//              accumulator of d fp32 columns x 128 lanes
-//   4 warps  : TMEM -> registers (lane = row), RoPE at the row's position,
-//              bf16 pack into a swizzled staging tile, coalesced stores.
+// Persistent kernel, one CTA per SM.  The (batch, KV head, 128-row tile)
+// work items of the k*c selected rows are split into contiguous ranges, one
+// per CTA, so that consecutive tiles of a CTA mostly share the head's B.
+//   warp 0     : TMA producer -- for each tile the selected chunks of A (one
+//                c x 32 box per chunk and 32-column K block) into an S-stage
+//                ring, and the head's B^T into an NB-slot ring when the head
+//                changes; K-major, 64-byte swizzle: [K block][row][64 B]
+//   warp 1     : TMEM allocation; lane 0 issues ceil(r/32) x 2 tcgen05.mma
+//                (M=128, N=d, K=16) per tile into one of two TMEM
+//                accumulators (d fp32 columns each)
+//   warps 2..9 : epilogue, two groups of four warps; warp w reads TMEM lane
+//                quarter w % 4 (row = quarter*32 + lane), group g the RoPE
+//                column pairs [g*d/4, (g+1)*d/4) and their partners at +d/2;
+//                RoPE at the row's position, bf16 pack into a swizzled
+//                staging tile, then coalesced stores of the whole tile.
+// Barriers: fullA/emptyA per A stage, fullB/emptyB per B slot, tfull/tempty
+// per accumulator.  Every wait is bounded; a timeout sets the status word and
+// a shared abort flag that every role checks before its next wait.
 constexpr int kTcRows = 128;
+constexpr int kPipeThreads = 320;
+constexpr int kEpiThreads = 256;
 
-// Shared memory: a 1 KB header (barriers, TMEM address, RoPE frequencies),
-// then, 1 KB aligned, the operand tiles A [KB][128][64 B] and B [KB][D][64 B];
-// after the MMAs the bf16 output staging tile (128 x D) reuses that region.
-__host__ __device__ constexpr int tc_tiles_bytes(int KB, int D) {
-  return KB * (kTcRows + D) * 64 > kTcRows * D * 2 ? KB * (kTcRows + D) * 64 : kTcRows * D * 2;
+struct PipeShape {
+  int KB, S, NB, smem;
+};
+__host__ __device__ constexpr int pipe_a_bytes(int KB) { return KB * kTcRows * 64; }
+__host__ __device__ constexpr int pipe_b_bytes(int KB, int D) { return KB * D * 64; }
+__host__ __device__ constexpr int pipe_smem(int KB, int D, int S, int NB) {
+  return 1024 /* alignment slack */ + 1024 /* header */ + S * pipe_a_bytes(KB) +
+         NB * pipe_b_bytes(KB, D) + kTcRows * D * 2 /* staging */;
 }
-__host__ __device__ constexpr int tc_smem_bytes(int KB, int D) {
-  return 1024 /* alignment slack */ + 1024 /* header */ + tc_tiles_bytes(KB, D);
+static PipeShape pipe_shape(int r, int D) {
+  const int KB = (r + 31) / 32;
+  const int cand[4][2] = {{2, 2}, {2, 1}, {1, 2}, {1, 1}};
+  for (auto& sn : cand) {
+    const int sm = pipe_smem(KB, D, sn[0], sn[1]);
+    if (sm <= 227 * 1024) return {KB, sn[0], sn[1], sm};
+  }
+  return {KB, 0, 0, 0};
 }
 
 template <int D>
-__global__ void __launch_bounds__(kTcRows, 2)
-k_rebuild_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapBt,
-             const int32_t* __restrict__ sel, const float2* __restrict__ rope_tab,
-             bf16* __restrict__ K_sp, int h_kv, int s, int r, int c, int k, int* __restrict__ status) {
+__global__ void __launch_bounds__(kPipeThreads, 1)
+k_rebuild_pipe(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapBt,
+               const int32_t* __restrict__ sel, const float2* __restrict__ rope_tab,
+               bf16* __restrict__ K_sp, int npairs, int h_kv, int s, int r, int c, int k, int S,
+               int NB, int* __restrict__ status) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int KB = (r + 31) / 32;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);            // [0] loads, [1] MMA
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2);
-  int* s_flag = reinterpret_cast<int*>(bars + 3);
-  float2* ftab = reinterpret_cast<float2*>(bars + 8);            // D/2 <= 64 entries
-  unsigned char* sA = smem + 1024;                   // KB x [128 rows][64 B]
-  unsigned char* sB = sA + KB * kTcRows * 64;        // KB x [D rows][64 B]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);   // <= 12 barriers
+  uint64_t* fullA = bars;                                // [S]
+  uint64_t* emptyA = bars + 2;                           // [S]
+  uint64_t* fullB = bars + 4;                            // [NB]
+  uint64_t* emptyB = bars + 6;                           // [NB]
+  uint64_t* tfull = bars + 8;                            // [2]
+  uint64_t* tempty = bars + 10;                          // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 256);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + 260);
+  float2* ftab = reinterpret_cast<float2*>(smem + 512);  // D/2 <= 64 entries
+  unsigned char* sA = smem + 1024;
+  unsigned char* sB = sA + S * pipe_a_bytes(KB);
+  uint4* stage = reinterpret_cast<uint4*>(sB + NB * pipe_b_bytes(KB, D));
 
-  const int pair = blockIdx.y, bb = pair / h_kv;
   const int rows = k * c;
-  const int row0 = blockIdx.x * kTcRows;
-  const int nrow = min(kTcRows, rows - row0);        // a multiple of c
+  const int tpp = (rows + kTcRows - 1) / kTcRows;        // tiles per (batch, KV head)
+  const int total = npairs * tpp;
+  const int lo = static_cast<int>(static_cast<long long>(blockIdx.x) * total / gridDim.x);
+  const int hi = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * total / gridDim.x);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
     tc::prefetch_tensormap(&mapA);
     tc::prefetch_tensormap(&mapBt);
-    tc::mbar_init(&bars[0], 1);
-    tc::mbar_init(&bars[1], 1);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&fullA[i], 1);
+      tc::mbar_init(&emptyA[i], 1);
+      tc::mbar_init(&fullB[i], 1);
+      tc::mbar_init(&emptyB[i], 1);
+      tc::mbar_init(&tfull[i], 1);
+      tc::mbar_init(&tempty[i], kEpiThreads / 32);
+    }
     tc::fence_mbar_init();
-    *s_flag = 1;
+    *s_abort = 0;
   }
-  if (warp == 0) {
-    tc::tmem_alloc(tmem_slot, D);
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, 2 * D);
     tc::tmem_relinquish();
   }
-  for (int i = tid; i < D / 2; i += kTcRows) ftab[i] = rope_tab[i];
+  for (int i = tid; i < D / 2; i += kPipeThreads) ftab[i] = rope_tab[i];
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
+  auto abort_now = [&]() {
+    *s_abort = 1;
+    flag_error(status, DEV_TIMEOUT);
+  };
 
-  // ---- TMA producer (warp 0)
   if (warp == 0) {
-    const int nch = nrow / c;
-    if (lane == 0) tc::mbar_expect_tx(&bars[0], static_cast<uint32_t>(KB * (nrow + D) * 64));
-    __syncwarp();
-    const int nA = nch * KB;
-    const int32_t* srow = sel + static_cast<size_t>(pair) * k + row0 / c;
-    for (int i = lane; i < nA + KB; i += 32) {
-      if (i < nA) {
-        const int ch = i / KB, kb = i - ch * KB;
-        const int chunk = srow[ch];
-        tc::tma_load_2d(sA + kb * (kTcRows * 64) + ch * c * 64, &mapA, &bars[0], kb * 32,
-                        bb * s + chunk * c);
-      } else {
-        const int kb = i - nA;
-        tc::tma_load_2d(sB + kb * (D * 64), &mapBt, &bars[0], kb * 32, pair * D);
-      }
-    }
-  }
-  // ---- MMA issue (thread 0)
-  if (tid == 0) {
-    if (tc::mbar_wait(&bars[0], 0, kWaitLimit)) {
-      tc::fence_after();
-      constexpr uint32_t idesc = tc::idesc_bf16_f32(kTcRows, D);
-      const uint32_t a0 = tc::smem_u32(sA), b0 = tc::smem_u32(sB);
-      for (int kb = 0; kb < KB; ++kb) {
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-          const uint64_t ad = tc::desc_k_sw64(a0 + kb * (kTcRows * 64) + ks * 32, 512);
-          const uint64_t bd = tc::desc_k_sw64(b0 + kb * (D * 64) + ks * 32, 512);
-          tc::mma_bf16(tmem, ad, bd, idesc, (kb | ks) != 0);
+    // ---------------------------------------------------------- producer
+    int prev = -1, nb = -1, lastA[2] = {-1, -1}, lastB[2] = {-1, -1};
+    for (int i = 0; i < hi - lo; ++i) {
+      const int tile = lo + i, pair = tile / tpp, ti = tile - pair * tpp;
+      const int bb = pair / h_kv;
+      if (pair != prev) {
+        ++nb;
+        const int bs = nb % NB, use = nb / NB;
+        bool ok = true;
+        if (lane == 0) ok = *s_abort == 0 && tc::mbar_wait(&emptyB[bs], (use & 1) ^ 1, kWaitLimit);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          if (lane == 0 && *s_abort == 0) abort_now();
+          break;
         }
+        if (lane == 0) tc::mbar_expect_tx(&fullB[bs], static_cast<uint32_t>(pipe_b_bytes(KB, D)));
+        __syncwarp();
+        for (int kb = lane; kb < KB; kb += 32)
+          tc::tma_load_2d(sB + bs * pipe_b_bytes(KB, D) + kb * (D * 64), &mapBt, &fullB[bs], kb * 32,
+                          pair * D);
+        lastB[bs] = use;
+        prev = pair;
       }
-      tc::mma_commit(&bars[1]);
-    } else {
-      *s_flag = 0;
-      flag_error(status, DEV_TIMEOUT);
-      tc::mbar_wait(&bars[0], 0, kWaitLimit);   // let copies in flight land
+      const int st = i % S, use = i / S;
+      const int row0 = ti * kTcRows, nrow = min(kTcRows, rows - row0), nch = nrow / c;
+      bool ok = true;
+      if (lane == 0) ok = *s_abort == 0 && tc::mbar_wait(&emptyA[st], (use & 1) ^ 1, kWaitLimit);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0 && *s_abort == 0) abort_now();
+        break;
+      }
+      if (lane == 0) tc::mbar_expect_tx(&fullA[st], static_cast<uint32_t>(KB * nrow * 64));
+      __syncwarp();
+      const int32_t* srow = sel + static_cast<size_t>(pair) * k + row0 / c;
+      unsigned char* dstA = sA + st * pipe_a_bytes(KB);
+      for (int j = lane; j < nch * KB; j += 32) {
+        const int ch = j / KB, kb = j - ch * KB;
+        tc::tma_load_2d(dstA + kb * (kTcRows * 64) + ch * c * 64, &mapA, &fullA[st], kb * 32,
+                        bb * s + srow[ch] * c);
+      }
+      lastA[st] = use;
     }
-  }
-  __syncthreads();
-  bool ok = *s_flag != 0;
-  if (ok) ok = tc::mbar_wait(&bars[1], 0, kWaitLimit);
-  ok = __syncthreads_and(ok);
-  if (ok) {
-    tc::fence_after();
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    // ---- epilogue: lane = row of the tile
-    const int row = warp * 32 + lane;
-    const int R = row0 + row;
-    int pos = 0;
-    if (row < nrow) pos = sel[static_cast<size_t>(pair) * k + R / c] * c + (R % c);
-    uint4* stage = reinterpret_cast<uint4*>(sA);      // [128][D/8] x 16 B, chunk-swizzled;
-                                                       // tc_tiles_bytes() >= 128 * D * 2
-    constexpr int Q = D / 8;                           // 16-byte chunks per row
-    const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-#pragma unroll 1
-    for (int half = 0; half < D / 64; ++half) {
-      float lo[32], hi[32];
-      tc::tmem_ld32(trow + half * 32, lo);
-      tc::tmem_ld32(trow + D / 2 + half * 32, hi);
-      uint32_t plo[16], phi[16];
+    // every copy issued has landed before the CTA may exit
+    if (lane == 0) {
+      for (int j = 0; j < 2; ++j) {
+        if (lastA[j] >= 0) tc::mbar_wait(&fullA[j], lastA[j] & 1, kWaitLimit);
+        if (lastB[j] >= 0) tc::mbar_wait(&fullB[j], lastB[j] & 1, kWaitLimit);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(kTcRows, D);
+      int prev = -1, nb = -1, bs = 0;
+      int issued = 0;
+      for (int i = 0; i < hi - lo; ++i) {
+        const int tile = lo + i, pair = tile / tpp;
+        if (pair != prev) {
+          ++nb;
+          bs = nb % NB;
+          if (*s_abort || !tc::mbar_wait(&fullB[bs], (nb / NB) & 1, kWaitLimit)) {
+            if (!*s_abort) abort_now();
+            break;
+          }
+          prev = pair;
+        }
+        const int st = i % S, acc = i & 1;
+        if (*s_abort || !tc::mbar_wait(&fullA[st], (i / S) & 1, kWaitLimit) ||
+            !tc::mbar_wait(&tempty[acc], ((i >> 1) & 1) ^ 1, kWaitLimit)) {
+          if (!*s_abort) abort_now();
+          break;
+        }
+        tc::fence_after();
+        const uint32_t a0 = tc::smem_u32(sA + st * pipe_a_bytes(KB));
+        const uint32_t b0 = tc::smem_u32(sB + bs * pipe_b_bytes(KB, D));
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * D);
+        for (int kb = 0; kb < KB; ++kb) {
 #pragma unroll
-      for (int i = 0; i < 32; i += 2) {
+          for (int ks = 0; ks < 2; ++ks) {
+            const uint64_t ad = tc::desc_k_sw64(a0 + kb * (kTcRows * 64) + ks * 32, 512);
+            const uint64_t bd = tc::desc_k_sw64(b0 + kb * (D * 64) + ks * 32, 512);
+            tc::mma_bf16(d_tmem, ad, bd, idesc, (kb | ks) != 0);
+          }
+        }
+        tc::mma_commit(&emptyA[st]);
+        tc::mma_commit(&tfull[acc]);
+        const bool last_of_pair = i == hi - lo - 1 || (tile + 1) / tpp != pair;
+        if (last_of_pair) tc::mma_commit(&emptyB[bs]);
+        ++issued;
+      }
+      // the MMAs issued have completed before TMEM is released
+      if (issued > 0) tc::mbar_wait(&tfull[(issued - 1) & 1], ((issued - 1) >> 1) & 1, kWaitLimit);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int ew = warp - 2, quarter = warp & 3, grp = ew >> 2;
+    const int row = quarter * 32 + lane;
+    constexpr int Q = D / 8;                 // 16-byte chunks per output row
+    constexpr int W = D / 4;                 // RoPE pairs per group
+    for (int i = 0; i < hi - lo; ++i) {
+      const int tile = lo + i, pair = tile / tpp, ti = tile - pair * tpp;
+      const int row0 = ti * kTcRows, nrow = min(kTcRows, rows - row0);
+      const int acc = i & 1;
+      const int R = row0 + row;
+      int pos = 0;
+      if (row < nrow) pos = sel[static_cast<size_t>(pair) * k + R / c] * c + (R % c);
+      bool ok = *s_abort == 0 && tc::mbar_wait(&tfull[acc], (i >> 1) & 1, kWaitLimit);
+      ok = tc::named_sync_and(1, kEpiThreads, ok);
+      if (!ok) {
+        if (tid == 64 && !*s_abort) abort_now();
+        break;
+      }
+      tc::fence_after();
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             static_cast<uint32_t>(acc * D + grp * W);
+      float lo_v[W], hi_v[W];
+      if constexpr (W == 32) {
+        tc::tmem_ld32(taddr, lo_v);
+        tc::tmem_ld32(taddr + D / 2, hi_v);
+      } else {
+        tc::tmem_ld16(taddr, lo_v);
+        tc::tmem_ld16(taddr + D / 2, hi_v);
+      }
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&tempty[acc]);
+      uint32_t plo[W / 2], phi[W / 2];
+#pragma unroll
+      for (int j = 0; j < W; j += 2) {
         float y1[2], y2[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           float sn, cs;
-          rope_sincos_fast(pos, ftab[half * 32 + i + e], &sn, &cs);
-          y1[e] = lo[i + e] * cs - hi[i + e] * sn;
-          y2[e] = hi[i + e] * cs + lo[i + e] * sn;
+          rope_sincos_fast(pos, ftab[grp * W + j + e], &sn, &cs);
+          y1[e] = lo_v[j + e] * cs - hi_v[j + e] * sn;
+          y2[e] = hi_v[j + e] * cs + lo_v[j + e] * sn;
         }
         const __nv_bfloat162 a = __floats2bfloat162_rn(y1[0], y1[1]);
         const __nv_bfloat162 b2 = __floats2bfloat162_rn(y2[0], y2[1]);
-        plo[i / 2] = *reinterpret_cast<const uint32_t*>(&a);
-        phi[i / 2] = *reinterpret_cast<const uint32_t*>(&b2);
+        plo[j / 2] = *reinterpret_cast<const uint32_t*>(&a);
+        phi[j / 2] = *reinterpret_cast<const uint32_t*>(&b2);
       }
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int qlo = half * 4 + q4, qhi = Q / 2 + half * 4 + q4;
+      for (int q4 = 0; q4 < W / 8; ++q4) {
+        const int qlo = grp * (W / 8) + q4, qhi = Q / 2 + qlo;
         stage[row * Q + (qlo ^ (row & (Q - 1)))] =
             make_uint4(plo[4 * q4], plo[4 * q4 + 1], plo[4 * q4 + 2], plo[4 * q4 + 3]);
         stage[row * Q + (qhi ^ (row & (Q - 1)))] =
             make_uint4(phi[4 * q4], phi[4 * q4 + 1], phi[4 * q4 + 2], phi[4 * q4 + 3]);
       }
+      tc::named_sync(1, kEpiThreads);
+      uint4* dst = reinterpret_cast<uint4*>(K_sp + (static_cast<size_t>(pair) * rows + row0) * D);
+      for (int idx = tid - 64; idx < nrow * Q; idx += kEpiThreads) {
+        const int rr = idx / Q, q = idx - rr * Q;
+        dst[idx] = stage[rr * Q + (q ^ (rr & (Q - 1)))];
+      }
+      tc::named_sync(1, kEpiThreads);
     }
-    tc::fence_before();
-    __syncthreads();
-    uint4* dst = reinterpret_cast<uint4*>(K_sp + (static_cast<size_t>(pair) * rows + row0) * D);
-    for (int idx = tid; idx < nrow * Q; idx += kTcRows) {
-      const int rr = idx / Q, q = idx - rr * Q;
-      dst[idx] = stage[rr * Q + (q ^ (rr & (Q - 1)))];
-    }
-  } else {
-    tc::fence_before();
-    __syncthreads();
   }
-  if (warp == 0) tc::tmem_dealloc(tmem, D);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  if (warp == 1) tc::tmem_dealloc(tmem, 2 * D);
 }
 
 bool tc_rebuild_supported(const shadowkv_params& p) {
@@ -296,14 +404,17 @@ cudaError_t make_rebuild_maps(Ctx& c) {
 
 template <int D>
 static cudaError_t rebuild_tc(Ctx& c, cudaStream_t st) {
-  const int KB = (c.p.r + 31) / 32;
-  const int smem = tc_smem_bytes(KB, D);
-  auto kern = k_rebuild_tc<D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const PipeShape ps = pipe_shape(c.p.r, D);
+  if (ps.S == 0) return cudaErrorNotSupported;
+  auto kern = k_rebuild_pipe<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ps.smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((c.p.k * c.p.c + kTcRows - 1) / kTcRows, c.p.b * c.p.h_kv);
-  kern<<<grid, kTcRows, smem, st>>>(c.mapA, c.mapBt, c.sel, c.rope_tab, static_cast<bf16*>(c.K_sparse),
-                                     c.p.h_kv, c.p.s, c.p.r, c.p.c, c.p.k, c.status);
+  const int tiles = (c.p.k * c.p.c + kTcRows - 1) / kTcRows * c.p.h_kv * c.p.b;
+  const int grid = std::min(c.nsm, tiles);
+  kern<<<grid, kPipeThreads, ps.smem, st>>>(c.mapA, c.mapBt, c.sel, c.rope_tab,
+                                            static_cast<bf16*>(c.K_sparse), c.p.b * c.p.h_kv,
+                                            c.p.h_kv, c.p.s,
+                                            c.p.r, c.p.c, c.p.k, ps.S, ps.NB, c.status);
   return cudaGetLastError();
 }
 
