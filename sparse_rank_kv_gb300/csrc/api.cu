@@ -371,6 +371,7 @@ skv_status shadowkv_prefill(const shadowkv_params* p, const void* k_pre, const v
     e = cudaMemcpyAsync(c.v_cpu, v, c.v_bytes, cudaMemcpyDeviceToHost, st);
   }
   if (e == cudaSuccess) e = skv::prefill_device(c, k_pre, v_src, st);
+  if (e == cudaSuccess) e = skv::launch_tile_a(c, 1, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) { s = cuda_fail(e, "prefill"); destroy(h); return s; }
   s = read_status(c);
@@ -398,6 +399,7 @@ skv_status shadowkv_load_state(const shadowkv_params* p, const shadowkv_state_in
   const size_t E = c.E;
   const size_t pairs = static_cast<size_t>(p->b) * p->h_kv;
   cudaError_t e = cudaMemcpyAsync(c.A, in->A, z.A, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess) e = skv::launch_tile_a(c, 1, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(c.L, in->L, z.L, cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess && p->o > 0) e = cudaMemcpyAsync(c.out_ids, in->outlier_ids, z.out_ids, cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess && p->o > 0) e = cudaMemcpyAsync(c.K_out, in->K_out, z.K_out, cudaMemcpyDeviceToDevice, st);
@@ -574,6 +576,24 @@ skv_status shadowkv_field_bytes(const shadowkv_ctx* h, int field, size_t* bytes)
   return SKV_OK;
 }
 
+// Host copy of the tiled A back to row-major: per 8-token group of the
+// chunked region, core matrix q row u (16 bytes) -> row u, piece q.
+static void untile_a_host(const skv::Ctx& c, unsigned char* A) {
+  const int r = c.p.r, QR = r / 8;
+  const size_t gbytes = static_cast<size_t>(8) * r * c.E;
+  const int gpb = c.n * c.p.c / 8;
+  std::vector<unsigned char> tmp(gbytes);
+  for (int bb = 0; bb < c.p.b; ++bb) {
+    unsigned char* base = A + static_cast<size_t>(bb) * c.p.s * r * c.E;
+    for (int g = 0; g < gpb; ++g) {
+      unsigned char* grp = base + g * gbytes;
+      std::memcpy(tmp.data(), grp, gbytes);
+      for (int q = 0; q < QR; ++q)
+        for (int u = 0; u < 8; ++u) std::memcpy(grp + (u * QR + q) * 16, tmp.data() + (q * 8 + u) * 16, 16);
+    }
+  }
+}
+
 skv_status shadowkv_export(shadowkv_ctx* h, int field, void* dst, size_t bytes) {
   if (!h || !dst) return fail(SKV_ERR_INVALID_ARG, "NULL argument");
   if (field < 0 || field >= SKV_FIELD_COUNT) return fail(SKV_ERR_INVALID_ARG, "unknown field %d", field);
@@ -587,6 +607,7 @@ skv_status shadowkv_export(shadowkv_ctx* h, int field, void* dst, size_t bytes) 
   CK(cudaDeviceSynchronize());
   if (on_host) std::memcpy(dst, src, bytes);
   else CK(cudaMemcpy(dst, src, bytes, cudaMemcpyDeviceToHost));
+  if (field == SKV_FIELD_A && c.a_tiled) untile_a_host(c, static_cast<unsigned char*>(dst));
   return SKV_OK;
 }
 

@@ -13,7 +13,7 @@ namespace skv {
 
 constexpr int kScoreTile = 128;      // landmarks per score tile (one per thread)
 constexpr int kSelectThreads = 1024;
-constexpr int kFetchWarps = 8;
+constexpr int kFetchWarps = 32;
 
 // ------------------------------------------------------------------ score
 // One thread per landmark row; q for the KV head's G query heads sits in
@@ -237,10 +237,11 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part,
 
 // ------------------------------------------------------------------ fetch
 // The step's misses form one compact list (entries pair * n + chunk and
-// pair * k + slot, count miss_total[par]).  A small fixed grid (one block per
-// SM) walks it, a warp per chunk: c*d elements read from pinned host memory
-// through its mapped device address into the chunk's cache slot.  Keeping
-// the grid small leaves the SMs to the key rebuild running alongside.
+// pair * k + slot, count miss_total[par]).  A small fixed grid (kFetchSMs
+// blocks of 32 warps, enough loads in flight to fill the host link) walks it,
+// a warp per chunk: c*d elements read from pinned host memory through its
+// mapped device address into the chunk's cache slot.  The key rebuild,
+// running alongside, leaves those SMs free.
 template <typename T>
 __global__ void __launch_bounds__(kFetchWarps * 32)
 k_fetch(const T* __restrict__ vcpu, T* __restrict__ slot_V, const int32_t* __restrict__ miss_chunk,
@@ -392,11 +393,11 @@ cudaError_t launch_fetch(Ctx& c, cudaStream_t st) {
   const int par = static_cast<int>(c.t & 1);
   const int npairs = c.p.b * c.p.h_kv;
   if (c.p.dtype == SKV_DTYPE_BF16)
-    k_fetch<bf16><<<c.nsm, kFetchWarps * 32, 0, st>>>(
+    k_fetch<bf16><<<std::min(c.nsm, kFetchSMs), kFetchWarps * 32, 0, st>>>(
         static_cast<const bf16*>(c.v_cpu_dev), static_cast<bf16*>(c.slot_V), c.miss_chunk,
         c.miss_slot, c.miss_count, par, c.p.s, c.n, c.p.c, c.p.d, c.p.k, npairs, c.status);
   else
-    k_fetch<float><<<c.nsm, kFetchWarps * 32, 0, st>>>(
+    k_fetch<float><<<std::min(c.nsm, kFetchSMs), kFetchWarps * 32, 0, st>>>(
         static_cast<const float*>(c.v_cpu_dev), static_cast<float*>(c.slot_V), c.miss_chunk,
         c.miss_slot, c.miss_count, par, c.p.s, c.n, c.p.c, c.p.d, c.p.k, npairs, c.status);
   kend(c, K_FETCH, st);

@@ -34,6 +34,10 @@ struct Timed {
   cudaEvent_t a, b;
 };
 
+// SMs reserved for the host-memory value fetch, which runs on a side stream
+// next to the key rebuild; the rebuild's grid leaves them free.
+constexpr int kFetchSMs = 16;
+
 struct Ctx {
   shadowkv_params p{};
   int device = 0;
@@ -72,7 +76,8 @@ struct Ctx {
   size_t v_bytes = 0;
 
   // tensor-core rebuild: TMA descriptors of A (b*s x r) and B^T (b*h_kv*d x r)
-  CUtensorMap mapA{}, mapBt{};
+  CUtensorMap mapBt{}, mapK{};
+  bool a_tiled = false;   // chunked region of A stored in 8-token core-matrix groups
   CUtensorMap mapL{};           // landmarks (b*h_kv*n x d) for the tensor-core score kernel
   bool tc_rebuild = false;      // shapes and dtype allow the tcgen05 rebuild
   bool tc_score = false;        // ... and the tcgen05 landmark scores
@@ -118,7 +123,8 @@ cudaError_t launch_build_mask(Ctx& c, cudaStream_t st);
 // rebuild.cu
 cudaError_t launch_rebuild(Ctx& c, cudaStream_t st);
 bool tc_rebuild_supported(const shadowkv_params& p);
-cudaError_t make_rebuild_maps(Ctx& c);   // encodes mapA / mapBt
+cudaError_t make_rebuild_maps(Ctx& c);   // encodes mapBt
+cudaError_t launch_tile_a(Ctx& c, int to_tiled, cudaStream_t st);   // no-op unless a_tiled
 // prefill_kernels.cu
 // Runs Algorithm 1 on the device.  v is a device pointer, or (v_mapped) the
 // mapped device address of pinned host memory.

@@ -4,6 +4,16 @@
 //
 // Output layout: K_sparse[b][h][pos*c + u][:] for the pos-th selected chunk
 // (ascending chunk order) and in-chunk token u.
+//
+// Layout of A in HBM.  Where the tensor-core path applies, the rows of the
+// chunked region [0, n*c) are stored in 8-token groups, each group as r/8
+// core matrices of 8 tokens x 8 ranks (128 contiguous bytes):
+//   element (t, j) at  (t/8) * 8r + (j/8) * 64 + (t%8) * 8 + j%8
+// within its batch's s*r block (tokens >= n*c stay row-major).  A chunk of c
+// tokens (c a multiple of 8) is then one contiguous block of c*r elements in
+// exactly the order the tensor core reads a K-major operand without swizzle,
+// so a single bulk copy moves it to shared memory.  The layout is internal:
+// export returns A row-major.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -13,6 +23,61 @@
 namespace skv {
 
 constexpr int kRbRows = 64;       // output rows per block
+
+// Offset of A element (token t, rank j) within its batch's block in the
+// tiled layout.
+__host__ __device__ __forceinline__ size_t a_tiled_index(int t, int j, int r) {
+  return static_cast<size_t>(t >> 3) * (8 * r) + static_cast<size_t>(j >> 3) * 64 + (t & 7) * 8 + (j & 7);
+}
+
+// In-place conversion of the chunked region of A between row-major and the
+// tiled layout, one warp per 8-token group: the group's 8*r elements
+// (r/8 16-byte pieces per row, <= 256 pieces) are read into registers before
+// any lane writes.  to_tiled = 1: row-major -> tiled, 0: back.
+__global__ void __launch_bounds__(256)
+k_tile_a(uint4* __restrict__ A, int s, int r, int groups_per_batch, long long total_groups, int to_tiled) {
+  const int lane = threadIdx.x & 31;
+  const long long w0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  const int QR = r / 8, npc = 8 * QR;          // pieces per row, per group
+  for (long long g = w0; g < total_groups; g += nw) {
+    const long long bb = g / groups_per_batch, gi = g - bb * groups_per_batch;
+    uint4* base = A + (bb * s * r + gi * 8 * r) / 8;   // 8 bf16 per piece
+    uint4 v[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const int i = lane + 32 * m;
+      if (i < npc) v[m] = base[i];
+    }
+    __syncwarp();
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const int i = lane + 32 * m;   // source piece index
+      if (i < npc) {
+        int dst;
+        if (to_tiled) {            // row-major piece (u, q) -> core matrix q, row u
+          const int u = i / QR, q = i - u * QR;
+          dst = q * 8 + u;
+        } else {                   // tiled piece (q, u) -> row-major (u, q)
+          const int q = i >> 3, u = i & 7;
+          dst = u * QR + q;
+        }
+        base[dst] = v[m];
+      }
+    }
+  }
+}
+
+cudaError_t launch_tile_a(Ctx& c, int to_tiled, cudaStream_t st) {
+  if (!c.a_tiled) return cudaSuccess;
+  const int gpb = c.n * c.p.c / 8;
+  const long long total = static_cast<long long>(gpb) * c.p.b;
+  const int blocks = static_cast<int>(std::min<long long>((total + 7) / 8, 4LL * c.nsm));
+  kbegin(c, K_MISC, st);
+  k_tile_a<<<blocks, 256, 0, st>>>(static_cast<uint4*>(c.A), c.p.s, c.p.r, gpb, total, to_tiled);
+  kend(c, K_MISC, st);
+  return cudaGetLastError();
+}
 constexpr int kRbThreads = 256;
 
 // SIMT reference kernel: fp32 products and sums.  Shared memory holds the
@@ -23,7 +88,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kRbThreads)
 k_rebuild_simt(const T* __restrict__ A, const T* __restrict__ Bt, const int32_t* __restrict__ sel,
                const float2* __restrict__ rope_tab, T* __restrict__ K_sp, int h_kv, int s, int r,
-               int c, int k) {
+               int c, int k, int a_tiled) {
   extern __shared__ __align__(16) float sm[];
   float* As = sm;                 // [kRbRows][r]
   float* Bs = sm + kRbRows * r;   // [r][D]
@@ -40,7 +105,8 @@ k_rebuild_simt(const T* __restrict__ A, const T* __restrict__ Bt, const int32_t*
     if (R < rows) {
       const int chunk = sel[static_cast<size_t>(pair) * k + R / c];
       const int tok = chunk * c + (R % c);
-      v = Ty<T>::to_f(A[(static_cast<size_t>(bb) * s + tok) * r + kk]);
+      const size_t in_batch = a_tiled ? a_tiled_index(tok, kk, r) : static_cast<size_t>(tok) * r + kk;
+      v = Ty<T>::to_f(A[static_cast<size_t>(bb) * s * r + in_batch]);
     }
     As[i] = v;
   }
@@ -94,50 +160,58 @@ k_rebuild_simt(const T* __restrict__ A, const T* __restrict__ Bt, const int32_t*
 // Persistent kernel, one CTA per SM.  The (batch, KV head, 128-row tile)
 // work items of the k*c selected rows are split into contiguous ranges, one
 // per CTA, so that consecutive tiles of a CTA mostly share the head's B.
-//   warp 0     : TMA producer -- for each tile the selected chunks of A (one
-//                c x 32 box per chunk and 32-column K block) into an S-stage
-//                ring, and the head's B^T into an NB-slot ring when the head
-//                changes; K-major, 64-byte swizzle: [K block][row][64 B]
+//   warp 0     : producer -- for each tile the selected chunks of A into an
+//                S-stage ring, one bulk copy per run of consecutive chunk ids
+//                (tiled A: a chunk is c*r contiguous elements already in the
+//                no-swizzle K-major order; gathering with TMA boxes of c rows
+//                x 32 ranks costs one TMA instruction per 512 bytes, and
+//                16-byte cp.async copies run out of requests in flight, both
+//                far below HBM speed); the head's B^T into an NB-slot ring by
+//                TMA (64-byte swizzle, [K block][row][64 B]) when the head
+//                changes
 //   warp 1     : TMEM allocation; lane 0 issues ceil(r/32) x 2 tcgen05.mma
-//                (M=128, N=d, K=16) per tile into one of two TMEM
+//                (M=128, N=d, K=16) per tile into one of four TMEM
 //                accumulators (d fp32 columns each)
-//   warps 2..9 : epilogue, two groups of four warps; warp w reads TMEM lane
+//   warps 2..17: epilogue, four groups of four warps; warp w reads TMEM lane
 //                quarter w % 4 (row = quarter*32 + lane), group g the RoPE
-//                column pairs [g*d/4, (g+1)*d/4) and their partners at +d/2;
-//                RoPE at the row's position, bf16 pack into a swizzled
-//                staging tile, then coalesced stores of the whole tile.
+//                column pairs [g*d/8, (g+1)*d/8) and their partners at +d/2;
+//                RoPE at the row's position, bf16 pack into a staging tile
+//                laid out as TMA's 128-byte swizzle ([d/64][128 rows][128 B]),
+//                then one thread stores it with d/64 TMA tensor stores that
+//                complete while the next tile is computed.
 // Barriers: fullA/emptyA per A stage, fullB/emptyB per B slot, tfull/tempty
 // per accumulator.  Every wait is bounded; a timeout sets the status word and
 // a shared abort flag that every role checks before its next wait.
 constexpr int kTcRows = 128;
-constexpr int kPipeThreads = 320;
-constexpr int kEpiThreads = 256;
+constexpr int kEpiThreads = 512;
+constexpr int kPipeThreads = 64 + kEpiThreads;
+constexpr int kNAcc = 4;          // TMEM accumulators (4 x d <= 512 columns)
 
 struct PipeShape {
-  int KB, S, NB, smem;
+  int S, NB, NS, smem;   // A stages, B slots, output staging buffers
 };
-__host__ __device__ constexpr int pipe_a_bytes(int KB) { return KB * kTcRows * 64; }
+__host__ __device__ constexpr int pipe_a_bytes(int r) { return kTcRows * r * 2; }
 __host__ __device__ constexpr int pipe_b_bytes(int KB, int D) { return KB * D * 64; }
-__host__ __device__ constexpr int pipe_smem(int KB, int D, int S, int NB) {
-  return 1024 /* alignment slack */ + 1024 /* header */ + S * pipe_a_bytes(KB) +
-         NB * pipe_b_bytes(KB, D) + kTcRows * D * 2 /* staging */;
+__host__ __device__ constexpr int pipe_smem(int r, int D, int S, int NB, int NS) {
+  return 1024 /* alignment slack */ + 1024 /* header */ + S * pipe_a_bytes(r) +
+         NB * pipe_b_bytes((r + 31) / 32, D) + NS * kTcRows * D * 2 /* staging */;
 }
 static PipeShape pipe_shape(int r, int D) {
-  const int KB = (r + 31) / 32;
-  const int cand[4][2] = {{2, 2}, {2, 1}, {1, 2}, {1, 1}};
-  for (auto& sn : cand) {
-    const int sm = pipe_smem(KB, D, sn[0], sn[1]);
-    if (sm <= 227 * 1024) return {KB, sn[0], sn[1], sm};
+  const int cand[6][3] = {{2, 2, 2}, {2, 1, 2}, {2, 2, 1}, {2, 1, 1}, {1, 2, 1}, {1, 1, 1}};
+  for (auto& x : cand) {
+    const int sm = pipe_smem(r, D, x[0], x[1], x[2]);
+    if (sm <= 227 * 1024) return {x[0], x[1], x[2], sm};
   }
-  return {KB, 0, 0, 0};
+  return {0, 0, 0, 0};
 }
 
 template <int D>
 __global__ void __launch_bounds__(kPipeThreads, 1)
-k_rebuild_pipe(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapBt,
+k_rebuild_pipe(const bf16* __restrict__ A, const __grid_constant__ CUtensorMap mapBt,
+               const __grid_constant__ CUtensorMap mapK,
                const int32_t* __restrict__ sel, const float2* __restrict__ rope_tab,
-               bf16* __restrict__ K_sp, int npairs, int h_kv, int s, int r, int c, int k, int S,
-               int NB, int* __restrict__ status) {
+               int npairs, int h_kv, int s, int r, int c, int k, int S,
+               int NB, int NS, int* __restrict__ status) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -147,14 +221,15 @@ k_rebuild_pipe(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
   uint64_t* emptyA = bars + 2;                           // [S]
   uint64_t* fullB = bars + 4;                            // [NB]
   uint64_t* emptyB = bars + 6;                           // [NB]
-  uint64_t* tfull = bars + 8;                            // [2]
-  uint64_t* tempty = bars + 10;                          // [2]
+  uint64_t* tfull = bars + 8;                            // [kNAcc]
+  uint64_t* tempty = bars + 12;                          // [kNAcc]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 256);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + 260);
   float2* ftab = reinterpret_cast<float2*>(smem + 512);  // D/2 <= 64 entries
   unsigned char* sA = smem + 1024;
-  unsigned char* sB = sA + S * pipe_a_bytes(KB);
-  uint4* stage = reinterpret_cast<uint4*>(sB + NB * pipe_b_bytes(KB, D));
+  const int a_bytes = pipe_a_bytes(r);
+  unsigned char* sB = sA + S * a_bytes;
+  unsigned char* stage0 = sB + NB * pipe_b_bytes(KB, D);   // NS x [D/64][128][128 B], 1024-aligned
 
   const int rows = k * c;
   const int tpp = (rows + kTcRows - 1) / kTcRows;        // tiles per (batch, KV head)
@@ -162,15 +237,34 @@ k_rebuild_pipe(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
   const int lo = static_cast<int>(static_cast<long long>(blockIdx.x) * total / gridDim.x);
   const int hi = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * total / gridDim.x);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row = (warp & 3) * 32 + lane;   // epilogue: TMEM lane = tile row
+
+  // producer lane l: chunk id of the tile's l-th chunk (<= 128 / 8 chunks)
+  auto chunk_ids = [&](int tile) {
+    const int pr = tile / tpp, r0 = (tile - pr * tpp) * kTcRows;
+    const int nc = min(kTcRows, rows - r0) / c;
+    return lane < nc ? sel[static_cast<size_t>(pr) * k + r0 / c + lane] : 0;
+  };
+  // epilogue thread: position of its row
+  auto row_pos = [&](int tile) {
+    const int pr = tile / tpp, r0 = (tile - pr * tpp) * kTcRows;
+    const int R = r0 + row;
+    return R < rows ? sel[static_cast<size_t>(pr) * k + R / c] * c + (R % c) : 0;
+  };
+  // both are loaded one tile ahead; the first before the setup
+  int first = 0;
+  if (hi > lo) first = warp == 0 ? chunk_ids(lo) : (warp >= 2 ? row_pos(lo) : 0);
 
   if (tid == 0) {
-    tc::prefetch_tensormap(&mapA);
     tc::prefetch_tensormap(&mapBt);
+    tc::prefetch_tensormap(&mapK);
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&fullA[i], 1);
       tc::mbar_init(&emptyA[i], 1);
       tc::mbar_init(&fullB[i], 1);
       tc::mbar_init(&emptyB[i], 1);
+    }
+    for (int i = 0; i < kNAcc; ++i) {
       tc::mbar_init(&tfull[i], 1);
       tc::mbar_init(&tempty[i], kEpiThreads / 32);
     }
@@ -178,7 +272,7 @@ k_rebuild_pipe(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     *s_abort = 0;
   }
   if (warp == 1) {
-    tc::tmem_alloc(tmem_slot, 2 * D);
+    tc::tmem_alloc(tmem_slot, kNAcc * D);
     tc::tmem_relinquish();
   }
   for (int i = tid; i < D / 2; i += kPipeThreads) ftab[i] = rope_tab[i];
@@ -193,10 +287,14 @@ k_rebuild_pipe(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
-    int prev = -1, nb = -1, lastA[2] = {-1, -1}, lastB[2] = {-1, -1};
+    const uint32_t cbytes = static_cast<uint32_t>(c) * r * 2;   // one chunk of tiled A
+    int prev = -1, nb = -1, lastA0 = -1, lastA1 = -1, lastB0 = -1, lastB1 = -1;
+    int cid_next = first;
     for (int i = 0; i < hi - lo; ++i) {
       const int tile = lo + i, pair = tile / tpp, ti = tile - pair * tpp;
       const int bb = pair / h_kv;
+      const int cid = cid_next;
+      if (i + 1 < hi - lo) cid_next = chunk_ids(tile + 1);
       if (pair != prev) {
         ++nb;
         const int bs = nb % NB, use = nb / NB;
@@ -209,10 +307,11 @@ k_rebuild_pipe(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
         }
         if (lane == 0) tc::mbar_expect_tx(&fullB[bs], static_cast<uint32_t>(pipe_b_bytes(KB, D)));
         __syncwarp();
-        for (int kb = lane; kb < KB; kb += 32)
-          tc::tma_load_2d(sB + bs * pipe_b_bytes(KB, D) + kb * (D * 64), &mapBt, &fullB[bs], kb * 32,
-                          pair * D);
-        lastB[bs] = use;
+        if (lane == 0)
+          for (int kb = 0; kb < KB; ++kb)
+            tc::tma_load_2d(sB + bs * pipe_b_bytes(KB, D) + kb * (D * 64), &mapBt, &fullB[bs],
+                            kb * 32, pair * D);
+        (bs ? lastB1 : lastB0) = use;
         prev = pair;
       }
       const int st = i % S, use = i / S;
@@ -224,23 +323,26 @@ k_rebuild_pipe(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
         if (lane == 0 && *s_abort == 0) abort_now();
         break;
       }
-      if (lane == 0) tc::mbar_expect_tx(&fullA[st], static_cast<uint32_t>(KB * nrow * 64));
-      __syncwarp();
-      const int32_t* srow = sel + static_cast<size_t>(pair) * k + row0 / c;
-      unsigned char* dstA = sA + st * pipe_a_bytes(KB);
-      for (int j = lane; j < nch * KB; j += 32) {
-        const int ch = j / KB, kb = j - ch * KB;
-        tc::tma_load_2d(dstA + kb * (kTcRows * 64) + ch * c * 64, &mapA, &fullA[st], kb * 32,
-                        bb * s + srow[ch] * c);
+      if (lane == 0) tc::mbar_expect_tx(&fullA[st], static_cast<uint32_t>(nch) * cbytes);
+      // lane l copies the run of consecutive chunk ids that starts at the
+      // tile's l-th chunk (chunk ids ascend; consecutive ids are contiguous)
+      const int cprev = __shfl_up_sync(0xffffffffu, cid, 1);
+      const bool cont = lane > 0 && lane < nch && cid == cprev + 1;
+      const unsigned long long cmask = __ballot_sync(0xffffffffu, cont);
+      if (lane < nch && !cont) {
+        const int len = __ffsll(~(cmask >> (lane + 1)));
+        tc::bulk_load(sA + st * a_bytes + lane * cbytes,
+                      A + (static_cast<size_t>(bb) * s + static_cast<size_t>(cid) * c) * r,
+                      static_cast<uint32_t>(len) * cbytes, &fullA[st]);
       }
-      lastA[st] = use;
+      (st ? lastA1 : lastA0) = use;
     }
     // every copy issued has landed before the CTA may exit
     if (lane == 0) {
-      for (int j = 0; j < 2; ++j) {
-        if (lastA[j] >= 0) tc::mbar_wait(&fullA[j], lastA[j] & 1, kWaitLimit);
-        if (lastB[j] >= 0) tc::mbar_wait(&fullB[j], lastB[j] & 1, kWaitLimit);
-      }
+      if (lastA0 >= 0) tc::mbar_wait(&fullA[0], lastA0 & 1, kWaitLimit);
+      if (lastA1 >= 0) tc::mbar_wait(&fullA[1], lastA1 & 1, kWaitLimit);
+      if (lastB0 >= 0) tc::mbar_wait(&fullB[0], lastB0 & 1, kWaitLimit);
+      if (lastB1 >= 0) tc::mbar_wait(&fullB[1], lastB1 & 1, kWaitLimit);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issue
@@ -259,23 +361,22 @@ k_rebuild_pipe(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
           }
           prev = pair;
         }
-        const int st = i % S, acc = i & 1;
+        const int st = i % S, acc = i % kNAcc;
         if (*s_abort || !tc::mbar_wait(&fullA[st], (i / S) & 1, kWaitLimit) ||
-            !tc::mbar_wait(&tempty[acc], ((i >> 1) & 1) ^ 1, kWaitLimit)) {
+            !tc::mbar_wait(&tempty[acc], ((i / kNAcc) & 1) ^ 1, kWaitLimit)) {
           if (!*s_abort) abort_now();
           break;
         }
         tc::fence_after();
-        const uint32_t a0 = tc::smem_u32(sA + st * pipe_a_bytes(KB));
+        const uint32_t a0 = tc::smem_u32(sA + st * a_bytes);
         const uint32_t b0 = tc::smem_u32(sB + bs * pipe_b_bytes(KB, D));
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * D);
-        for (int kb = 0; kb < KB; ++kb) {
-#pragma unroll
-          for (int ks = 0; ks < 2; ++ks) {
-            const uint64_t ad = tc::desc_k_sw64(a0 + kb * (kTcRows * 64) + ks * 32, 512);
-            const uint64_t bd = tc::desc_k_sw64(b0 + kb * (D * 64) + ks * 32, 512);
-            tc::mma_bf16(d_tmem, ad, bd, idesc, (kb | ks) != 0);
-          }
+        // K steps of 16: A = two core matrices (128 B apart, 8-row groups
+        // 16r bytes apart); B = half of a 64-byte swizzled K block
+        for (int ks = 0; ks < r / 16; ++ks) {
+          const uint64_t ad = tc::desc_k_none(a0 + ks * 256, 128, static_cast<uint32_t>(r) * 16);
+          const uint64_t bd = tc::desc_k_sw64(b0 + (ks >> 1) * (D * 64) + (ks & 1) * 32, 512);
+          tc::mma_bf16(d_tmem, ad, bd, idesc, ks != 0);
         }
         tc::mma_commit(&emptyA[st]);
         tc::mma_commit(&tfull[acc]);
@@ -284,23 +385,29 @@ k_rebuild_pipe(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
         ++issued;
       }
       // the MMAs issued have completed before TMEM is released
-      if (issued > 0) tc::mbar_wait(&tfull[(issued - 1) & 1], ((issued - 1) >> 1) & 1, kWaitLimit);
+      if (issued > 0)
+        tc::mbar_wait(&tfull[(issued - 1) % kNAcc], ((issued - 1) / kNAcc) & 1, kWaitLimit);
     }
     __syncwarp();
   } else {
     // ---------------------------------------------------------- epilogue
     const int ew = warp - 2, quarter = warp & 3, grp = ew >> 2;
-    const int row = quarter * 32 + lane;
     constexpr int Q = D / 8;                 // 16-byte chunks per output row
-    constexpr int W = D / 4;                 // RoPE pairs per group
+    constexpr int W = D / 8;                 // RoPE pairs per group
+    int pos_next = first;
     for (int i = 0; i < hi - lo; ++i) {
       const int tile = lo + i, pair = tile / tpp, ti = tile - pair * tpp;
       const int row0 = ti * kTcRows, nrow = min(kTcRows, rows - row0);
-      const int acc = i & 1;
-      const int R = row0 + row;
-      int pos = 0;
-      if (row < nrow) pos = sel[static_cast<size_t>(pair) * k + R / c] * c + (R % c);
-      bool ok = *s_abort == 0 && tc::mbar_wait(&tfull[acc], (i >> 1) & 1, kWaitLimit);
+      const int acc = i % kNAcc;
+      const int pos = pos_next;
+      if (i + 1 < hi - lo) pos_next = row_pos(tile + 1);
+      // the stores that last read this tile's staging buffer are done reading
+      if (tid == 64) {
+        if (NS == 1) tc::bulk_wait_read_all();
+        else tc::bulk_wait_read_1();
+      }
+      unsigned char* stage = stage0 + (i % NS) * (kTcRows * D * 2);
+      bool ok = *s_abort == 0 && tc::mbar_wait(&tfull[acc], (i / kNAcc) & 1, kWaitLimit);
       ok = tc::named_sync_and(1, kEpiThreads, ok);
       if (!ok) {
         if (tid == 64 && !*s_abort) abort_now();
@@ -310,12 +417,12 @@ k_rebuild_pipe(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc * D + grp * W);
       float lo_v[W], hi_v[W];
-      if constexpr (W == 32) {
-        tc::tmem_ld32(taddr, lo_v);
-        tc::tmem_ld32(taddr + D / 2, hi_v);
-      } else {
+      if constexpr (W == 16) {
         tc::tmem_ld16(taddr, lo_v);
         tc::tmem_ld16(taddr + D / 2, hi_v);
+      } else {
+        tc::tmem_ld8(taddr, lo_v);
+        tc::tmem_ld8(taddr + D / 2, hi_v);
       }
       tc::fence_before();
       __syncwarp();
@@ -336,32 +443,36 @@ k_rebuild_pipe(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
         plo[j / 2] = *reinterpret_cast<const uint32_t*>(&a);
         phi[j / 2] = *reinterpret_cast<const uint32_t*>(&b2);
       }
+      // 16-byte unit qq of the row: column block qq/8, unit qq%8 XOR row%8
+      auto st16 = [&](int qq, uint4 v) {
+        const int off = (qq >> 3) * (kTcRows * 128) + row * 128 + (((qq & 7) ^ (row & 7)) << 4);
+        *reinterpret_cast<uint4*>(stage + off) = v;
+      };
 #pragma unroll
       for (int q4 = 0; q4 < W / 8; ++q4) {
-        const int qlo = grp * (W / 8) + q4, qhi = Q / 2 + qlo;
-        stage[row * Q + (qlo ^ (row & (Q - 1)))] =
-            make_uint4(plo[4 * q4], plo[4 * q4 + 1], plo[4 * q4 + 2], plo[4 * q4 + 3]);
-        stage[row * Q + (qhi ^ (row & (Q - 1)))] =
-            make_uint4(phi[4 * q4], phi[4 * q4 + 1], phi[4 * q4 + 2], phi[4 * q4 + 3]);
+        const int qlo = grp * (W / 8) + q4;
+        st16(qlo, make_uint4(plo[4 * q4], plo[4 * q4 + 1], plo[4 * q4 + 2], plo[4 * q4 + 3]));
+        st16(Q / 2 + qlo, make_uint4(phi[4 * q4], phi[4 * q4 + 1], phi[4 * q4 + 2], phi[4 * q4 + 3]));
       }
+      tc::fence_proxy_async_smem();
       tc::named_sync(1, kEpiThreads);
-      uint4* dst = reinterpret_cast<uint4*>(K_sp + (static_cast<size_t>(pair) * rows + row0) * D);
-      for (int idx = tid - 64; idx < nrow * Q; idx += kEpiThreads) {
-        const int rr = idx / Q, q = idx - rr * Q;
-        dst[idx] = stage[rr * Q + (q ^ (rr & (Q - 1)))];
+      if (tid == 64) {
+        for (int cb = 0; cb < D / 64; ++cb)
+          tc::tma_store_3d(&mapK, stage + cb * (kTcRows * 128), cb * 64, row0, pair);
+        tc::bulk_commit();
       }
-      tc::named_sync(1, kEpiThreads);
     }
   }
+  if (tid == 64) tc::bulk_wait_all();
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
-  if (warp == 1) tc::tmem_dealloc(tmem, 2 * D);
+  if (warp == 1) tc::tmem_dealloc(tmem, kNAcc * D);
 }
 
 bool tc_rebuild_supported(const shadowkv_params& p) {
   return p.dtype == SKV_DTYPE_BF16 && (p.d == 64 || p.d == 128) && p.c % 8 == 0 &&
-         kTcRows % p.c == 0 && p.r % 8 == 0 && p.r <= 256;
+         kTcRows % p.c == 0 && p.r % 16 == 0 && p.r <= 256 && pipe_shape(p.r, p.d).S > 0;
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -392,29 +503,47 @@ static cudaError_t encode_rows(CUtensorMap* map, void* base, uint64_t nrows, int
   return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// 3D bf16 map over K_sparse [pairs][k*c][d]: box 64 columns x 128 rows x 1
+// with the 128-byte swizzle (rows past k*c of a head are clipped on store).
+static cudaError_t encode_ksparse(CUtensorMap* map, void* base, int D, int rows, uint64_t pairs) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows), pairs};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(rows) * D * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTcRows), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t make_rebuild_maps(Ctx& c) {
   c.tc_rebuild = false;
+  c.a_tiled = false;
   if (!tc_rebuild_supported(c.p)) return cudaSuccess;
   const uint64_t pairs = static_cast<uint64_t>(c.p.b) * c.p.h_kv;
-  cudaError_t e = encode_rows(&c.mapA, c.A, static_cast<uint64_t>(c.p.b) * c.p.s, c.p.r, c.p.c);
-  if (e == cudaSuccess) e = encode_rows(&c.mapBt, c.Bt, pairs * c.p.d, c.p.r, c.p.d);
-  if (e == cudaSuccess) c.tc_rebuild = true;
+  cudaError_t e = encode_rows(&c.mapBt, c.Bt, pairs * c.p.d, c.p.r, c.p.d);
+  if (e == cudaSuccess) e = encode_ksparse(&c.mapK, c.K_sparse, c.p.d, c.p.k * c.p.c, pairs);
+  if (e == cudaSuccess) c.tc_rebuild = c.a_tiled = true;
   return e;
 }
 
 template <int D>
 static cudaError_t rebuild_tc(Ctx& c, cudaStream_t st) {
   const PipeShape ps = pipe_shape(c.p.r, D);
-  if (ps.S == 0) return cudaErrorNotSupported;
+  if (ps.S == 0 || !c.a_tiled) return cudaErrorNotSupported;
   auto kern = k_rebuild_pipe<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ps.smem);
   if (e != cudaSuccess) return e;
   const int tiles = (c.p.k * c.p.c + kTcRows - 1) / kTcRows * c.p.h_kv * c.p.b;
-  const int grid = std::min(c.nsm, tiles);
-  kern<<<grid, kPipeThreads, ps.smem, st>>>(c.mapA, c.mapBt, c.sel, c.rope_tab,
-                                            static_cast<bf16*>(c.K_sparse), c.p.b * c.p.h_kv,
+  const int sms = c.nsm > 2 * kFetchSMs ? c.nsm - kFetchSMs : c.nsm;   // leave the fetch its SMs
+  const int grid = std::min(sms, tiles);
+  kern<<<grid, kPipeThreads, ps.smem, st>>>(static_cast<const bf16*>(c.A), c.mapBt, c.mapK, c.sel,
+                                            c.rope_tab,
+                                            c.p.b * c.p.h_kv,
                                             c.p.h_kv, c.p.s,
-                                            c.p.r, c.p.c, c.p.k, ps.S, ps.NB, c.status);
+                                            c.p.r, c.p.c, c.p.k, ps.S, ps.NB, ps.NS, c.status);
   return cudaGetLastError();
 }
 
@@ -428,7 +557,7 @@ static cudaError_t rebuild_simt(Ctx& c, cudaStream_t st) {
   dim3 grid((c.p.k * c.p.c + kRbRows - 1) / kRbRows, c.p.b * c.p.h_kv);
   kern<<<grid, kRbThreads, smem, st>>>(static_cast<const T*>(c.A), static_cast<const T*>(c.Bt),
                                         c.sel, c.rope_tab, static_cast<T*>(c.K_sparse), c.p.h_kv,
-                                        c.p.s, c.p.r, c.p.c, c.p.k);
+                                        c.p.s, c.p.r, c.p.c, c.p.k, c.a_tiled ? 1 : 0);
   return cudaGetLastError();
 }
 
