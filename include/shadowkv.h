@@ -177,11 +177,14 @@ enum {
   SKV_OPT_CACHE = 0,        /* 1 (default): reuse the previous step's chunks; 0: fetch all k */
   SKV_OPT_TIMING = 1,       /* 1: time each kernel with CUDA events on its stream */
   SKV_OPT_SPLIT_TOKENS = 2, /* tokens per attention split (multiple of 32 in 32..256 whose K/V
-                               rows fit in shared memory; default 128) */
+                               rows fit in shared memory; default 128).  Setting it selects the
+                               classic split-KV attention kernel; by default bf16 contexts use
+                               the pipelined (TMA-fed, 64-token items) kernel */
   SKV_OPT_CUDA_CORES = 3    /* 1: compute the landmark scores and rebuild the keys with the
                                CUDA-core kernels even where the tensor-core (tcgen05) kernels
                                apply (bf16; for the rebuild also c a multiple of 8 dividing 128
-                               and r a multiple of 8); for cross-checking the two */
+                               and r a multiple of 16), and run the classic split-KV attention
+                               instead of the pipelined one; for cross-checking the paths */
 };
 skv_status shadowkv_set_option(shadowkv_ctx* ctx, int option, long long value);
 

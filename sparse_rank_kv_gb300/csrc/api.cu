@@ -72,7 +72,9 @@ struct Sizes {
 int n_of(const shadowkv_params& p) { return (p.s - p.w) / p.c; }
 int max_splits_of(const shadowkv_params& p) {
   const long long T = static_cast<long long>(p.o + p.k) * p.c + p.w + p.max_new;
-  return static_cast<int>((T + 31) / 32);   // the smallest split is 32 tokens
+  // the smallest classic split is 32 tokens; the pipelined kernel's 64-token
+  // items are aligned to the three segments (at most 3 more)
+  return static_cast<int>((T + 31) / 32) + 3;
 }
 
 Sizes sizes_of(const shadowkv_params& p) {
@@ -246,6 +248,7 @@ skv_status create(const shadowkv_params* p, cudaStream_t st, shadowkv_ctx** out)
 
   e = skv::make_rebuild_maps(c);
   if (e == cudaSuccess) e = skv::make_score_map(c);
+  if (e == cudaSuccess) e = skv::make_attn_maps(c);
   if (e != cudaSuccess) return bail(cuda_fail(e, "encode TMA descriptors"));
 
   e = cudaStreamCreateWithFlags(&c.side, cudaStreamNonBlocking);
@@ -482,6 +485,7 @@ skv_status shadowkv_set_option(shadowkv_ctx* h, int option, long long value) {
       if (skv::attn_smem_bytes(c.E, c.G, c.p.d, static_cast<int>(value), c.max_splits) > 227 * 1024)
         return fail(SKV_ERR_UNSUPPORTED, "split of %lld tokens does not fit in shared memory", value);
       c.split_tokens = static_cast<int>(value);
+      c.split_set = true;
       return SKV_OK;
     }
     case SKV_OPT_CUDA_CORES:

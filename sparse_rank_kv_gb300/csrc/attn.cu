@@ -305,7 +305,9 @@ static cudaError_t attn_d(Ctx& c, const void* q, void* out, int n_loc, cudaStrea
 cudaError_t launch_attn(Ctx& c, const void* q, void* out, int n_loc, cudaStream_t st) {
   kbegin(c, K_ATTN, st);
   cudaError_t e;
-  if (c.p.dtype == SKV_DTYPE_BF16)
+  if (c.attn_pipe && !c.force_simt && !c.split_set)
+    e = launch_attn_pipe(c, q, out, n_loc, st);
+  else if (c.p.dtype == SKV_DTYPE_BF16)
     e = c.p.d == 128 ? attn_d<bf16, 128>(c, q, out, n_loc, st) : attn_d<bf16, 64>(c, q, out, n_loc, st);
   else
     e = c.p.d == 128 ? attn_d<float, 128>(c, q, out, n_loc, st) : attn_d<float, 64>(c, q, out, n_loc, st);

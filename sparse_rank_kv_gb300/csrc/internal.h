@@ -47,6 +47,7 @@ struct Ctx {
   int ntile = 0;      // score tiles per (b, h_kv)
   int loc_cap = 0;    // w + max_new
   int split_tokens = 128;
+  bool split_set = false;       // split size chosen by the caller: classic split-KV kernel
   int max_splits = 0;
   bool cache_on = true, timing_on = false;
   long long t = 0;    // decode steps enqueued
@@ -82,6 +83,8 @@ struct Ctx {
   bool tc_rebuild = false;      // shapes and dtype allow the tcgen05 rebuild
   bool tc_score = false;        // ... and the tcgen05 landmark scores
   bool force_simt = false;      // test hook: use the CUDA-core kernels anyway
+  bool attn_pipe = false;       // bf16 shapes the pipelined attention handles
+  CUtensorMap mapKo{}, mapKs{}, mapKl{};   // K_out, K_sparse, K_loc (64-row boxes)
 
   cudaStream_t side = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
@@ -119,6 +122,9 @@ bool tc_score_supported(const shadowkv_params& p);
 cudaError_t make_score_map(Ctx& c);
 // attn.cu
 cudaError_t launch_attn(Ctx& c, const void* q, void* out, int n_loc, cudaStream_t st);
+bool attn_pipe_supported(const shadowkv_params& p);
+cudaError_t make_attn_maps(Ctx& c);
+cudaError_t launch_attn_pipe(Ctx& c, const void* q, void* out, int n_loc, cudaStream_t st);
 cudaError_t launch_build_mask(Ctx& c, cudaStream_t st);
 // rebuild.cu
 cudaError_t launch_rebuild(Ctx& c, cudaStream_t st);
