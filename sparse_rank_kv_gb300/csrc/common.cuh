@@ -139,6 +139,9 @@ __device__ __forceinline__ uint32_t order_key(float x) {
   const uint32_t u = __float_as_uint(x);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+__device__ __forceinline__ float from_order_key(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
 
 // ------------------------------------------------------------ top-k select
 constexpr int kTopkCand = 4096;   // boundary-bin candidates kept after the first pass

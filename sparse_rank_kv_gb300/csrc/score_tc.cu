@@ -11,14 +11,15 @@
 //               G are zero-filled by TMA) into a 5-stage shared-memory ring,
 //               K-major with the 64-byte swizzle
 //   warp 1    : tcgen05.mma (M=128, N=16, K=16) x (d/16) per tile into one of
-//               four TMEM accumulators; commits free the ring slot and publish
+//               eight TMEM accumulators; commits free the ring slot and publish
 //               the accumulator
-//   warps 2-9 : epilogue, two warpgroups taking alternate tiles (four TMEM
-//               accumulators let the MMAs run ahead) -- one landmark row per
-//               thread (TMEM lane), scale, store the G logits, and per 32-row
-//               warp the max and sum of exp over the non-outlier rows (softmax
-//               partials); the outlier-mask word of the group's next tile is
-//               loaded before waiting on the current one
+//   warps 2-17: epilogue, four warpgroups taking every fourth tile (eight
+//               TMEM accumulators let the MMAs run ahead) -- one landmark row
+//               per thread (TMEM lane), scale, store the G logits, and per
+//               32-row warp the max (one integer warp reduction of
+//               order-preserving keys) and sum of exp over the non-outlier
+//               rows (softmax partials); the outlier-mask word of the group's
+//               next tile is loaded before waiting on the current one
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -29,8 +30,9 @@ namespace skv {
 
 constexpr int kScTile = 128;
 constexpr int kScStages = 5;
-constexpr int kScThreads = 320;
-constexpr int kScAcc = 4;        // TMEM accumulators of 16 columns
+constexpr int kScGroups = 4;     // epilogue warpgroups
+constexpr int kScThreads = 64 + kScGroups * 128;
+constexpr int kScAcc = 8;        // TMEM accumulators of 16 columns
 
 __host__ __device__ constexpr int sc_stage_bytes(int D) { return (D / 32) * (kScTile + 16) * 64; }
 __host__ __device__ constexpr int sc_smem_bytes(int D) {
@@ -132,7 +134,7 @@ k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUt
     }
   } else {
     const int q4 = warp & 3;               // TMEM lane quarter of this warp
-    const int eg = (warp - 2) >> 2;        // epilogue warpgroup: tiles eg, eg + 2, ...
+    const int eg = (warp - 2) >> 2;        // epilogue warpgroup: tiles eg, eg + kScGroups, ...
     const int row = q4 * 32 + lane;
     const int nw = (n + 31) >> 5;
     auto mask_word = [&](int i) -> uint32_t {
@@ -143,8 +145,8 @@ k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUt
       return w < nw ? __ldg(&mask[static_cast<size_t>(pair) * nw + w]) : 0u;
     };
     uint32_t mword = mask_word(eg);
-    for (int i = eg; i < ntl; i += 2) {
-      const uint32_t mnext = mask_word(i + 2);
+    for (int i = eg; i < ntl; i += kScGroups) {
+      const uint32_t mnext = mask_word(i + kScGroups);
       const int a = i % kScAcc;
       const uint32_t tph = (i / kScAcc) & 1;
       const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(&tfull[a], tph, kWaitLimit));
@@ -167,7 +169,7 @@ k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUt
       for (int g = 0; g < G; ++g) {
         const float x = acc[g] * scale;
         if (j < n) P[(static_cast<size_t>(pair) * G + g) * n + j] = x;
-        const float m = warp_max(valid ? x : -INFINITY);
+        const float m = from_order_key(__reduce_max_sync(0xffffffffu, order_key(valid ? x : -INFINITY)));
         const float e = warp_sum(valid ? __expf(x - m) : 0.f);
         if (lane == 0) part[((static_cast<size_t>(pair) * G + g) * ntile + ti) * 4 + q4] = make_float2(m, e);
       }
