@@ -70,6 +70,9 @@ struct Sizes {
 };
 
 int n_of(const shadowkv_params& p) { return (p.s - p.w) / p.c; }
+// Local-window rows per (batch, KV head): w + max_new rounded up to whole
+// 8-token groups (tiled values are stored by group).
+int loc_cap_of(const shadowkv_params& p) { return (p.w + p.max_new + 7) / 8 * 8; }
 int max_splits_of(const shadowkv_params& p) {
   const long long T = static_cast<long long>(p.o + p.k) * p.c + p.w + p.max_new;
   // the smallest classic split is 32 tokens; the pipelined kernel's 64-token
@@ -81,7 +84,7 @@ Sizes sizes_of(const shadowkv_params& p) {
   const size_t E = p.dtype == SKV_DTYPE_BF16 ? 2 : 4;
   const size_t b = p.b, h = p.h_kv, hq = p.h_q, d = p.d, s = p.s, r = p.r, c = p.c, k = p.k,
                o = p.o, n = n_of(p);
-  const size_t cap = static_cast<size_t>(p.w) + p.max_new;
+  const size_t cap = loc_cap_of(p);
   const size_t ntile = (n + 127) / 128, nw = (n + 31) / 32;
   Sizes z{};
   z.A = b * s * r * E;
@@ -184,7 +187,8 @@ skv_status create(const shadowkv_params* p, cudaStream_t st, shadowkv_ctx** out)
   c.n = n_of(*p);
   c.G = p->h_q / p->h_kv;
   c.ntile = (c.n + 127) / 128;
-  c.loc_cap = p->w + p->max_new;
+  c.loc_cap = loc_cap_of(*p);
+  c.v_tiled = skv::attn_tc_supported(*p);
   c.max_splits = max_splits_of(*p);
   c.split_tokens = 128;
   auto bail = [&](skv_status s) { destroy(h); return s; };
@@ -227,6 +231,9 @@ skv_status create(const shadowkv_params* p, cudaStream_t st, shadowkv_ctx** out)
   e = cudaMemsetAsync(c.arena + small0, 0, c.arena_bytes - small0, st);
   if (e != cudaSuccess) return bail(cuda_fail(e, "cudaMemsetAsync"));
   e = skv::launch_fill_i32(c, c.slot_chunk, -1, z.slot_chunk / 4, st);
+  // local window rows not yet written read as zeros (finite under zero weights)
+  if (e == cudaSuccess) e = cudaMemsetAsync(c.K_loc, 0, z.K_loc, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c.V_loc, 0, z.V_loc, st);
   if (e != cudaSuccess) return bail(cuda_fail(e, "fill slot table"));
 
   // RoPE frequency table: inv_freq_i / (2 pi) as an fp32 (hi, lo) pair
@@ -249,6 +256,7 @@ skv_status create(const shadowkv_params* p, cudaStream_t st, shadowkv_ctx** out)
   e = skv::make_rebuild_maps(c);
   if (e == cudaSuccess) e = skv::make_score_map(c);
   if (e == cudaSuccess) e = skv::make_attn_maps(c);
+  if (e == cudaSuccess) e = skv::make_attn_tc_maps(c);
   if (e != cudaSuccess) return bail(cuda_fail(e, "encode TMA descriptors"));
 
   e = cudaStreamCreateWithFlags(&c.side, cudaStreamNonBlocking);
@@ -375,6 +383,7 @@ skv_status shadowkv_prefill(const shadowkv_params* p, const void* k_pre, const v
   }
   if (e == cudaSuccess) e = skv::prefill_device(c, k_pre, v_src, st);
   if (e == cudaSuccess) e = skv::launch_tile_a(c, 1, st);
+  if (e == cudaSuccess) e = skv::launch_tile_v(c, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) { s = cuda_fail(e, "prefill"); destroy(h); return s; }
   s = read_status(c);
@@ -415,6 +424,7 @@ skv_status shadowkv_load_state(const shadowkv_params* p, const shadowkv_state_in
     e = cudaMemcpy2DAsync(c.V_loc, row * c.loc_cap, in->V_loc, row * p->w, row * p->w, pairs,
                           cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess) e = skv::launch_transpose_b(c, in->B, st);
+  if (e == cudaSuccess) e = skv::launch_tile_v(c, st);
   if (e == cudaSuccess) e = skv::launch_build_mask(c, st);
   if (e == cudaSuccess) {
     if (in->v_on_host) parallel_memcpy(c.v_cpu, in->V, c.v_bytes);
@@ -557,8 +567,9 @@ static void* field_ptr(skv::Ctx& c, int field, size_t* bytes, bool* on_host) {
     case SKV_FIELD_OUTLIER_IDS: *bytes = z.out_ids; return c.out_ids;
     case SKV_FIELD_K_OUT: *bytes = z.K_out; return c.K_out;
     case SKV_FIELD_V_OUT: *bytes = z.V_out; return c.V_out;
-    case SKV_FIELD_K_LOC: *bytes = z.K_loc; return c.K_loc;
-    case SKV_FIELD_V_LOC: *bytes = z.V_loc; return c.V_loc;
+    // the local window is exported as w + max_new rows per (batch, KV head)
+    case SKV_FIELD_K_LOC: *bytes = z.K_loc / c.loc_cap * (c.p.w + c.p.max_new); return c.K_loc;
+    case SKV_FIELD_V_LOC: *bytes = z.V_loc / c.loc_cap * (c.p.w + c.p.max_new); return c.V_loc;
     case SKV_FIELD_SEL: *bytes = z.sel; return c.sel;
     case SKV_FIELD_SEL_SLOT: *bytes = z.sel_slot; return c.sel_slot;
     case SKV_FIELD_HITS: *bytes = z.hits; return c.hits;
@@ -598,6 +609,19 @@ static void untile_a_host(const skv::Ctx& c, unsigned char* A) {
   }
 }
 
+// Host copy of tiled values back to row-major, in place: `rows` (a multiple of
+// 8) rows of 128 bf16 in 8-row groups.
+static void untile_v_host(unsigned char* V, size_t rows) {
+  std::vector<uint16_t> tmp(1024);
+  uint16_t* v = reinterpret_cast<uint16_t*>(V);
+  for (size_t g = 0; g < rows / 8; ++g) {
+    uint16_t* grp = v + g * 1024;
+    std::memcpy(tmp.data(), grp, 2048);
+    for (int t = 0; t < 8; ++t)
+      for (int j = 0; j < 128; ++j) grp[t * 128 + j] = tmp[(j >> 3) * 64 + (j & 7) * 8 + t];
+  }
+}
+
 skv_status shadowkv_export(shadowkv_ctx* h, int field, void* dst, size_t bytes) {
   if (!h || !dst) return fail(SKV_ERR_INVALID_ARG, "NULL argument");
   if (field < 0 || field >= SKV_FIELD_COUNT) return fail(SKV_ERR_INVALID_ARG, "unknown field %d", field);
@@ -609,9 +633,22 @@ skv_status shadowkv_export(shadowkv_ctx* h, int field, void* dst, size_t bytes) 
   if (bytes != want) return fail(SKV_ERR_INVALID_ARG, "field %d has %zu bytes, got %zu", field, want, bytes);
   DeviceGuard g(c.device);
   CK(cudaDeviceSynchronize());
+  const size_t pairs = static_cast<size_t>(c.p.b) * c.p.h_kv;
+  if (field == SKV_FIELD_K_LOC || field == SKV_FIELD_V_LOC) {
+    // whole buffer, values untiled, then w + max_new of the loc_cap rows per head
+    const size_t row = static_cast<size_t>(c.p.d) * c.E, keep = static_cast<size_t>(c.p.w) + c.p.max_new;
+    std::vector<unsigned char> full(pairs * c.loc_cap * row);
+    CK(cudaMemcpy(full.data(), src, full.size(), cudaMemcpyDeviceToHost));
+    if (field == SKV_FIELD_V_LOC && c.v_tiled) untile_v_host(full.data(), pairs * c.loc_cap);
+    for (size_t pr = 0; pr < pairs; ++pr)
+      std::memcpy(static_cast<unsigned char*>(dst) + pr * keep * row, full.data() + pr * c.loc_cap * row, keep * row);
+    return SKV_OK;
+  }
   if (on_host) std::memcpy(dst, src, bytes);
   else CK(cudaMemcpy(dst, src, bytes, cudaMemcpyDeviceToHost));
   if (field == SKV_FIELD_A && c.a_tiled) untile_a_host(c, static_cast<unsigned char*>(dst));
+  if (c.v_tiled && (field == SKV_FIELD_V_OUT || field == SKV_FIELD_SLOT_V))
+    untile_v_host(static_cast<unsigned char*>(dst), bytes / (static_cast<size_t>(c.p.d) * c.E));
   return SKV_OK;
 }
 

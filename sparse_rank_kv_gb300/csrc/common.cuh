@@ -90,6 +90,31 @@ __device__ __forceinline__ void rope_sincos_fast(int pos, float2 f, float* sn, f
   __sincosf(turns * 6.283185307179586f, sn, cs);
 }
 
+// ------------------------------------------------------ tiled value rows
+// Values of bf16 contexts with d = 128 are stored in 8-token groups laid out
+// as the tensor core's no-swizzle K-major tiles of V^T: element (token t,
+// dimension j) of a group at (j/8)*64 + (j%8)*8 + t.  transpose8x8 turns the
+// row-major group held by a half-warp -- lane q holds the 16-byte piece q
+// (dimensions 8q..8q+7) of rows 0..7 in in[t] -- into the tiled group: out[r]
+// = the 8 tokens of dimension 8q + r, stored at 16-byte unit 8q + r.
+__device__ __forceinline__ void transpose8x8(const uint4 (&in)[8], uint4 (&out)[8]) {
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    uint32_t e[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const uint32_t w = (r >> 1) == 0 ? in[t].x : (r >> 1) == 1 ? in[t].y : (r >> 1) == 2 ? in[t].z : in[t].w;
+      e[t] = (r & 1) ? (w >> 16) : (w & 0xffffu);
+    }
+    out[r] = make_uint4(e[0] | (e[1] << 16), e[2] | (e[3] << 16), e[4] | (e[5] << 16), e[6] | (e[7] << 16));
+  }
+}
+// Offset of element (row t, dimension j) of a tiled [rows][128] block whose
+// 8-row groups start at multiples of 8 rows.
+__host__ __device__ __forceinline__ size_t vt_off(size_t t, int j) {
+  return (t >> 3) * 1024 + static_cast<size_t>(j >> 3) * 64 + (j & 7) * 8 + (t & 7);
+}
+
 // ------------------------------------------------------------ reductions
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

@@ -79,7 +79,7 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part,
          int32_t* __restrict__ miss_slot, int32_t* __restrict__ miss_total, int par,
          int32_t* __restrict__ hits, unsigned long long* __restrict__ counters,
          const T* __restrict__ k_new, const T* __restrict__ v_new, T* __restrict__ K_loc,
-         T* __restrict__ V_loc, int loc_row, int loc_cap, int* __restrict__ status) {
+         T* __restrict__ V_loc, int loc_row, int loc_cap, int v_tiled, int* __restrict__ status) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int nw = (n + 31) >> 5;
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
@@ -102,7 +102,8 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part,
     for (int i = tid; i < D; i += nthr) {
       const size_t dst = (static_cast<size_t>(pair) * loc_cap + loc_row) * D + i;
       K_loc[dst] = k_new[static_cast<size_t>(pair) * D + i];
-      V_loc[dst] = v_new[static_cast<size_t>(pair) * D + i];
+      const size_t vdst = v_tiled ? static_cast<size_t>(pair) * loc_cap * D + vt_off(loc_row, i) : dst;
+      V_loc[vdst] = v_new[static_cast<size_t>(pair) * D + i];
     }
   }
   // log-sum-exp of each query head over the candidate chunks (4 partials
@@ -283,6 +284,80 @@ k_fetch(const T* __restrict__ vcpu, T* __restrict__ slot_V, const int32_t* __res
   }
 }
 
+// Tiled-value fetch (bf16, d = 128): a half-warp per 8-token group, lane q
+// reading the 16-byte piece q of the group's 8 rows from pinned host memory
+// and writing the group's 16 x 8 tiled units (one 128-byte run per lane).
+__global__ void __launch_bounds__(kFetchWarps * 32)
+k_fetch_tiled(const bf16* __restrict__ vcpu, bf16* __restrict__ slot_V, const int32_t* __restrict__ miss_chunk,
+              const int32_t* __restrict__ miss_slot, const int32_t* __restrict__ miss_total, int par, int s,
+              int n, int c, int k, int npairs, int* __restrict__ status) {
+  const int lane = threadIdx.x & 31, q = lane & 15;
+  const int h0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 4;
+  const int nh = (gridDim.x * blockDim.x) >> 4;
+  int total = miss_total[par];
+  if (total > npairs * k) {
+    if (h0 == 0 && lane == 0) flag_error(status, DEV_BAD_COUNT);
+    total = npairs * k;
+  }
+  const int gpc = c >> 3;   // groups per chunk
+  for (int gi = h0; gi < total * gpc; gi += nh) {
+    const int m = gi / gpc, gs = gi - m * gpc;
+    const int pc = miss_chunk[m], ps = miss_slot[m];
+    const int pair = pc / n, chunk = pc - pair * n;
+    const int slot = ps - pair * k;
+    if (pair < 0 || pair >= npairs || chunk < 0 || slot < 0 || slot >= k) {
+      if (q == 0) flag_error(status, DEV_BAD_SLOT);
+      continue;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(
+        vcpu + (static_cast<size_t>(pair) * s + static_cast<size_t>(chunk) * c + gs * 8) * 128);
+    uint4* dst = reinterpret_cast<uint4*>(slot_V + ((static_cast<size_t>(pair) * k + slot) * c + gs * 8) * 128);
+    uint4 in[8], outv[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) in[t] = src[t * 16 + q];
+    transpose8x8(in, outv);
+#pragma unroll
+    for (int r = 0; r < 8; ++r) dst[q * 8 + r] = outv[r];
+  }
+}
+
+// In-place tiling of the 8-row groups of a row-major [rows][128] bf16 array
+// (rows a multiple of 8), a half-warp per group.
+__global__ void __launch_bounds__(256) k_tile_v(bf16* __restrict__ V, long long groups) {
+  const int lane = threadIdx.x & 31, q = lane & 15;
+  const long long h0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
+  const long long nh = (static_cast<long long>(gridDim.x) * blockDim.x) >> 4;
+  const long long iters = (groups + nh - 1) / nh;
+  for (long long it = 0; it < iters; ++it) {
+    const long long g = h0 + it * nh;
+    const bool on = g < groups;
+    uint4* base = reinterpret_cast<uint4*>(V + (on ? g : 0) * 1024);
+    uint4 in[8], outv[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) in[t] = on ? base[t * 16 + q] : make_uint4(0, 0, 0, 0);
+    transpose8x8(in, outv);
+    __syncwarp();   // every lane of the group has read it before any writes
+    if (on) {
+#pragma unroll
+      for (int r = 0; r < 8; ++r) base[q * 8 + r] = outv[r];
+    }
+  }
+}
+
+cudaError_t launch_tile_v(Ctx& c, cudaStream_t st) {
+  if (!c.v_tiled) return cudaSuccess;
+  const long long pairs = static_cast<long long>(c.p.b) * c.p.h_kv;
+  const long long g_out = pairs * c.p.o * c.p.c / 8, g_loc = pairs * c.loc_cap / 8;
+  kbegin(c, K_MISC, st);
+  if (g_out > 0)
+    k_tile_v<<<static_cast<int>(std::min<long long>((g_out + 15) / 16, 8LL * c.nsm)), 256, 0, st>>>(
+        static_cast<bf16*>(c.V_out), g_out);
+  k_tile_v<<<static_cast<int>(std::min<long long>((g_loc + 15) / 16, 8LL * c.nsm)), 256, 0, st>>>(
+      static_cast<bf16*>(c.V_loc), g_loc);
+  kend(c, K_MISC, st);
+  return cudaGetLastError();
+}
+
 // --------------------------------------------------------- outlier mask
 // Rebuilds the per-(batch, KV head) outlier bitmap from outlier_ids and
 // checks that the ids are ascending, distinct and < n.
@@ -360,7 +435,8 @@ static cudaError_t select_t(Ctx& c, const void* k_new, const void* v_new, int lo
       c.cache_on ? 1 : 0, c.sel, c.sel_slot, c.slot_chunk, c.miss_chunk, c.miss_slot,
       c.miss_count, static_cast<int>(c.t & 1), c.hits, c.counters, static_cast<const T*>(k_new),
       static_cast<const T*>(v_new),
-      static_cast<T*>(c.K_loc), static_cast<T*>(c.V_loc), loc_row, c.loc_cap, c.status);
+      static_cast<T*>(c.K_loc), static_cast<T*>(c.V_loc), loc_row, c.loc_cap, c.v_tiled ? 1 : 0,
+      c.status);
   return cudaGetLastError();
 }
 
@@ -392,7 +468,11 @@ cudaError_t launch_fetch(Ctx& c, cudaStream_t st) {
   kbegin(c, K_FETCH, st);
   const int par = static_cast<int>(c.t & 1);
   const int npairs = c.p.b * c.p.h_kv;
-  if (c.p.dtype == SKV_DTYPE_BF16)
+  if (c.v_tiled)
+    k_fetch_tiled<<<std::min(c.nsm, kFetchSMs), kFetchWarps * 32, 0, st>>>(
+        static_cast<const bf16*>(c.v_cpu_dev), static_cast<bf16*>(c.slot_V), c.miss_chunk,
+        c.miss_slot, c.miss_count, par, c.p.s, c.n, c.p.c, c.p.k, npairs, c.status);
+  else if (c.p.dtype == SKV_DTYPE_BF16)
     k_fetch<bf16><<<std::min(c.nsm, kFetchSMs), kFetchWarps * 32, 0, st>>>(
         static_cast<const bf16*>(c.v_cpu_dev), static_cast<bf16*>(c.slot_V), c.miss_chunk,
         c.miss_slot, c.miss_count, par, c.p.s, c.n, c.p.c, c.p.d, c.p.k, npairs, c.status);

@@ -79,6 +79,8 @@ struct Ctx {
   // tensor-core rebuild: TMA descriptors of A (b*s x r) and B^T (b*h_kv*d x r)
   CUtensorMap mapBt{}, mapK{};
   bool a_tiled = false;   // chunked region of A stored in 8-token core-matrix groups
+  bool v_tiled = false;   // V_out, V_loc, slot_V stored in 8-token tiled groups (tensor-core attention)
+  CUtensorMap mapTs{}, mapTo{}, mapTl{};   // K_sparse, K_out, K_loc for the tensor-core attention
   CUtensorMap mapL{};           // landmarks (b*h_kv*n x d) for the tensor-core score kernel
   bool tc_rebuild = false;      // shapes and dtype allow the tcgen05 rebuild
   bool tc_score = false;        // ... and the tcgen05 landmark scores
@@ -131,6 +133,11 @@ cudaError_t launch_rebuild(Ctx& c, cudaStream_t st);
 bool tc_rebuild_supported(const shadowkv_params& p);
 cudaError_t make_rebuild_maps(Ctx& c);   // encodes mapBt
 cudaError_t launch_tile_a(Ctx& c, int to_tiled, cudaStream_t st);   // no-op unless a_tiled
+cudaError_t launch_tile_v(Ctx& c, cudaStream_t st);                 // no-op unless v_tiled
+bool attn_tc_supported(const shadowkv_params& p);
+cudaError_t make_attn_tc_maps(Ctx& c);
+cudaError_t launch_attn_tc(Ctx& c, const void* q, void* out, int n_loc, cudaStream_t st);
+cudaError_t encode_q_map(const Ctx& c, const void* q, CUtensorMap* map);
 // prefill_kernels.cu
 // Runs Algorithm 1 on the device.  v is a device pointer, or (v_mapped) the
 // mapped device address of pinned host memory.

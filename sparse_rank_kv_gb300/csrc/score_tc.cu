@@ -219,7 +219,7 @@ cudaError_t make_score_map(Ctx& c) {
 // The queries live in the caller's buffer, so their descriptor is encoded for
 // every step: a 3D view {d, G, b*h_kv} read in boxes of 32 x 16 x 1, the rows
 // past G being zero-filled.
-static cudaError_t encode_q(const Ctx& c, const void* q, CUtensorMap* map) {
+cudaError_t encode_q_map(const Ctx& c, const void* q, CUtensorMap* map) {
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
   if (reinterpret_cast<uintptr_t>(q) % 16) return cudaErrorMisalignedAddress;
@@ -263,7 +263,7 @@ static cudaError_t score_tc_d(Ctx& c, const CUtensorMap& mq, cudaStream_t st) {
 cudaError_t launch_score_tc(Ctx& c, const void* q, cudaStream_t st) {
   if (!c.tc_score || c.force_simt) return cudaErrorNotSupported;
   CUtensorMap mq;
-  if (encode_q(c, q, &mq) != cudaSuccess) return cudaErrorNotSupported;
+  if (encode_q_map(c, q, &mq) != cudaSuccess) return cudaErrorNotSupported;
   return c.p.d == 128 ? score_tc_d<128>(c, mq, st) : score_tc_d<64>(c, mq, st);
 }
 
