@@ -291,8 +291,7 @@ static cudaError_t attn_t(Ctx& c, const void* q, void* out, int n_loc, cudaStrea
   const size_t smem = attn_smem_bytes(sizeof(T), G, D, S, c.max_splits);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
   auto kern = k_attn<T, D, G>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
   kern<<<dim3(c.p.b * c.p.h_kv, nsplit), kAt, smem, st>>>(
@@ -368,8 +367,7 @@ cudaError_t noalloc_launch(const shadowkv_params& p, const void* q, const void* 
   const size_t smem = skv::attn_smem_bytes(sizeof(T), G, D, S, nsplit);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
   auto kern = skv::k_attn<T, D, G>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = skv::set_smem_once(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
   // every token is one plain segment: no rebuilt chunks, no local window

@@ -447,7 +447,7 @@ static cudaError_t attn_pipe_t(Ctx& c, const void* q, void* out, int n_loc, cuda
   constexpr int NST = ap_stages(G, D);
   const int smem = ap_smem_bytes(G, D, NST);
   auto kern = k_attn_pipe<D, G, NST>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   const int npairs = c.p.b * c.p.h_kv;
   const int items = npairs * attn_pipe_splits(c, n_loc);

@@ -107,6 +107,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapKo, const __grid_constant__ CUt
   const int hi = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * total / gridDim.x);
   const int nit = hi - lo;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  tc::grid_dep_launch();
 
   if (tid == 0) {
     tc::prefetch_tensormap(&mapKs);
@@ -152,6 +153,8 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapKo, const __grid_constant__ CUt
       flag_error(status, DEV_TIMEOUT);
     }
   };
+  // the rebuild may still be finishing: its keys are read after this
+  tc::grid_dep_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -545,25 +548,28 @@ template <int G>
 static cudaError_t attn_tc_t(Ctx& c, const CUtensorMap& mq, void* out, int n_loc, cudaStream_t st) {
   const int smem = at_smem_bytes();
   auto kern = k_attn_tc<G>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   const int npairs = c.p.b * c.p.h_kv;
   const int items = npairs * attn_tc_splits(c, n_loc);
   const int grid = std::min(std::min(c.nsm, items), npairs * (kAtMaxSlots - 2));
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kAtD));
-  kern<<<grid, kAtThreads, smem, st>>>(
-      c.mapTo, c.mapTs, c.mapTl, mq, static_cast<const bf16*>(c.V_out), static_cast<const bf16*>(c.slot_V),
-      c.sel_slot, static_cast<const bf16*>(c.V_loc), static_cast<bf16*>(out), c.attn_part, c.attn_count,
-      c.p.o * c.p.c, c.p.k * c.p.c, n_loc, c.loc_cap, c.p.c, c.p.k, npairs, c.max_splits, scale_log2,
-      c.status);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kAtThreads), smem, st, c.mapTo, c.mapTs, c.mapTl, mq,
+                    static_cast<const bf16*>(c.V_out), static_cast<const bf16*>(c.slot_V),
+                    static_cast<const int32_t*>(c.sel_slot), static_cast<const bf16*>(c.V_loc),
+                    static_cast<bf16*>(out), c.attn_part, c.attn_count, c.p.o * c.p.c, c.p.k * c.p.c,
+                    n_loc, c.loc_cap, c.p.c, c.p.k, npairs, c.max_splits, scale_log2, c.status);
 }
 
 cudaError_t launch_attn_tc(Ctx& c, const void* q, void* out, int n_loc, cudaStream_t st) {
   if (attn_tc_splits(c, n_loc) > c.max_splits) return cudaErrorInvalidValue;
   CUtensorMap mq;
-  cudaError_t e = encode_q_map(c, q, &mq);
-  if (e != cudaSuccess) return e;
+  if (q == c.q_buf && c.q_map) {
+    mq = c.mapQ;
+  } else {
+    const cudaError_t e = encode_q_map(c, q, &mq);
+    if (e != cudaSuccess) return e;
+  }
   switch (c.G) {
     case 1: return attn_tc_t<1>(c, mq, out, n_loc, st);
     case 2: return attn_tc_t<2>(c, mq, out, n_loc, st);

@@ -8,6 +8,7 @@
 // (the attention kernel is in attn.cu, the key rebuild in rebuild.cu)
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace skv {
 
@@ -96,8 +97,10 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part,
 
   const int pair = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthr = blockDim.x;
+  tc::grid_dep_launch();
 
-  // append the new token's key/value to the local window
+  // append the new token's key/value to the local window (the score kernel,
+  // which may still be finishing, does not touch it)
   if (k_new != nullptr) {
     for (int i = tid; i < D; i += nthr) {
       const size_t dst = (static_cast<size_t>(pair) * loc_cap + loc_row) * D + i;
@@ -106,6 +109,7 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part,
       V_loc[vdst] = v_new[static_cast<size_t>(pair) * D + i];
     }
   }
+  tc::grid_dep_wait();   // the logits and partials of the score kernel
   // log-sum-exp of each query head over the candidate chunks (4 partials
   // of 32 landmarks per 128-landmark score tile)
   for (int g = warp; g < G; g += nthr / 32) {
@@ -427,17 +431,15 @@ static cudaError_t select_t(Ctx& c, const void* k_new, const void* v_new, int lo
                             cudaStream_t st) {
   const size_t smem = select_smem_bytes(c.n, c.p.k, c.G);
   auto kern = k_select<T, D, G>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<c.p.b * c.p.h_kv, kSelectThreads, smem, st>>>(
+  return launch_pdl(kern, dim3(c.p.b * c.p.h_kv), dim3(kSelectThreads), smem, st,
       c.logits, c.score_part, c.out_mask, c.n, c.ntile, c.p.k, c.p.group_reduce,
       c.cache_on ? 1 : 0, c.sel, c.sel_slot, c.slot_chunk, c.miss_chunk, c.miss_slot,
       c.miss_count, static_cast<int>(c.t & 1), c.hits, c.counters, static_cast<const T*>(k_new),
       static_cast<const T*>(v_new),
       static_cast<T*>(c.K_loc), static_cast<T*>(c.V_loc), loc_row, c.loc_cap, c.v_tiled ? 1 : 0,
       c.status);
-  return cudaGetLastError();
 }
 
 template <typename T, int D>

@@ -1,6 +1,7 @@
 // Host-side internals of the ShadowKV library: the context and the kernel
 // launchers each .cu file provides to the C ABI in api.cu.
 #pragma once
+#include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -81,6 +82,11 @@ struct Ctx {
   bool a_tiled = false;   // chunked region of A stored in 8-token core-matrix groups
   bool v_tiled = false;   // V_out, V_loc, slot_V stored in 8-token tiled groups (tensor-core attention)
   CUtensorMap mapTs{}, mapTo{}, mapTl{};   // K_sparse, K_out, K_loc for the tensor-core attention
+  // the step's queries, copied from the caller's buffer so that their
+  // tensor map (mapQ, 16-row boxes) is encoded once
+  void* q_buf = nullptr;
+  CUtensorMap mapQ{};
+  bool q_map = false;
   CUtensorMap mapL{};           // landmarks (b*h_kv*n x d) for the tensor-core score kernel
   bool tc_rebuild = false;      // shapes and dtype allow the tcgen05 rebuild
   bool tc_score = false;        // ... and the tcgen05 landmark scores
@@ -124,6 +130,26 @@ bool tc_score_supported(const shadowkv_params& p);
 cudaError_t make_score_map(Ctx& c);
 // attn.cu
 cudaError_t launch_attn(Ctx& c, const void* q, void* out, int n_loc, cudaStream_t st);
+// Launches kern with programmatic stream serialization: it may begin while
+// the previous kernel of the stream finishes (it calls grid_dep_wait before
+// reading that kernel's results).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per device, kernel and size
+cudaError_t set_smem_once(const void* func, int bytes);
 bool attn_pipe_supported(const shadowkv_params& p);
 cudaError_t make_attn_maps(Ctx& c);
 cudaError_t launch_attn_pipe(Ctx& c, const void* q, void* out, int n_loc, cudaStream_t st);

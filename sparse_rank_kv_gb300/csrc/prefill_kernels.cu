@@ -402,8 +402,7 @@ static cudaError_t prefill_stats(Ctx& c, const T* K, const T* V, cudaStream_t st
   SKV_TRY(cudaGetLastError());
   if (o > 0) {
     const size_t smem = sizeof(uint32_t) * (n + 2 * ((n + 31) / 32)) + sizeof(int) * (o + topk_scratch_ints(1024)) + 16;
-    SKV_TRY(cudaFuncSetAttribute(k_outlier_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem)));
+    SKV_TRY(set_smem_once(reinterpret_cast<const void*>(k_outlier_select), static_cast<int>(smem)));
     kbegin(c, K_OUTLIERS, st);
     k_outlier_select<<<pairs, 1024, smem, st>>>(c.min_cos, c.out_ids, n, o);
     kend(c, K_OUTLIERS, st);

@@ -251,10 +251,7 @@ k_rebuild_pipe(const bf16* __restrict__ A, const __grid_constant__ CUtensorMap m
     const int R = r0 + row;
     return R < rows ? sel[static_cast<size_t>(pr) * k + R / c] * c + (R % c) : 0;
   };
-  // both are loaded one tile ahead; the first before the setup
-  int first = 0;
-  if (hi > lo) first = warp == 0 ? chunk_ids(lo) : (warp >= 2 ? row_pos(lo) : 0);
-
+  tc::grid_dep_launch();
   if (tid == 0) {
     tc::prefetch_tensormap(&mapBt);
     tc::prefetch_tensormap(&mapK);
@@ -284,6 +281,11 @@ k_rebuild_pipe(const bf16* __restrict__ A, const __grid_constant__ CUtensorMap m
     *s_abort = 1;
     flag_error(status, DEV_TIMEOUT);
   };
+  // the selection may still be finishing: its chunk ids are read after this
+  tc::grid_dep_wait();
+  // both are loaded one tile ahead
+  int first = 0;
+  if (hi > lo) first = warp == 0 ? chunk_ids(lo) : (warp >= 2 ? row_pos(lo) : 0);
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
@@ -534,25 +536,22 @@ static cudaError_t rebuild_tc(Ctx& c, cudaStream_t st) {
   const PipeShape ps = pipe_shape(c.p.r, D);
   if (ps.S == 0 || !c.a_tiled) return cudaErrorNotSupported;
   auto kern = k_rebuild_pipe<D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ps.smem);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), ps.smem);
   if (e != cudaSuccess) return e;
   const int tiles = (c.p.k * c.p.c + kTcRows - 1) / kTcRows * c.p.h_kv * c.p.b;
   const int sms = c.nsm > 2 * kFetchSMs ? c.nsm - kFetchSMs : c.nsm;   // leave the fetch its SMs
   const int grid = std::min(sms, tiles);
-  kern<<<grid, kPipeThreads, ps.smem, st>>>(static_cast<const bf16*>(c.A), c.mapBt, c.mapK, c.sel,
-                                            c.rope_tab,
-                                            c.p.b * c.p.h_kv,
-                                            c.p.h_kv, c.p.s,
-                                            c.p.r, c.p.c, c.p.k, ps.S, ps.NB, ps.NS, c.status);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kPipeThreads), ps.smem, st, static_cast<const bf16*>(c.A),
+                    c.mapBt, c.mapK, static_cast<const int32_t*>(c.sel),
+                    static_cast<const float2*>(c.rope_tab), c.p.b * c.p.h_kv, c.p.h_kv, c.p.s, c.p.r,
+                    c.p.c, c.p.k, ps.S, ps.NB, ps.NS, c.status);
 }
 
 template <typename T, int D>
 static cudaError_t rebuild_simt(Ctx& c, cudaStream_t st) {
   const size_t smem = sizeof(float) * (static_cast<size_t>(kRbRows) * c.p.r + static_cast<size_t>(c.p.r) * D);
   auto kern = k_rebuild_simt<T, D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid((c.p.k * c.p.c + kRbRows - 1) / kRbRows, c.p.b * c.p.h_kv);
   kern<<<grid, kRbThreads, smem, st>>>(static_cast<const T*>(c.A), static_cast<const T*>(c.Bt),

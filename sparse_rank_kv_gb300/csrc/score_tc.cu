@@ -61,6 +61,7 @@ k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUt
   const int t_end = static_cast<int>(static_cast<long long>(total_tiles) * (blockIdx.x + 1) / gridDim.x);
   const int ntl = t_end - t_begin;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  tc::grid_dep_launch();
 
   if (threadIdx.x == 0) {
     tc::prefetch_tensormap(&mapL);
@@ -239,7 +240,7 @@ template <int D, int G>
 static cudaError_t score_tc_t(Ctx& c, const CUtensorMap& mq, cudaStream_t st) {
   const int smem = sc_smem_bytes(D);
   auto kern = k_score_tc<D, G>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   const int total = c.p.b * c.p.h_kv * c.ntile;
   const int grid = total < c.nsm ? total : c.nsm;
@@ -263,7 +264,8 @@ static cudaError_t score_tc_d(Ctx& c, const CUtensorMap& mq, cudaStream_t st) {
 cudaError_t launch_score_tc(Ctx& c, const void* q, cudaStream_t st) {
   if (!c.tc_score || c.force_simt) return cudaErrorNotSupported;
   CUtensorMap mq;
-  if (encode_q_map(c, q, &mq) != cudaSuccess) return cudaErrorNotSupported;
+  if (q == c.q_buf && c.q_map) mq = c.mapQ;
+  else if (encode_q_map(c, q, &mq) != cudaSuccess) return cudaErrorNotSupported;
   return c.p.d == 128 ? score_tc_d<128>(c, mq, st) : score_tc_d<64>(c, mq, st);
 }
 
