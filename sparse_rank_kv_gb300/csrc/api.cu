@@ -72,14 +72,15 @@ size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 // Byte sizes of every device buffer of a context, in allocation order.
 struct Sizes {
-  size_t A, Bt, L, K_out, V_out, K_loc, V_loc, slot_V, K_sparse;
+  size_t A, Bt, L, K_out, V_out, K_loc, V_loc, slot_V, K_sparse, KV_out, KV_loc, KV_slot;
   size_t min_cos, logits, score_part, attn_part, basis, rope_tab, q_buf;
   size_t out_ids, out_mask, sel, sel_slot, slot_chunk, miss_chunk, miss_slot;
-  size_t miss_count, hits, attn_count, counters, status;
+  size_t miss_count, miss_base, hits, attn_count, counters, status;
   size_t total() const {
-    const size_t v[] = {A, Bt, L, K_out, V_out, K_loc, V_loc, slot_V, K_sparse, min_cos, logits,
+    const size_t v[] = {A, Bt, L, K_out, V_out, K_loc, V_loc, slot_V, K_sparse, KV_out, KV_loc, KV_slot,
+                        min_cos, logits,
                         score_part, attn_part, basis, rope_tab, q_buf, out_ids, out_mask, sel, sel_slot,
-                        slot_chunk, miss_chunk, miss_slot, miss_count, hits, attn_count, counters,
+                        slot_chunk, miss_chunk, miss_slot, miss_count, miss_base, hits, attn_count, counters,
                         status};
     size_t t = 0;
     for (size_t x : v) t += up(x);
@@ -110,7 +111,11 @@ Sizes sizes_of(const shadowkv_params& p) {
   z.L = b * h * n * d * E;
   z.K_out = z.V_out = b * h * o * c * d * E;
   z.K_loc = z.V_loc = b * h * cap * d * E;
-  z.slot_V = z.K_sparse = b * h * k * c * d * E;
+  const bool rec = skv::attn_tc_supported(p);   // records replace slot_V and K_sparse
+  z.slot_V = z.K_sparse = rec ? 0 : b * h * k * c * d * E;
+  z.KV_out = rec ? 2 * z.K_out : 0;
+  z.KV_loc = rec ? 2 * z.K_loc : 0;
+  z.KV_slot = rec ? 2 * b * h * k * c * d * E : 0;
   z.min_cos = b * h * n * 4;
   z.logits = b * hq * n * 4;
   z.score_part = b * hq * ntile * 4 * 8;   // 4 softmax partials per 128-landmark tile
@@ -121,7 +126,7 @@ Sizes sizes_of(const shadowkv_params& p) {
   z.out_ids = b * h * o * 4;
   z.out_mask = b * h * nw * 4;
   z.sel = z.sel_slot = z.slot_chunk = z.miss_chunk = z.miss_slot = b * h * k * 4;
-  z.hits = z.attn_count = b * h * 4;
+  z.hits = z.attn_count = z.miss_base = b * h * 4;
   z.miss_count = 2 * 4;   // compact miss-list length per step parity
   z.counters = 2 * 8;
   z.status = 4;
@@ -207,7 +212,8 @@ skv_status create(const shadowkv_params* p, cudaStream_t st, shadowkv_ctx** out)
   c.G = p->h_q / p->h_kv;
   c.ntile = (c.n + 127) / 128;
   c.loc_cap = loc_cap_of(*p);
-  c.v_tiled = skv::attn_tc_supported(*p);
+  c.kv_rec = skv::attn_tc_supported(*p);
+  c.fetch_sms = c.kv_rec ? skv::kFetchSMsRec : skv::kFetchSMs;
   c.max_splits = max_splits_of(*p);
   c.split_tokens = 128;
   auto bail = [&](skv_status s) { destroy(h); return s; };
@@ -226,6 +232,9 @@ skv_status create(const shadowkv_params* p, cudaStream_t st, shadowkv_ctx** out)
   c.K_out = take(z.K_out); c.V_out = take(z.V_out);
   c.K_loc = take(z.K_loc); c.V_loc = take(z.V_loc);
   c.slot_V = take(z.slot_V); c.K_sparse = take(z.K_sparse);
+  c.KV_out = take(z.KV_out); c.KV_loc = take(z.KV_loc); c.KV_slot = take(z.KV_slot);
+  if (c.kv_rec) c.slot_V = c.K_sparse = nullptr;
+  else c.KV_out = c.KV_loc = c.KV_slot = nullptr;
   c.min_cos = static_cast<float*>(take(z.min_cos));
   c.logits = static_cast<float*>(take(z.logits));
   c.score_part = static_cast<float2*>(take(z.score_part));
@@ -241,6 +250,7 @@ skv_status create(const shadowkv_params* p, cudaStream_t st, shadowkv_ctx** out)
   c.miss_chunk = static_cast<int32_t*>(take(z.miss_chunk));
   c.miss_slot = static_cast<int32_t*>(take(z.miss_slot));
   c.miss_count = static_cast<int32_t*>(take(z.miss_count));
+  c.miss_base = static_cast<int32_t*>(take(z.miss_base));
   c.hits = static_cast<int32_t*>(take(z.hits));
   c.attn_count = static_cast<int32_t*>(take(z.attn_count));
   c.counters = static_cast<unsigned long long*>(take(z.counters));
@@ -254,6 +264,7 @@ skv_status create(const shadowkv_params* p, cudaStream_t st, shadowkv_ctx** out)
   // local window rows not yet written read as zeros (finite under zero weights)
   if (e == cudaSuccess) e = cudaMemsetAsync(c.K_loc, 0, z.K_loc, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(c.V_loc, 0, z.V_loc, st);
+  if (e == cudaSuccess && c.kv_rec) e = cudaMemsetAsync(c.KV_loc, 0, z.KV_loc, st);
   if (e != cudaSuccess) return bail(cuda_fail(e, "fill slot table"));
 
   // RoPE frequency table: inv_freq_i / (2 pi) as an fp32 (hi, lo) pair
@@ -276,8 +287,7 @@ skv_status create(const shadowkv_params* p, cudaStream_t st, shadowkv_ctx** out)
   e = skv::make_rebuild_maps(c);
   if (e == cudaSuccess) e = skv::make_score_map(c);
   if (e == cudaSuccess) e = skv::make_attn_maps(c);
-  if (e == cudaSuccess) e = skv::make_attn_tc_maps(c);
-  if (e == cudaSuccess && (c.tc_score || c.v_tiled)) {
+  if (e == cudaSuccess && (c.tc_score || c.kv_rec)) {
     e = skv::encode_q_map(c, c.q_buf, &c.mapQ);
     c.q_map = e == cudaSuccess;
   }
@@ -407,7 +417,7 @@ skv_status shadowkv_prefill(const shadowkv_params* p, const void* k_pre, const v
   }
   if (e == cudaSuccess) e = skv::prefill_device(c, k_pre, v_src, st);
   if (e == cudaSuccess) e = skv::launch_tile_a(c, 1, st);
-  if (e == cudaSuccess) e = skv::launch_tile_v(c, st);
+  if (e == cudaSuccess) e = skv::launch_pack_kv(c, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) { s = cuda_fail(e, "prefill"); destroy(h); return s; }
   s = read_status(c);
@@ -448,7 +458,7 @@ skv_status shadowkv_load_state(const shadowkv_params* p, const shadowkv_state_in
     e = cudaMemcpy2DAsync(c.V_loc, row * c.loc_cap, in->V_loc, row * p->w, row * p->w, pairs,
                           cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess) e = skv::launch_transpose_b(c, in->B, st);
-  if (e == cudaSuccess) e = skv::launch_tile_v(c, st);
+  if (e == cudaSuccess) e = skv::launch_pack_kv(c, st);
   if (e == cudaSuccess) e = skv::launch_build_mask(c, st);
   if (e == cudaSuccess) {
     if (in->v_on_host) parallel_memcpy(c.v_cpu, in->V, c.v_bytes);
@@ -602,9 +612,13 @@ static void* field_ptr(skv::Ctx& c, int field, size_t* bytes, bool* on_host) {
     case SKV_FIELD_SEL_SLOT: *bytes = z.sel_slot; return c.sel_slot;
     case SKV_FIELD_HITS: *bytes = z.hits; return c.hits;
     case SKV_FIELD_LOGITS: *bytes = z.logits; return c.logits;
-    case SKV_FIELD_K_SPARSE: *bytes = z.K_sparse; return c.K_sparse;
+    case SKV_FIELD_K_SPARSE:
+      *bytes = c.kv_rec ? z.KV_slot / 2 : z.K_sparse;
+      return c.kv_rec ? c.KV_slot : c.K_sparse;
     case SKV_FIELD_SLOT_CHUNK: *bytes = z.slot_chunk; return c.slot_chunk;
-    case SKV_FIELD_SLOT_V: *bytes = z.slot_V; return c.slot_V;
+    case SKV_FIELD_SLOT_V:
+      *bytes = c.kv_rec ? z.KV_slot / 2 : z.slot_V;
+      return c.kv_rec ? c.KV_slot : c.slot_V;
     case SKV_FIELD_V_CPU: *bytes = c.v_bytes; *on_host = true; return c.v_cpu;
     case SKV_FIELD_SVD_BASIS: *bytes = z.basis; return c.has_basis ? c.basis : nullptr;
     default: *bytes = 0; return nullptr;
@@ -637,19 +651,6 @@ static void untile_a_host(const skv::Ctx& c, unsigned char* A) {
   }
 }
 
-// Host copy of tiled values back to row-major, in place: `rows` (a multiple of
-// 8) rows of 128 bf16 in 8-row groups.
-static void untile_v_host(unsigned char* V, size_t rows) {
-  std::vector<uint16_t> tmp(1024);
-  uint16_t* v = reinterpret_cast<uint16_t*>(V);
-  for (size_t g = 0; g < rows / 8; ++g) {
-    uint16_t* grp = v + g * 1024;
-    std::memcpy(tmp.data(), grp, 2048);
-    for (int t = 0; t < 8; ++t)
-      for (int j = 0; j < 128; ++j) grp[t * 128 + j] = tmp[(j >> 3) * 64 + (j & 7) * 8 + t];
-  }
-}
-
 skv_status shadowkv_export(shadowkv_ctx* h, int field, void* dst, size_t bytes) {
   if (!h || !dst) return fail(SKV_ERR_INVALID_ARG, "NULL argument");
   if (field < 0 || field >= SKV_FIELD_COUNT) return fail(SKV_ERR_INVALID_ARG, "unknown field %d", field);
@@ -667,16 +668,36 @@ skv_status shadowkv_export(shadowkv_ctx* h, int field, void* dst, size_t bytes) 
     const size_t row = static_cast<size_t>(c.p.d) * c.E, keep = static_cast<size_t>(c.p.w) + c.p.max_new;
     std::vector<unsigned char> full(pairs * c.loc_cap * row);
     CK(cudaMemcpy(full.data(), src, full.size(), cudaMemcpyDeviceToHost));
-    if (field == SKV_FIELD_V_LOC && c.v_tiled) untile_v_host(full.data(), pairs * c.loc_cap);
     for (size_t pr = 0; pr < pairs; ++pr)
       std::memcpy(static_cast<unsigned char*>(dst) + pr * keep * row, full.data() + pr * c.loc_cap * row, keep * row);
+    return SKV_OK;
+  }
+  if (c.kv_rec && (field == SKV_FIELD_SLOT_V || field == SKV_FIELD_K_SPARSE)) {
+    // from the slot records: values per slot, or the rebuilt keys of the
+    // selected chunks in selection order
+    std::vector<uint16_t> rec(pairs * c.p.k * c.p.c * 256);
+    CK(cudaMemcpy(rec.data(), c.KV_slot, rec.size() * 2, cudaMemcpyDeviceToHost));
+    std::vector<int32_t> sel_slot(pairs * c.p.k);
+    CK(cudaMemcpy(sel_slot.data(), c.sel_slot, sel_slot.size() * 4, cudaMemcpyDeviceToHost));
+    uint16_t* o = static_cast<uint16_t*>(dst);
+    const int gpc = c.p.c / 8;
+    for (size_t pr = 0; pr < pairs; ++pr)
+      for (int i = 0; i < c.p.k; ++i) {
+        const int slot = field == SKV_FIELD_SLOT_V ? i : sel_slot[pr * c.p.k + i];
+        if (slot < 0 || slot >= c.p.k) return fail(SKV_ERR_STATE, "slot %d out of range", slot);
+        for (int u = 0; u < c.p.c; ++u) {
+          const uint16_t* r = rec.data() + ((pr * c.p.k + slot) * gpc + u / 8) * 2048;
+          uint16_t* row = o + ((pr * c.p.k + i) * c.p.c + u) * 128;
+          for (int j = 0; j < 128; ++j)
+            row[j] = field == SKV_FIELD_K_SPARSE ? r[(j >> 3) * 64 + (u & 7) * 8 + (j & 7)]
+                                                 : r[1024 + (j >> 3) * 64 + (j & 7) * 8 + (u & 7)];
+        }
+      }
     return SKV_OK;
   }
   if (on_host) std::memcpy(dst, src, bytes);
   else CK(cudaMemcpy(dst, src, bytes, cudaMemcpyDeviceToHost));
   if (field == SKV_FIELD_A && c.a_tiled) untile_a_host(c, static_cast<unsigned char*>(dst));
-  if (c.v_tiled && (field == SKV_FIELD_V_OUT || field == SKV_FIELD_SLOT_V))
-    untile_v_host(static_cast<unsigned char*>(dst), bytes / (static_cast<size_t>(c.p.d) * c.E));
   return SKV_OK;
 }
 

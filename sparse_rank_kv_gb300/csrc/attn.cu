@@ -58,7 +58,7 @@ k_attn(const T* __restrict__ K_out, const T* __restrict__ V_out, const T* __rest
        const T* __restrict__ K_loc, const T* __restrict__ V_loc, const T* __restrict__ q,
        T* __restrict__ out, float* __restrict__ part, int32_t* __restrict__ ticket, int n_out,
        int n_sp, int n_loc, int loc_cap, int c, int c_shift, int k, int S, int nsplit, int max_splits,
-       float scale_log2, int v_tiled) {
+       float scale_log2, const T* __restrict__ KVo, const T* __restrict__ KVs, const T* __restrict__ KVl) {
   using Lay = AttnLayout<T, D>;
   constexpr int RB = Lay::RB, NCH = Lay::NCH, V = Lay::V;
   constexpr int NDP = D / 2;          // dimension pairs
@@ -95,20 +95,27 @@ k_attn(const T* __restrict__ K_out, const T* __restrict__ V_out, const T* __rest
   const int lc = tid % LPR;
   for (int i = tid / LPR; i < cnt; i += RPI) {
     int t = t0 + i;
-    const T *kr, *vr;
-    int u = 0;   // row within its 8-row group (tiled values)
+    const T *kr = nullptr, *vr = nullptr, *rec = nullptr;
+    int u = 0;   // row within its 8-row group record
     if (t < n_out) {
+      if (KVo) rec = KVo + (static_cast<size_t>(pair) * n_out + (t & ~7)) * 2 * D;
       kr = K_out + (static_cast<size_t>(pair) * n_out + t) * D;
       vr = V_out + (static_cast<size_t>(pair) * n_out + t) * D;
       u = t & 7;
     } else if ((t -= n_out) < n_sp) {
-      kr = K_sp + (static_cast<size_t>(pair) * n_sp + t) * D;
       const int cq = c_shift >= 0 ? (t >> c_shift) : t / c;
       const int slot = s_slot[cq - ch0];
-      vr = slot_V + ((static_cast<size_t>(pair) * k + slot) * c + (t - cq * c)) * D;
-      u = (t - cq * c) & 7;
+      const int rr = t - cq * c;
+      if (KVs) {
+        rec = KVs + ((static_cast<size_t>(pair) * k + slot) * c + (rr & ~7)) * 2 * D;
+      } else {
+        kr = K_sp + (static_cast<size_t>(pair) * n_sp + t) * D;
+        vr = slot_V + ((static_cast<size_t>(pair) * k + slot) * c + rr) * D;
+      }
+      u = rr & 7;
     } else {
       t -= n_sp;
+      if (KVl) rec = KVl + (static_cast<size_t>(pair) * loc_cap + (t & ~7)) * 2 * D;
       kr = K_loc + (static_cast<size_t>(pair) * loc_cap + t) * D;
       vr = V_loc + (static_cast<size_t>(pair) * loc_cap + t) * D;
       u = t & 7;
@@ -117,12 +124,14 @@ k_attn(const T* __restrict__ K_out, const T* __restrict__ V_out, const T* __rest
     unsigned char* vrow = Vs + static_cast<size_t>(i) * RB;
 #pragma unroll
     for (int ch = lc; ch < NCH; ch += LPR) {
-      cp_async16(krow + ((ch ^ (i & (NCH - 1))) << 4), kr + ch * V);
-      if (!v_tiled) {
+      if (rec == nullptr) {
+        cp_async16(krow + ((ch ^ (i & (NCH - 1))) << 4), kr + ch * V);
         cp_async16(vrow + (ch << 4), vr + ch * V);
       } else if constexpr (sizeof(T) == 2 && D == 128) {
-        // tiled group: dimensions 8ch + r of row u sit 8 elements apart
-        const uint16_t* gb = reinterpret_cast<const uint16_t*>(vr - u * D) + ch * 64 + u;
+        // group record: key piece ch of row u contiguous in the K tile;
+        // value dimensions 8ch + r of row u 8 elements apart in the V^T tile
+        cp_async16(krow + ((ch ^ (i & (NCH - 1))) << 4), rec + ch * 64 + u * 8);
+        const uint16_t* gb = reinterpret_cast<const uint16_t*>(rec + 1024) + ch * 64 + u;
         uint32_t w[4];
 #pragma unroll
         for (int r = 0; r < 4; ++r) w[r] = static_cast<uint32_t>(gb[16 * r]) | (static_cast<uint32_t>(gb[16 * r + 8]) << 16);
@@ -300,7 +309,8 @@ static cudaError_t attn_t(Ctx& c, const void* q, void* out, int n_loc, cudaStrea
       static_cast<const T*>(c.K_loc), static_cast<const T*>(c.V_loc), static_cast<const T*>(q),
       static_cast<T*>(out), c.attn_part, c.attn_count, n_out, n_sp, n_loc, c.loc_cap, c.p.c,
       (c.p.c & (c.p.c - 1)) == 0 ? __builtin_ctz(static_cast<unsigned>(c.p.c)) : -1, c.p.k, S, nsplit,
-      c.max_splits, scale_log2, c.v_tiled ? 1 : 0);
+      c.max_splits, scale_log2, static_cast<const T*>(c.KV_out), static_cast<const T*>(c.KV_slot),
+      static_cast<const T*>(c.KV_loc));
   return cudaGetLastError();
 }
 
@@ -317,9 +327,9 @@ static cudaError_t attn_d(Ctx& c, const void* q, void* out, int n_loc, cudaStrea
 cudaError_t launch_attn(Ctx& c, const void* q, void* out, int n_loc, cudaStream_t st) {
   kbegin(c, K_ATTN, st);
   cudaError_t e;
-  if (c.v_tiled && !c.force_simt && !c.split_set)
+  if (c.kv_rec && !c.force_simt && !c.split_set)
     e = launch_attn_tc(c, q, out, n_loc, st);
-  else if (c.attn_pipe && !c.v_tiled && !c.force_simt && !c.split_set)
+  else if (c.attn_pipe && !c.kv_rec && !c.force_simt && !c.split_set)
     e = launch_attn_pipe(c, q, out, n_loc, st);
   else if (c.p.dtype == SKV_DTYPE_BF16)
     e = c.p.d == 128 ? attn_d<bf16, 128>(c, q, out, n_loc, st) : attn_d<bf16, 64>(c, q, out, n_loc, st);
@@ -375,7 +385,7 @@ cudaError_t noalloc_launch(const shadowkv_params& p, const void* q, const void* 
       static_cast<const T*>(K), static_cast<const T*>(V), static_cast<const T*>(K),
       static_cast<const T*>(V), nullptr, static_cast<const T*>(K), static_cast<const T*>(V),
       static_cast<const T*>(q), static_cast<T*>(out), part, ticket, n_tokens, 0, 0, 0, 1, 0, 1, S,
-      nsplit, nsplit, scale_log2, 0);
+      nsplit, nsplit, scale_log2, nullptr, nullptr, nullptr);
   return cudaGetLastError();
 }
 

@@ -8,13 +8,13 @@
 // contiguous range of items.
 //   warp 0     : producer -- the head's q (TMA, 16 rows of which the rows
 //                past G read as zeros) into a 2-slot ring when the head
-//                changes; per item the K rows by TMA (4 boxes of 32 columns x
-//                128 rows, 64-byte swizzle) and the V rows by bulk copies
-//                into a 3-stage ring.  V is stored in HBM in 8-token groups
-//                laid out as the tensor core's no-swizzle K-major tiles of
-//                V^T ([d/8][d%8][token%8], 2 KB per group), so a selected
-//                chunk is one copy from its cache slot and the outliers or
-//                the local window one copy per item.
+//                changes; per item the keys and values by bulk copies into a
+//                3-stage ring.  Keys and values are stored by 8-token group
+//                in 4 KB records laid out as the tensor core's no-swizzle
+//                K-major tiles: K ([d/8][token%8][d%8], 2 KB), then V^T
+//                ([d/8][d%8][token%8], 2 KB); a selected chunk is one copy
+//                from its cache slot, the outliers or the local window one
+//                copy per item.
 //   warp 1     : tcgen05.mma.  S = K q^T (M = 128 tokens, N = 16, K = d) into
 //                one of two TMEM S buffers; after the softmax warps publish
 //                P, O = V^T P^T (M = d, N = 16, K = 128 tokens) into one of
@@ -30,8 +30,6 @@
 //                its first item of that head; the CTA that completes a head's
 //                last items (atomic count) combines the partials in slot
 //                order (the slots follow from the fixed item ranges).
-#include <cudaTypedefs.h>
-
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
@@ -44,9 +42,7 @@ constexpr int kAtStages = 3;
 constexpr int kAtThreads = 192;
 constexpr int kAtSoft = 128;                 // softmax / accumulation threads
 constexpr int kAtMaxSlots = 64;
-constexpr int kAtKBytes = kAtT * kAtD * 2;   // K tile: 4 x [128 rows][64 B]
-constexpr int kAtVBytes = kAtT * kAtD * 2;   // V tile: 16 groups x 2 KB
-constexpr int kAtStage = kAtKBytes + kAtVBytes;
+constexpr int kAtStage = kAtT / 8 * 4096;   // 16 group records (K tile | V^T tile)
 constexpr int kAtQBytes = 16 * kAtD * 2;     // q: 4 x [16 rows][64 B]
 constexpr int kAtPBytes = 16 * kAtT * 2;     // P^T: 16 x 128 bf16
 __host__ __device__ constexpr int at_smem_bytes() {
@@ -67,10 +63,9 @@ __device__ __forceinline__ AtSeg at_item(int j, int i_out, int i_sp, int n_out, 
 
 template <int G>
 __global__ void __launch_bounds__(kAtThreads, 1)
-k_attn_tc(const __grid_constant__ CUtensorMap mapKo, const __grid_constant__ CUtensorMap mapKs,
-          const __grid_constant__ CUtensorMap mapKl, const __grid_constant__ CUtensorMap mapQ,
-          const bf16* __restrict__ V_out, const bf16* __restrict__ slot_V,
-          const int32_t* __restrict__ sel_slot, const bf16* __restrict__ V_loc,
+k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_out,
+          const bf16* __restrict__ KV_slot, const int32_t* __restrict__ sel_slot,
+          const bf16* __restrict__ KV_loc,
           bf16* __restrict__ out, float* __restrict__ part, int32_t* __restrict__ ticket, int n_out,
           int n_sp, int n_loc, int loc_cap, int c, int k, int npairs, int max_splits, float scale_log2,
           int* __restrict__ status) {
@@ -110,10 +105,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapKo, const __grid_constant__ CUt
   tc::grid_dep_launch();
 
   if (tid == 0) {
-    tc::prefetch_tensormap(&mapKs);
     tc::prefetch_tensormap(&mapQ);
-    if (n_out > 0) tc::prefetch_tensormap(&mapKo);
-    if (n_loc > 0) tc::prefetch_tensormap(&mapKl);
     for (int i = 0; i < kAtStages; ++i) {
       tc::mbar_init(&full[i], 1);
       tc::mbar_init(&empty[i], 1);
@@ -134,12 +126,10 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapKo, const __grid_constant__ CUt
     tc::tmem_alloc(tmem_slot, 64);
     tc::tmem_relinquish();
   }
-  // V tiles past a partial item and the P rows past G are multiplied by
+  // records past a partial item and the P rows past G are multiplied by
   // zero weights: start them at zero so that they are finite
-  for (int s = 0; s < kAtStages; ++s) {
-    uint4* z = reinterpret_cast<uint4*>(stages + s * kAtStage + kAtKBytes);
-    for (int i = tid; i < kAtVBytes / 16; i += kAtThreads) z[i] = make_uint4(0, 0, 0, 0);
-  }
+  for (int i = tid; i < kAtStages * kAtStage / 16; i += kAtThreads)
+    reinterpret_cast<uint4*>(stages)[i] = make_uint4(0, 0, 0, 0);
   for (int i = tid; i < 2 * kAtPBytes / 16; i += kAtThreads)
     reinterpret_cast<uint4*>(pbuf)[i] = make_uint4(0, 0, 0, 0);
   tc::fence_proxy_async_smem();
@@ -193,26 +183,21 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapKo, const __grid_constant__ CUt
         if (lane == 0) abort_now();
         break;
       }
-      unsigned char* sK = stages + st * kAtStage;
-      unsigned char* sV = sK + kAtKBytes;
-      const int vgroups = (sg.cnt + 7) >> 3;
+      unsigned char* sR = stages + st * kAtStage;
+      const int groups = (sg.cnt + 7) >> 3;
       if (lane == 0) {
-        tc::mbar_expect_tx(&full[st], static_cast<uint32_t>(kAtKBytes + vgroups * 2048));
-        const CUtensorMap* m = sg.seg == 0 ? &mapKo : sg.seg == 1 ? &mapKs : &mapKl;
-#pragma unroll
-        for (int kb = 0; kb < kAtD / 32; ++kb)
-          tc::tma_load_3d(sK + kb * (kAtT * 64), m, &full[st], kb * 32, sg.t0, pair);
+        tc::mbar_expect_tx(&full[st], static_cast<uint32_t>(groups * 4096));
         if (sg.seg == 0)
-          tc::bulk_load(sV, V_out + (static_cast<size_t>(pair) * n_out + sg.t0) * kAtD,
-                        static_cast<uint32_t>(vgroups * 2048), &full[st]);
+          tc::bulk_load(sR, KV_out + (static_cast<size_t>(pair) * n_out + sg.t0) * 2 * kAtD,
+                        static_cast<uint32_t>(groups * 4096), &full[st]);
         else if (sg.seg == 2)
-          tc::bulk_load(sV, V_loc + (static_cast<size_t>(pair) * loc_cap + sg.t0) * kAtD,
-                        static_cast<uint32_t>(vgroups * 2048), &full[st]);
+          tc::bulk_load(sR, KV_loc + (static_cast<size_t>(pair) * loc_cap + sg.t0) * 2 * kAtD,
+                        static_cast<uint32_t>(groups * 4096), &full[st]);
       }
       __syncwarp();
       if (lane < nch)
-        tc::bulk_load(sV + lane * c * kAtD * 2, slot_V + (static_cast<size_t>(pair) * k + slot) * c * kAtD,
-                      static_cast<uint32_t>(c * kAtD * 2), &full[st]);
+        tc::bulk_load(sR + lane * c * 512, KV_slot + (static_cast<size_t>(pair) * k + slot) * c * 2 * kAtD,
+                      static_cast<uint32_t>(c * 512), &full[st]);
       lastA[st] = use;
     }
     if (lane == 0) {
@@ -250,11 +235,13 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapKo, const __grid_constant__ CUt
         tc::fence_after();
         const uint32_t a0 = tc::smem_u32(stages + st * kAtStage);
         const uint32_t b0 = tc::smem_u32(qbuf + (nq & 1) * kAtQBytes);
+        // K tiles: core matrices of 8 tokens x 8 dims; dim groups 128 B
+        // apart, token groups (records) 4 KB apart.  q: 64-byte swizzle.
 #pragma unroll
         for (int kb = 0; kb < kAtD / 32; ++kb)
 #pragma unroll
           for (int ks = 0; ks < 2; ++ks)
-            tc::mma_bf16(tmem + sb * 16, tc::desc_k_sw64(a0 + kb * (kAtT * 64) + ks * 32, 512),
+            tc::mma_bf16(tmem + sb * 16, tc::desc_k_none(a0 + (kb * 2 + ks) * 256, 128, 4096),
                          tc::desc_k_sw64(b0 + kb * (16 * 64) + ks * 32, 512), idesc, (kb | ks) != 0);
         tc::mma_commit(&sfull[sb]);
         const bool last_of_pair = it == nit - 1 || (item + 1) / nsplit != pair;
@@ -267,14 +254,14 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapKo, const __grid_constant__ CUt
       auto issue_o = [&](int it) {
         const int st = it % kAtStages, b = it & 1;
         tc::fence_after();
-        const uint32_t a0 = tc::smem_u32(stages + st * kAtStage + kAtKBytes);
+        const uint32_t a0 = tc::smem_u32(stages + st * kAtStage + 2048);
         const uint32_t b0 = tc::smem_u32(pbuf + b * kAtPBytes);
-        // V^T: core matrices of 8 dims x 8 tokens; 8-dim groups 128 B apart,
-        // 8-token groups 2 KB apart.  P^T: 8 heads x 8 tokens; head groups
-        // 128 B apart, token groups 256 B apart.  16 tokens per MMA.
+        // V^T: core matrices of 8 dims x 8 tokens; dim groups 128 B apart,
+        // token groups (records) 4 KB apart.  P^T: 8 heads x 8 tokens; head
+        // groups 128 B apart, token groups 256 B apart.  16 tokens per MMA.
 #pragma unroll
         for (int ks = 0; ks < kAtT / 16; ++ks)
-          tc::mma_bf16(tmem + 32 + b * 16, tc::desc_k_none(a0 + ks * 4096, 2048, 128),
+          tc::mma_bf16(tmem + 32 + b * 16, tc::desc_k_none(a0 + ks * 8192, 4096, 128),
                        tc::desc_k_none(b0 + ks * 512, 256, 128), idesc, ks != 0);
         tc::mma_commit(&ofull[b]);
         tc::mma_commit(&empty[st]);
@@ -496,47 +483,9 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapKo, const __grid_constant__ CUt
 }
 
 // ---------------------------------------------------------------- host side
-static PFN_cuTensorMapEncodeTiled_v12000 at_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult qr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &qr) ==
-            cudaSuccess &&
-        qr == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
-// 3D bf16 map over [pairs][rows][128]: box 32 columns x 128 rows x 1, 64-byte
-// swizzle; rows past `rows` of a head read as zeros.
-static cudaError_t at_encode_k(CUtensorMap* map, void* base, int rows, uint64_t pairs) {
-  auto fn = at_encode_fn();
-  if (!fn) return cudaErrorNotSupported;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kAtD), static_cast<cuuint64_t>(rows), pairs};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kAtD) * 2, static_cast<cuuint64_t>(rows) * kAtD * 2};
-  const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(kAtT), 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 bool attn_tc_supported(const shadowkv_params& p) {
   return p.dtype == SKV_DTYPE_BF16 && p.d == kAtD && p.c % 8 == 0 && kAtT % p.c == 0 &&
-         at_smem_bytes() <= 227 * 1024;
-}
-
-cudaError_t make_attn_tc_maps(Ctx& c) {
-  if (!c.v_tiled) return cudaSuccess;
-  const uint64_t pairs = static_cast<uint64_t>(c.p.b) * c.p.h_kv;
-  const int n_out = c.p.o * c.p.c;
-  cudaError_t e = at_encode_k(&c.mapTs, c.K_sparse, c.p.k * c.p.c, pairs);
-  if (e == cudaSuccess && n_out > 0) e = at_encode_k(&c.mapTo, c.K_out, n_out, pairs);
-  if (e == cudaSuccess) e = at_encode_k(&c.mapTl, c.K_loc, c.loc_cap, pairs);
-  return e;
+         static_cast<long long>(p.b) * p.h_kv <= 1024 && at_smem_bytes() <= 227 * 1024;
 }
 
 int attn_tc_splits(const Ctx& c, int n_loc) {
@@ -554,9 +503,9 @@ static cudaError_t attn_tc_t(Ctx& c, const CUtensorMap& mq, void* out, int n_loc
   const int items = npairs * attn_tc_splits(c, n_loc);
   const int grid = std::min(std::min(c.nsm, items), npairs * (kAtMaxSlots - 2));
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kAtD));
-  return launch_pdl(kern, dim3(grid), dim3(kAtThreads), smem, st, c.mapTo, c.mapTs, c.mapTl, mq,
-                    static_cast<const bf16*>(c.V_out), static_cast<const bf16*>(c.slot_V),
-                    static_cast<const int32_t*>(c.sel_slot), static_cast<const bf16*>(c.V_loc),
+  return launch_pdl(kern, dim3(grid), dim3(kAtThreads), smem, st, mq, static_cast<const bf16*>(c.KV_out),
+                    static_cast<const bf16*>(c.KV_slot), static_cast<const int32_t*>(c.sel_slot),
+                    static_cast<const bf16*>(c.KV_loc),
                     static_cast<bf16*>(out), c.attn_part, c.attn_count, c.p.o * c.p.c, c.p.k * c.p.c,
                     n_loc, c.loc_cap, c.p.c, c.p.k, npairs, c.max_splits, scale_log2, c.status);
 }

@@ -77,10 +77,12 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part,
          const uint32_t* __restrict__ mask, int n, int ntile, int k, int group_reduce,
          int cache_on, int32_t* __restrict__ sel, int32_t* __restrict__ sel_slot,
          int32_t* __restrict__ slot_chunk, int32_t* __restrict__ miss_chunk,
-         int32_t* __restrict__ miss_slot, int32_t* __restrict__ miss_total, int par,
+         int32_t* __restrict__ miss_slot, int32_t* __restrict__ miss_total,
+         int32_t* __restrict__ miss_base, int par,
          int32_t* __restrict__ hits, unsigned long long* __restrict__ counters,
          const T* __restrict__ k_new, const T* __restrict__ v_new, T* __restrict__ K_loc,
-         T* __restrict__ V_loc, int loc_row, int loc_cap, int v_tiled, int* __restrict__ status) {
+         T* __restrict__ V_loc, T* __restrict__ KV_loc, int loc_row, int loc_cap,
+         int* __restrict__ status) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int nw = (n + 31) >> 5;
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
@@ -104,9 +106,15 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part,
   if (k_new != nullptr) {
     for (int i = tid; i < D; i += nthr) {
       const size_t dst = (static_cast<size_t>(pair) * loc_cap + loc_row) * D + i;
-      K_loc[dst] = k_new[static_cast<size_t>(pair) * D + i];
-      const size_t vdst = v_tiled ? static_cast<size_t>(pair) * loc_cap * D + vt_off(loc_row, i) : dst;
-      V_loc[vdst] = v_new[static_cast<size_t>(pair) * D + i];
+      const T kv = k_new[static_cast<size_t>(pair) * D + i], vv = v_new[static_cast<size_t>(pair) * D + i];
+      K_loc[dst] = kv;
+      V_loc[dst] = vv;
+      if (KV_loc != nullptr) {
+        // the token's place in its group record: K tile, then V^T tile
+        T* rec = KV_loc + (static_cast<size_t>(pair) * loc_cap + (loc_row & ~7)) * 2 * D;
+        rec[(i >> 3) * 64 + (loc_row & 7) * 8 + (i & 7)] = kv;
+        rec[1024 + (i >> 3) * 64 + (i & 7) * 8 + (loc_row & 7)] = vv;
+      }
     }
   }
   tc::grid_dep_wait();   // the logits and partials of the score kernel
@@ -218,6 +226,7 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part,
   __shared__ int s_base;
   if (tid == 0) {
     s_base = atomicAdd(&miss_total[par], min(nmiss, nfree));
+    miss_base[pair] = s_base;
     if (pair == 0) miss_total[par ^ 1] = 0;
   }
   __syncthreads();
@@ -242,7 +251,7 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part,
 
 // ------------------------------------------------------------------ fetch
 // The step's misses form one compact list (entries pair * n + chunk and
-// pair * k + slot, count miss_total[par]).  A small fixed grid (kFetchSMs
+// pair * k + slot, count miss_total[par]).  A small fixed grid (fetch_sms
 // blocks of 32 warps, enough loads in flight to fill the host link) walks it,
 // a warp per chunk: c*d elements read from pinned host memory through its
 // mapped device address into the chunk's cache slot.  The key rebuild,
@@ -288,11 +297,12 @@ k_fetch(const T* __restrict__ vcpu, T* __restrict__ slot_V, const int32_t* __res
   }
 }
 
-// Tiled-value fetch (bf16, d = 128): a half-warp per 8-token group, lane q
-// reading the 16-byte piece q of the group's 8 rows from pinned host memory
-// and writing the group's 16 x 8 tiled units (one 128-byte run per lane).
+// Fetch into slot records (bf16, d = 128): a half-warp per 8-token group,
+// lane q reading the 16-byte piece q of the group's 8 rows from pinned host
+// memory and writing the V^T half of the group's record (one 128-byte run per
+// lane).
 __global__ void __launch_bounds__(kFetchWarps * 32)
-k_fetch_tiled(const bf16* __restrict__ vcpu, bf16* __restrict__ slot_V, const int32_t* __restrict__ miss_chunk,
+k_fetch_rec(const bf16* __restrict__ vcpu, bf16* __restrict__ KV_slot, const int32_t* __restrict__ miss_chunk,
               const int32_t* __restrict__ miss_slot, const int32_t* __restrict__ miss_total, int par, int s,
               int n, int c, int k, int npairs, int* __restrict__ status) {
   const int lane = threadIdx.x & 31, q = lane & 15;
@@ -315,7 +325,7 @@ k_fetch_tiled(const bf16* __restrict__ vcpu, bf16* __restrict__ slot_V, const in
     }
     const uint4* src = reinterpret_cast<const uint4*>(
         vcpu + (static_cast<size_t>(pair) * s + static_cast<size_t>(chunk) * c + gs * 8) * 128);
-    uint4* dst = reinterpret_cast<uint4*>(slot_V + ((static_cast<size_t>(pair) * k + slot) * c + gs * 8) * 128);
+    uint4* dst = reinterpret_cast<uint4*>(KV_slot + ((static_cast<size_t>(pair) * k + slot) * c + gs * 8) * 256 + 1024);
     uint4 in[8], outv[8];
 #pragma unroll
     for (int t = 0; t < 8; ++t) in[t] = src[t * 16 + q];
@@ -325,39 +335,40 @@ k_fetch_tiled(const bf16* __restrict__ vcpu, bf16* __restrict__ slot_V, const in
   }
 }
 
-// In-place tiling of the 8-row groups of a row-major [rows][128] bf16 array
-// (rows a multiple of 8), a half-warp per group.
-__global__ void __launch_bounds__(256) k_tile_v(bf16* __restrict__ V, long long groups) {
+// Records of row-major [rows][128] bf16 keys and values (rows a multiple of
+// 8): a half-warp per 8-token group, lane q moving the 16-byte piece q of the
+// group's key rows into the K tile (pieces ordered [q][row]) and the
+// transposed values into the V^T tile.
+__global__ void __launch_bounds__(256)
+k_pack_kv(const bf16* __restrict__ K, const bf16* __restrict__ V, bf16* __restrict__ KV, long long groups) {
   const int lane = threadIdx.x & 31, q = lane & 15;
   const long long h0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
   const long long nh = (static_cast<long long>(gridDim.x) * blockDim.x) >> 4;
-  const long long iters = (groups + nh - 1) / nh;
-  for (long long it = 0; it < iters; ++it) {
-    const long long g = h0 + it * nh;
-    const bool on = g < groups;
-    uint4* base = reinterpret_cast<uint4*>(V + (on ? g : 0) * 1024);
+  for (long long g = h0; g < groups; g += nh) {
+    const uint4* ks = reinterpret_cast<const uint4*>(K + g * 1024);
+    const uint4* vs = reinterpret_cast<const uint4*>(V + g * 1024);
+    uint4* rec = reinterpret_cast<uint4*>(KV + g * 2048);
     uint4 in[8], outv[8];
 #pragma unroll
-    for (int t = 0; t < 8; ++t) in[t] = on ? base[t * 16 + q] : make_uint4(0, 0, 0, 0);
-    transpose8x8(in, outv);
-    __syncwarp();   // every lane of the group has read it before any writes
-    if (on) {
+    for (int t = 0; t < 8; ++t) rec[q * 8 + t] = ks[t * 16 + q];
 #pragma unroll
-      for (int r = 0; r < 8; ++r) base[q * 8 + r] = outv[r];
-    }
+    for (int t = 0; t < 8; ++t) in[t] = vs[t * 16 + q];
+    transpose8x8(in, outv);
+#pragma unroll
+    for (int r = 0; r < 8; ++r) rec[128 + q * 8 + r] = outv[r];
   }
 }
 
-cudaError_t launch_tile_v(Ctx& c, cudaStream_t st) {
-  if (!c.v_tiled) return cudaSuccess;
+cudaError_t launch_pack_kv(Ctx& c, cudaStream_t st) {
+  if (!c.kv_rec) return cudaSuccess;
   const long long pairs = static_cast<long long>(c.p.b) * c.p.h_kv;
   const long long g_out = pairs * c.p.o * c.p.c / 8, g_loc = pairs * c.loc_cap / 8;
   kbegin(c, K_MISC, st);
   if (g_out > 0)
-    k_tile_v<<<static_cast<int>(std::min<long long>((g_out + 15) / 16, 8LL * c.nsm)), 256, 0, st>>>(
-        static_cast<bf16*>(c.V_out), g_out);
-  k_tile_v<<<static_cast<int>(std::min<long long>((g_loc + 15) / 16, 8LL * c.nsm)), 256, 0, st>>>(
-      static_cast<bf16*>(c.V_loc), g_loc);
+    k_pack_kv<<<static_cast<int>(std::min<long long>((g_out + 15) / 16, 8LL * c.nsm)), 256, 0, st>>>(
+        static_cast<const bf16*>(c.K_out), static_cast<const bf16*>(c.V_out), static_cast<bf16*>(c.KV_out), g_out);
+  k_pack_kv<<<static_cast<int>(std::min<long long>((g_loc + 15) / 16, 8LL * c.nsm)), 256, 0, st>>>(
+      static_cast<const bf16*>(c.K_loc), static_cast<const bf16*>(c.V_loc), static_cast<bf16*>(c.KV_loc), g_loc);
   kend(c, K_MISC, st);
   return cudaGetLastError();
 }
@@ -436,9 +447,9 @@ static cudaError_t select_t(Ctx& c, const void* k_new, const void* v_new, int lo
   return launch_pdl(kern, dim3(c.p.b * c.p.h_kv), dim3(kSelectThreads), smem, st,
       c.logits, c.score_part, c.out_mask, c.n, c.ntile, c.p.k, c.p.group_reduce,
       c.cache_on ? 1 : 0, c.sel, c.sel_slot, c.slot_chunk, c.miss_chunk, c.miss_slot,
-      c.miss_count, static_cast<int>(c.t & 1), c.hits, c.counters, static_cast<const T*>(k_new),
+      c.miss_count, c.miss_base, static_cast<int>(c.t & 1), c.hits, c.counters, static_cast<const T*>(k_new),
       static_cast<const T*>(v_new),
-      static_cast<T*>(c.K_loc), static_cast<T*>(c.V_loc), loc_row, c.loc_cap, c.v_tiled ? 1 : 0,
+      static_cast<T*>(c.K_loc), static_cast<T*>(c.V_loc), static_cast<T*>(c.KV_loc), loc_row, c.loc_cap,
       c.status);
 }
 
@@ -470,16 +481,16 @@ cudaError_t launch_fetch(Ctx& c, cudaStream_t st) {
   kbegin(c, K_FETCH, st);
   const int par = static_cast<int>(c.t & 1);
   const int npairs = c.p.b * c.p.h_kv;
-  if (c.v_tiled)
-    k_fetch_tiled<<<std::min(c.nsm, kFetchSMs), kFetchWarps * 32, 0, st>>>(
-        static_cast<const bf16*>(c.v_cpu_dev), static_cast<bf16*>(c.slot_V), c.miss_chunk,
+  if (c.kv_rec)
+    k_fetch_rec<<<std::min(c.nsm, c.fetch_sms), kFetchWarps * 32, 0, st>>>(
+        static_cast<const bf16*>(c.v_cpu_dev), static_cast<bf16*>(c.KV_slot), c.miss_chunk,
         c.miss_slot, c.miss_count, par, c.p.s, c.n, c.p.c, c.p.k, npairs, c.status);
   else if (c.p.dtype == SKV_DTYPE_BF16)
-    k_fetch<bf16><<<std::min(c.nsm, kFetchSMs), kFetchWarps * 32, 0, st>>>(
+    k_fetch<bf16><<<std::min(c.nsm, c.fetch_sms), kFetchWarps * 32, 0, st>>>(
         static_cast<const bf16*>(c.v_cpu_dev), static_cast<bf16*>(c.slot_V), c.miss_chunk,
         c.miss_slot, c.miss_count, par, c.p.s, c.n, c.p.c, c.p.d, c.p.k, npairs, c.status);
   else
-    k_fetch<float><<<std::min(c.nsm, kFetchSMs), kFetchWarps * 32, 0, st>>>(
+    k_fetch<float><<<std::min(c.nsm, c.fetch_sms), kFetchWarps * 32, 0, st>>>(
         static_cast<const float*>(c.v_cpu_dev), static_cast<float*>(c.slot_V), c.miss_chunk,
         c.miss_slot, c.miss_count, par, c.p.s, c.n, c.p.c, c.p.d, c.p.k, npairs, c.status);
   kend(c, K_FETCH, st);

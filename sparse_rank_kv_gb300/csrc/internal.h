@@ -36,8 +36,11 @@ struct Timed {
 };
 
 // SMs reserved for the host-memory value fetch, which runs on a side stream
-// next to the key rebuild; the rebuild's grid leaves them free.
+// next to the key rebuild; the rebuild's grid leaves them free.  When only
+// the missed chunks are rebuilt (records) the rebuild is small and the fetch
+// gets more SMs.
 constexpr int kFetchSMs = 16;
+constexpr int kFetchSMsRec = 48;
 
 struct Ctx {
   shadowkv_params p{};
@@ -80,8 +83,13 @@ struct Ctx {
   // tensor-core rebuild: TMA descriptors of A (b*s x r) and B^T (b*h_kv*d x r)
   CUtensorMap mapBt{}, mapK{};
   bool a_tiled = false;   // chunked region of A stored in 8-token core-matrix groups
-  bool v_tiled = false;   // V_out, V_loc, slot_V stored in 8-token tiled groups (tensor-core attention)
-  CUtensorMap mapTs{}, mapTo{}, mapTl{};   // K_sparse, K_out, K_loc for the tensor-core attention
+  // Tensor-core attention (bf16, d = 128): keys and values of every 8-token
+  // group in one 4 KB record, K tiles then V^T tiles in the MMA operand order;
+  // the cache slots keep their rebuilt keys, so only missed chunks are rebuilt
+  bool kv_rec = false;
+  int fetch_sms = kFetchSMs;
+  void *KV_out = nullptr, *KV_loc = nullptr, *KV_slot = nullptr;
+  int32_t* miss_base = nullptr;   // per (batch, KV head): start of its misses in the step's list
   // the step's queries, copied from the caller's buffer so that their
   // tensor map (mapQ, 16-row boxes) is encoded once
   void* q_buf = nullptr;
@@ -159,9 +167,8 @@ cudaError_t launch_rebuild(Ctx& c, cudaStream_t st);
 bool tc_rebuild_supported(const shadowkv_params& p);
 cudaError_t make_rebuild_maps(Ctx& c);   // encodes mapBt
 cudaError_t launch_tile_a(Ctx& c, int to_tiled, cudaStream_t st);   // no-op unless a_tiled
-cudaError_t launch_tile_v(Ctx& c, cudaStream_t st);                 // no-op unless v_tiled
+cudaError_t launch_pack_kv(Ctx& c, cudaStream_t st);                // records of outliers and local window (kv_rec)
 bool attn_tc_supported(const shadowkv_params& p);
-cudaError_t make_attn_tc_maps(Ctx& c);
 cudaError_t launch_attn_tc(Ctx& c, const void* q, void* out, int n_loc, cudaStream_t st);
 cudaError_t encode_q_map(const Ctx& c, const void* q, CUtensorMap* map);
 // prefill_kernels.cu

@@ -88,7 +88,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kRbThreads)
 k_rebuild_simt(const T* __restrict__ A, const T* __restrict__ Bt, const int32_t* __restrict__ sel,
                const float2* __restrict__ rope_tab, T* __restrict__ K_sp, int h_kv, int s, int r,
-               int c, int k, int a_tiled) {
+               int c, int k, int a_tiled, const int32_t* __restrict__ sel_slot, T* __restrict__ KV_slot) {
   extern __shared__ __align__(16) float sm[];
   float* As = sm;                 // [kRbRows][r]
   float* Bs = sm + kRbRows * r;   // [r][D]
@@ -142,15 +142,26 @@ k_rebuild_simt(const T* __restrict__ A, const T* __restrict__ Bt, const int32_t*
     if (R >= rows) continue;
     const int chunk = sel[static_cast<size_t>(pair) * k + R / c];
     const int pos = chunk * c + (R % c);
-    T* dst = K_sp + (static_cast<size_t>(pair) * rows + R) * D;
+    // row-major K_sparse, or (records) the K tile of the chunk's slot record:
+    // element (row u, column j) at (j / 8) * 64 + (u % 8) * 8 + j % 8
+    T* dst;
+    int u8 = 0;
+    if (KV_slot != nullptr) {
+      const int u = R % c, slot = sel_slot[static_cast<size_t>(pair) * k + R / c];
+      dst = KV_slot + ((static_cast<size_t>(pair) * k + slot) * (c / 8) + (u >> 3)) * 2048;
+      u8 = u & 7;
+    } else {
+      dst = K_sp + (static_cast<size_t>(pair) * rows + R) * D;
+    }
+    auto at = [&](int j) -> T& { return KV_slot != nullptr ? dst[(j >> 3) * 64 + u8 * 8 + (j & 7)] : dst[j]; };
 #pragma unroll
     for (int j = 0; j < CJ / 2; ++j) {
       const int col = tx + 32 * j;
       float sn, cs;
       rope_sincos(pos, rope_tab[col], &sn, &cs);
       const float x1 = acc[i][j], x2 = acc[i][j + CJ / 2];
-      dst[col] = Ty<T>::from_f(x1 * cs - x2 * sn);
-      dst[col + D / 2] = Ty<T>::from_f(x2 * cs + x1 * sn);
+      at(col) = Ty<T>::from_f(x1 * cs - x2 * sn);
+      at(col + D / 2) = Ty<T>::from_f(x2 * cs + x1 * sn);
     }
   }
 }
@@ -205,13 +216,20 @@ static PipeShape pipe_shape(int r, int D) {
   return {0, 0, 0, 0};
 }
 
-template <int D>
+// REC = false: every selected row, in selection order, to K_sparse (TMA
+// store).  REC = true (d = 128): only the chunks that missed the cache, from
+// the step's miss list, into the K tiles of their slot records; the other
+// slots keep the keys rebuilt at earlier steps (the rebuilt keys of a chunk
+// depend only on A, B and its positions).
+template <int D, bool REC>
 __global__ void __launch_bounds__(kPipeThreads, 1)
 k_rebuild_pipe(const bf16* __restrict__ A, const __grid_constant__ CUtensorMap mapBt,
                const __grid_constant__ CUtensorMap mapK,
                const int32_t* __restrict__ sel, const float2* __restrict__ rope_tab,
-               int npairs, int h_kv, int s, int r, int c, int k, int S,
-               int NB, int NS, int* __restrict__ status) {
+               const int32_t* __restrict__ miss_chunk, const int32_t* __restrict__ miss_slot,
+               const int32_t* __restrict__ miss_base, const int32_t* __restrict__ hits,
+               bf16* __restrict__ KV_slot, int n, int npairs, int h_kv, int s, int r, int c, int k,
+               int S, int NB, int NS, int* __restrict__ status) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -230,31 +248,60 @@ k_rebuild_pipe(const bf16* __restrict__ A, const __grid_constant__ CUtensorMap m
   const int a_bytes = pipe_a_bytes(r);
   unsigned char* sB = sA + S * a_bytes;
   unsigned char* stage0 = sB + NB * pipe_b_bytes(KB, D);   // NS x [D/64][128][128 B], 1024-aligned
+  int* s_tp = reinterpret_cast<int*>(stage0 + NS * (kTcRows * D * 2));   // REC: tile prefix [npairs + 1]
+  int* s_rows = s_tp + npairs + 1;                                      // REC: missed rows per head
+  int* s_mb = s_rows + npairs;                                          // REC: miss-list start per head
 
   const int rows = k * c;
   const int tpp = (rows + kTcRows - 1) / kTcRows;        // tiles per (batch, KV head)
-  const int total = npairs * tpp;
-  const int lo = static_cast<int>(static_cast<long long>(blockIdx.x) * total / gridDim.x);
-  const int hi = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * total / gridDim.x);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row = (warp & 3) * 32 + lane;   // epilogue: TMEM lane = tile row
+  int total = npairs * tpp, lo = 0, hi = 0;
 
+  // a tile: its head, first row, rows, and the index of its first chunk in
+  // the selection (REC: in the step's miss list)
+  struct Tile {
+    int pair, row0, nrow, e0;
+  };
+  auto tinfo = [&](int tile) -> Tile {
+    if constexpr (REC) {
+      int a = 0, b = npairs;   // the last head whose tiles start at or before `tile`
+      while (b - a > 1) {
+        const int m = (a + b) >> 1;
+        if (s_tp[m] <= tile) a = m;
+        else b = m;
+      }
+      const int r0 = (tile - s_tp[a]) * kTcRows;
+      return {a, r0, min(kTcRows, s_rows[a] - r0), s_mb[a] + r0 / c};
+    } else {
+      const int pr = tile / tpp, r0 = (tile - pr * tpp) * kTcRows;
+      return {pr, r0, min(kTcRows, rows - r0), pr * k + r0 / c};
+    }
+  };
+  auto chunk_at = [&](int e, int pr) -> int {
+    if constexpr (REC) return miss_chunk[e] - pr * n;
+    else return sel[e];
+  };
   // producer lane l: chunk id of the tile's l-th chunk (<= 128 / 8 chunks)
   auto chunk_ids = [&](int tile) {
-    const int pr = tile / tpp, r0 = (tile - pr * tpp) * kTcRows;
-    const int nc = min(kTcRows, rows - r0) / c;
-    return lane < nc ? sel[static_cast<size_t>(pr) * k + r0 / c + lane] : 0;
+    const Tile t = tinfo(tile);
+    return lane < t.nrow / c ? chunk_at(t.e0 + lane, t.pair) : 0;
   };
-  // epilogue thread: position of its row
-  auto row_pos = [&](int tile) {
-    const int pr = tile / tpp, r0 = (tile - pr * tpp) * kTcRows;
-    const int R = r0 + row;
-    return R < rows ? sel[static_cast<size_t>(pr) * k + R / c] * c + (R % c) : 0;
+  // epilogue thread: position of its row, and (REC) the slot its chunk fills
+  struct RowInfo {
+    int pos, slot;
+  };
+  auto row_info = [&](int tile) -> RowInfo {
+    const Tile t = tinfo(tile);
+    if (row >= t.nrow) return {0, 0};
+    const int e = t.e0 + row / c;
+    const int slot = REC ? miss_slot[e] - t.pair * k : 0;
+    return {chunk_at(e, t.pair) * c + (row % c), slot};
   };
   tc::grid_dep_launch();
   if (tid == 0) {
     tc::prefetch_tensormap(&mapBt);
-    tc::prefetch_tensormap(&mapK);
+    if (!REC) tc::prefetch_tensormap(&mapK);
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&fullA[i], 1);
       tc::mbar_init(&emptyA[i], 1);
@@ -283,9 +330,41 @@ k_rebuild_pipe(const bf16* __restrict__ A, const __grid_constant__ CUtensorMap m
   };
   // the selection may still be finishing: its chunk ids are read after this
   tc::grid_dep_wait();
+  if constexpr (REC) {
+    if (warp == 0) {
+      // exclusive prefix of the heads' tile counts, 32 heads per round
+      int base = 0;
+      for (int p0 = 0; p0 < npairs; p0 += 32) {
+        const int p = p0 + lane;
+        const int mrows = p < npairs ? max(0, k - hits[p]) * c : 0;
+        const int nt = (mrows + kTcRows - 1) / kTcRows;
+        int incl = nt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        if (p < npairs) {
+          s_tp[p] = base + incl - nt;
+          s_rows[p] = mrows;
+          s_mb[p] = miss_base[p];
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) s_tp[npairs] = base;
+    }
+    __syncthreads();
+    total = s_tp[npairs];
+  }
+  lo = static_cast<int>(static_cast<long long>(blockIdx.x) * total / gridDim.x);
+  hi = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * total / gridDim.x);
   // both are loaded one tile ahead
   int first = 0;
-  if (hi > lo) first = warp == 0 ? chunk_ids(lo) : (warp >= 2 ? row_pos(lo) : 0);
+  RowInfo first_row{0, 0};
+  if (hi > lo) {
+    if (warp == 0) first = chunk_ids(lo);
+    else if (warp >= 2) first_row = row_info(lo);
+  }
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
@@ -293,8 +372,9 @@ k_rebuild_pipe(const bf16* __restrict__ A, const __grid_constant__ CUtensorMap m
     int prev = -1, nb = -1, lastA0 = -1, lastA1 = -1, lastB0 = -1, lastB1 = -1;
     int cid_next = first;
     for (int i = 0; i < hi - lo; ++i) {
-      const int tile = lo + i, pair = tile / tpp, ti = tile - pair * tpp;
-      const int bb = pair / h_kv;
+      const int tile = lo + i;
+      const Tile tl = tinfo(tile);
+      const int pair = tl.pair, bb = pair / h_kv;
       const int cid = cid_next;
       if (i + 1 < hi - lo) cid_next = chunk_ids(tile + 1);
       if (pair != prev) {
@@ -317,7 +397,7 @@ k_rebuild_pipe(const bf16* __restrict__ A, const __grid_constant__ CUtensorMap m
         prev = pair;
       }
       const int st = i % S, use = i / S;
-      const int row0 = ti * kTcRows, nrow = min(kTcRows, rows - row0), nch = nrow / c;
+      const int nch = tl.nrow / c;
       bool ok = true;
       if (lane == 0) ok = *s_abort == 0 && tc::mbar_wait(&emptyA[st], (use & 1) ^ 1, kWaitLimit);
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -353,7 +433,7 @@ k_rebuild_pipe(const bf16* __restrict__ A, const __grid_constant__ CUtensorMap m
       int prev = -1, nb = -1, bs = 0;
       int issued = 0;
       for (int i = 0; i < hi - lo; ++i) {
-        const int tile = lo + i, pair = tile / tpp;
+        const int tile = lo + i, pair = tinfo(tile).pair;
         if (pair != prev) {
           ++nb;
           bs = nb % NB;
@@ -382,7 +462,7 @@ k_rebuild_pipe(const bf16* __restrict__ A, const __grid_constant__ CUtensorMap m
         }
         tc::mma_commit(&emptyA[st]);
         tc::mma_commit(&tfull[acc]);
-        const bool last_of_pair = i == hi - lo - 1 || (tile + 1) / tpp != pair;
+        const bool last_of_pair = i == hi - lo - 1 || tinfo(tile + 1).pair != pair;
         if (last_of_pair) tc::mma_commit(&emptyB[bs]);
         ++issued;
       }
@@ -396,19 +476,21 @@ k_rebuild_pipe(const bf16* __restrict__ A, const __grid_constant__ CUtensorMap m
     const int ew = warp - 2, quarter = warp & 3, grp = ew >> 2;
     constexpr int Q = D / 8;                 // 16-byte chunks per output row
     constexpr int W = D / 8;                 // RoPE pairs per group
-    int pos_next = first;
+    RowInfo ri_next = first_row;
     for (int i = 0; i < hi - lo; ++i) {
-      const int tile = lo + i, pair = tile / tpp, ti = tile - pair * tpp;
-      const int row0 = ti * kTcRows, nrow = min(kTcRows, rows - row0);
+      const int tile = lo + i;
+      const Tile tl = tinfo(tile);
+      const int pair = tl.pair, row0 = tl.row0, nrow = tl.nrow;
       const int acc = i % kNAcc;
-      const int pos = pos_next;
-      if (i + 1 < hi - lo) pos_next = row_pos(tile + 1);
+      const RowInfo ri = ri_next;
+      const int pos = ri.pos;
+      if (i + 1 < hi - lo) ri_next = row_info(tile + 1);
       // the stores that last read this tile's staging buffer are done reading
-      if (tid == 64) {
+      if (!REC && tid == 64) {
         if (NS == 1) tc::bulk_wait_read_all();
         else tc::bulk_wait_read_1();
       }
-      unsigned char* stage = stage0 + (i % NS) * (kTcRows * D * 2);
+      unsigned char* stage = stage0 + (REC ? 0 : (i % NS) * (kTcRows * D * 2));
       bool ok = *s_abort == 0 && tc::mbar_wait(&tfull[acc], (i / kNAcc) & 1, kWaitLimit);
       ok = tc::named_sync_and(1, kEpiThreads, ok);
       if (!ok) {
@@ -445,27 +527,44 @@ k_rebuild_pipe(const bf16* __restrict__ A, const __grid_constant__ CUtensorMap m
         plo[j / 2] = *reinterpret_cast<const uint32_t*>(&a);
         phi[j / 2] = *reinterpret_cast<const uint32_t*>(&b2);
       }
-      // 16-byte unit qq of the row: column block qq/8, unit qq%8 XOR row%8
-      auto st16 = [&](int qq, uint4 v) {
-        const int off = (qq >> 3) * (kTcRows * 128) + row * 128 + (((qq & 7) ^ (row & 7)) << 4);
-        *reinterpret_cast<uint4*>(stage + off) = v;
-      };
+      if constexpr (REC) {
+        // the row's 16-byte pieces go straight to the K tile of its slot's
+        // group record: piece qq of row u at qq * 128 + u * 16 bytes
+        if (row < nrow) {
+          const int u = row % c;
+          uint4* recp = reinterpret_cast<uint4*>(
+              KV_slot + ((static_cast<size_t>(pair) * k + ri.slot) * (c / 8) + (u >> 3)) * 2048);
 #pragma unroll
-      for (int q4 = 0; q4 < W / 8; ++q4) {
-        const int qlo = grp * (W / 8) + q4;
-        st16(qlo, make_uint4(plo[4 * q4], plo[4 * q4 + 1], plo[4 * q4 + 2], plo[4 * q4 + 3]));
-        st16(Q / 2 + qlo, make_uint4(phi[4 * q4], phi[4 * q4 + 1], phi[4 * q4 + 2], phi[4 * q4 + 3]));
-      }
-      tc::fence_proxy_async_smem();
-      tc::named_sync(1, kEpiThreads);
-      if (tid == 64) {
-        for (int cb = 0; cb < D / 64; ++cb)
-          tc::tma_store_3d(&mapK, stage + cb * (kTcRows * 128), cb * 64, row0, pair);
-        tc::bulk_commit();
+          for (int q4 = 0; q4 < W / 8; ++q4) {
+            const int qlo = grp * (W / 8) + q4;
+            recp[qlo * 8 + (u & 7)] = make_uint4(plo[4 * q4], plo[4 * q4 + 1], plo[4 * q4 + 2], plo[4 * q4 + 3]);
+            recp[(Q / 2 + qlo) * 8 + (u & 7)] =
+                make_uint4(phi[4 * q4], phi[4 * q4 + 1], phi[4 * q4 + 2], phi[4 * q4 + 3]);
+          }
+        }
+      } else {
+        // 16-byte unit qq of the row: column block qq/8, unit qq%8 XOR row%8
+        auto st16 = [&](int qq, uint4 v) {
+          const int off = (qq >> 3) * (kTcRows * 128) + row * 128 + (((qq & 7) ^ (row & 7)) << 4);
+          *reinterpret_cast<uint4*>(stage + off) = v;
+        };
+#pragma unroll
+        for (int q4 = 0; q4 < W / 8; ++q4) {
+          const int qlo = grp * (W / 8) + q4;
+          st16(qlo, make_uint4(plo[4 * q4], plo[4 * q4 + 1], plo[4 * q4 + 2], plo[4 * q4 + 3]));
+          st16(Q / 2 + qlo, make_uint4(phi[4 * q4], phi[4 * q4 + 1], phi[4 * q4 + 2], phi[4 * q4 + 3]));
+        }
+        tc::fence_proxy_async_smem();
+        tc::named_sync(1, kEpiThreads);
+        if (tid == 64) {
+          for (int cb = 0; cb < D / 64; ++cb)
+            tc::tma_store_3d(&mapK, stage + cb * (kTcRows * 128), cb * 64, row0, pair);
+          tc::bulk_commit();
+        }
       }
     }
   }
-  if (tid == 64) tc::bulk_wait_all();
+  if (!REC && tid == 64) tc::bulk_wait_all();
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
@@ -526,25 +625,38 @@ cudaError_t make_rebuild_maps(Ctx& c) {
   if (!tc_rebuild_supported(c.p)) return cudaSuccess;
   const uint64_t pairs = static_cast<uint64_t>(c.p.b) * c.p.h_kv;
   cudaError_t e = encode_rows(&c.mapBt, c.Bt, pairs * c.p.d, c.p.r, c.p.d);
-  if (e == cudaSuccess) e = encode_ksparse(&c.mapK, c.K_sparse, c.p.d, c.p.k * c.p.c, pairs);
+  if (e == cudaSuccess && !c.kv_rec) e = encode_ksparse(&c.mapK, c.K_sparse, c.p.d, c.p.k * c.p.c, pairs);
   if (e == cudaSuccess) c.tc_rebuild = c.a_tiled = true;
   return e;
 }
 
-template <int D>
+template <int D, bool REC>
 static cudaError_t rebuild_tc(Ctx& c, cudaStream_t st) {
-  const PipeShape ps = pipe_shape(c.p.r, D);
+  const int npairs = c.p.b * c.p.h_kv;
+  PipeShape ps = pipe_shape(c.p.r, D);
+  if (REC) {
+    // no staging tiles; the head tile tables instead
+    ps = {0, 0, 0, 0};
+    const int tables = (3 * npairs + 1) * 4;
+    const int cand[4][2] = {{2, 2}, {2, 1}, {1, 2}, {1, 1}};
+    for (auto& x : cand) {
+      const int sm = pipe_smem(c.p.r, D, x[0], x[1], 0) + tables;
+      if (sm <= 227 * 1024) { ps = {x[0], x[1], 0, sm}; break; }
+    }
+  }
   if (ps.S == 0 || !c.a_tiled) return cudaErrorNotSupported;
-  auto kern = k_rebuild_pipe<D>;
+  auto kern = k_rebuild_pipe<D, REC>;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), ps.smem);
   if (e != cudaSuccess) return e;
-  const int tiles = (c.p.k * c.p.c + kTcRows - 1) / kTcRows * c.p.h_kv * c.p.b;
-  const int sms = c.nsm > 2 * kFetchSMs ? c.nsm - kFetchSMs : c.nsm;   // leave the fetch its SMs
+  const int tiles = (c.p.k * c.p.c + kTcRows - 1) / kTcRows * npairs;
+  const int sms = c.nsm > 2 * c.fetch_sms ? c.nsm - c.fetch_sms : c.nsm;   // leave the fetch its SMs
   const int grid = std::min(sms, tiles);
   return launch_pdl(kern, dim3(grid), dim3(kPipeThreads), ps.smem, st, static_cast<const bf16*>(c.A),
                     c.mapBt, c.mapK, static_cast<const int32_t*>(c.sel),
-                    static_cast<const float2*>(c.rope_tab), c.p.b * c.p.h_kv, c.p.h_kv, c.p.s, c.p.r,
-                    c.p.c, c.p.k, ps.S, ps.NB, ps.NS, c.status);
+                    static_cast<const float2*>(c.rope_tab), static_cast<const int32_t*>(c.miss_chunk),
+                    static_cast<const int32_t*>(c.miss_slot), static_cast<const int32_t*>(c.miss_base),
+                    static_cast<const int32_t*>(c.hits), static_cast<bf16*>(c.KV_slot), c.n, npairs, c.p.h_kv,
+                    c.p.s, c.p.r, c.p.c, c.p.k, ps.S, ps.NB, ps.NS, c.status);
 }
 
 template <typename T, int D>
@@ -556,15 +668,18 @@ static cudaError_t rebuild_simt(Ctx& c, cudaStream_t st) {
   dim3 grid((c.p.k * c.p.c + kRbRows - 1) / kRbRows, c.p.b * c.p.h_kv);
   kern<<<grid, kRbThreads, smem, st>>>(static_cast<const T*>(c.A), static_cast<const T*>(c.Bt),
                                         c.sel, c.rope_tab, static_cast<T*>(c.K_sparse), c.p.h_kv,
-                                        c.p.s, c.p.r, c.p.c, c.p.k, c.a_tiled ? 1 : 0);
+                                        c.p.s, c.p.r, c.p.c, c.p.k, c.a_tiled ? 1 : 0, c.sel_slot,
+                                        static_cast<T*>(c.KV_slot));
   return cudaGetLastError();
 }
 
 cudaError_t launch_rebuild(Ctx& c, cudaStream_t st) {
   kbegin(c, K_REBUILD, st);
   cudaError_t e;
-  if (c.tc_rebuild && !c.force_simt)
-    e = c.p.d == 128 ? rebuild_tc<128>(c, st) : rebuild_tc<64>(c, st);
+  if (c.tc_rebuild && !c.force_simt && c.kv_rec)
+    e = rebuild_tc<128, true>(c, st);
+  else if (c.tc_rebuild && !c.force_simt)
+    e = c.p.d == 128 ? rebuild_tc<128, false>(c, st) : rebuild_tc<64, false>(c, st);
   else if (c.p.dtype == SKV_DTYPE_BF16)
     e = c.p.d == 128 ? rebuild_simt<bf16, 128>(c, st) : rebuild_simt<bf16, 64>(c, st);
   else
