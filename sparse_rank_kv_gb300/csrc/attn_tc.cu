@@ -41,13 +41,12 @@ constexpr int kAtD = 128;                    // head dimension handled here
 constexpr int kAtStages = 3;
 constexpr int kAtThreads = 192;
 constexpr int kAtSoft = 128;                 // softmax / accumulation threads
-constexpr int kAtMaxSlots = 64;
 constexpr int kAtStage = kAtT / 8 * 4096;   // 16 group records (K tile | V^T tile)
 constexpr int kAtQBytes = 16 * kAtD * 2;     // q: 4 x [16 rows][64 B]
 constexpr int kAtPBytes = 16 * kAtT * 2;     // P^T: 16 x 128 bf16
 __host__ __device__ constexpr int at_smem_bytes() {
   return 1024 /* alignment slack */ + kAtStages * kAtStage + 2 * kAtQBytes + 2 * kAtPBytes +
-         4096 /* barriers, reductions, slot list */ + 2 * 8 * kAtMaxSlots * 4 /* combine scratch */;
+         1024 /* barriers, reductions */;
 }
 
 struct AtSeg {
@@ -88,11 +87,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 256);
   volatile int* s_abort = reinterpret_cast<volatile int*>(misc + 260);
   int* s_last = reinterpret_cast<int*>(misc + 264);
-  int* s_nslot = reinterpret_cast<int*>(misc + 268);
   float* red = reinterpret_cast<float*>(misc + 512);      // [2][4][8]
-  int* s_slots = reinterpret_cast<int*>(misc + 1024);     // [kAtMaxSlots]
-  float* mw = reinterpret_cast<float*>(misc + 4096);      // [8][kAtMaxSlots]
-  float* lw = mw + 8 * kAtMaxSlots;                       // [8][kAtMaxSlots]
 
   const int i_out = (n_out + kAtT - 1) / kAtT, i_sp = (n_sp + kAtT - 1) / kAtT,
             i_loc = (n_loc + kAtT - 1) / kAtT;
@@ -126,10 +121,9 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
     tc::tmem_alloc(tmem_slot, 64);
     tc::tmem_relinquish();
   }
-  // records past a partial item and the P rows past G are multiplied by
-  // zero weights: start them at zero so that they are finite
-  for (int i = tid; i < kAtStages * kAtStage / 16; i += kAtThreads)
-    reinterpret_cast<uint4*>(stages)[i] = make_uint4(0, 0, 0, 0);
+  // the P rows past G are multiplied by zero values of V: start them at
+  // zero so that they are finite (the producer does the same for the value
+  // record that pads a partial item to 16 tokens)
   for (int i = tid; i < 2 * kAtPBytes / 16; i += kAtThreads)
     reinterpret_cast<uint4*>(pbuf)[i] = make_uint4(0, 0, 0, 0);
   tc::fence_proxy_async_smem();
@@ -185,6 +179,15 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
       }
       unsigned char* sR = stages + st * kAtStage;
       const int groups = (sg.cnt + 7) >> 3;
+      if ((groups & 1) && groups < kAtT / 8) {
+        // P V runs over whole 16-token steps: the V^T half of the record
+        // after an odd count of groups meets zero weights and must be finite
+        uint4* pad = reinterpret_cast<uint4*>(sR + groups * 4096 + 2048);
+#pragma unroll
+        for (int i = 0; i < 2048 / 16 / 32; ++i) pad[i * 32 + lane] = make_uint4(0, 0, 0, 0);
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+      }
       if (lane == 0) {
         tc::mbar_expect_tx(&full[st], static_cast<uint32_t>(groups * 4096));
         if (sg.seg == 0)
@@ -253,6 +256,8 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
       };
       auto issue_o = [&](int it) {
         const int st = it % kAtStages, b = it & 1;
+        const int item = lo + it, pair = item / nsplit;
+        const int nks = (at_item(item - pair * nsplit, i_out, i_sp, n_out, n_sp, n_loc).cnt + 15) >> 4;
         tc::fence_after();
         const uint32_t a0 = tc::smem_u32(stages + st * kAtStage + 2048);
         const uint32_t b0 = tc::smem_u32(pbuf + b * kAtPBytes);
@@ -261,8 +266,9 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
         // groups 128 B apart, token groups 256 B apart.  16 tokens per MMA.
 #pragma unroll
         for (int ks = 0; ks < kAtT / 16; ++ks)
-          tc::mma_bf16(tmem + 32 + b * 16, tc::desc_k_none(a0 + ks * 8192, 4096, 128),
-                       tc::desc_k_none(b0 + ks * 512, 256, 128), idesc, ks != 0);
+          if (ks < nks)
+            tc::mma_bf16(tmem + 32 + b * 16, tc::desc_k_none(a0 + ks * 8192, 4096, 128),
+                         tc::desc_k_none(b0 + ks * 512, 256, 128), idesc, ks != 0);
         tc::mma_commit(&ofull[b]);
         tc::mma_commit(&empty[st]);
       };
@@ -349,46 +355,59 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
       tc::named_sync(1, kAtSoft);
       if (!*s_last) return;
       __threadfence();
+      // CTAs cta_of(x0) .. cta_of(x1 - 1) hold the head's items [x0, x1),
+      // each its partial in the slot of its first item of the head.  Every
+      // thread loads the (max, sum, value) of all heads for up to U CTAs at
+      // once (one round trip) and merges them online.
       const int x0 = pair * nsplit, x1 = x0 + nsplit;
-      if (ct == 0) {
-        const int nb = static_cast<int>(gridDim.x);
-        int b = static_cast<int>(static_cast<long long>(x0) * nb / total);
-        while (b + 1 < nb && lo_of(b + 1) <= x0) ++b;
-        while (b > 0 && lo_of(b) > x0) --b;
-        int n = 0;
-        for (; b < nb && n < kAtMaxSlots; ++b) {
-          const int l0 = lo_of(b);
-          if (l0 >= x1) break;
-          s_slots[n++] = max(l0, x0) - x0;
-        }
-        *s_nslot = n;
-      }
-      tc::named_sync(1, kAtSoft);
-      const int ns = *s_nslot;
+      const int nb = static_cast<int>(gridDim.x);
+      auto cta_of = [&](int x) {
+        return static_cast<int>((static_cast<long long>(x + 1) * nb - 1) / total);
+      };
+      const int b0 = cta_of(x0), b1 = cta_of(x1 - 1);
+      constexpr int U = G <= 4 ? 4 : 2;
       const size_t pb = static_cast<size_t>(pair) * G * max_splits;
-      for (int idx = ct; idx < G * ns; idx += kAtSoft) {
-        const int g = idx / ns, si = idx - g * ns;
-        const float* pp = part + (pb + static_cast<size_t>(g) * max_splits + s_slots[si]) * (kAtD + 2);
-        mw[g * kAtMaxSlots + si] = __ldcg(pp + kAtD);
-        lw[g * kAtMaxSlots + si] = __ldcg(pp + kAtD + 1);
-      }
-      tc::named_sync(1, kAtSoft);
-      if (ct < G) {
-        float M = -INFINITY, den = 0.f;
-        for (int si = 0; si < ns; ++si) M = fmaxf(M, mw[ct * kAtMaxSlots + si]);
-        for (int si = 0; si < ns; ++si) den = fmaf(exp2f(mw[ct * kAtMaxSlots + si] - M), lw[ct * kAtMaxSlots + si], den);
-        const float inv = 1.f / den;
-        for (int si = 0; si < ns; ++si) mw[ct * kAtMaxSlots + si] = exp2f(mw[ct * kAtMaxSlots + si] - M) * inv;
-      }
-      tc::named_sync(1, kAtSoft);
+      float M[G], den[G], num[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const float* pg = part + (pb + static_cast<size_t>(g) * max_splits) * (kAtD + 2) + row;
-        float num = 0.f;
-#pragma unroll 4
-        for (int si = 0; si < ns; ++si) num = fmaf(mw[g * kAtMaxSlots + si], __ldcg(pg + s_slots[si] * (kAtD + 2)), num);
-        out[(static_cast<size_t>(pair) * G + g) * kAtD + row] = __float2bfloat16_rn(num);
+        M[g] = -INFINITY;
+        den[g] = 0.f;
+        num[g] = 0.f;
       }
+      for (int bb = b0; bb <= b1; bb += U) {
+        float mv[U][G], lv[U][G], pv[U][G];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int slot = bb + u <= b1 ? max(lo_of(bb + u), x0) - x0 : -1;
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            if (slot >= 0) {
+              const float* pp = part + (pb + static_cast<size_t>(g) * max_splits + slot) * (kAtD + 2);
+              mv[u][g] = __ldcg(pp + kAtD);
+              lv[u][g] = __ldcg(pp + kAtD + 1);
+              pv[u][g] = __ldcg(pp + row);
+            } else {
+              mv[u][g] = -INFINITY;
+              lv[u][g] = 0.f;
+              pv[u][g] = 0.f;
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            if (mv[u][g] == -INFINITY) continue;
+            const float mn = fmaxf(M[g], mv[u][g]);
+            const float so = M[g] == -INFINITY ? 0.f : exp2f(M[g] - mn), ss = exp2f(mv[u][g] - mn);
+            den[g] = den[g] * so + lv[u][g] * ss;
+            num[g] = num[g] * so + pv[u][g] * ss;
+            M[g] = mn;
+          }
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+        out[(static_cast<size_t>(pair) * G + g) * kAtD + row] = __float2bfloat16_rn(num[g] / den[g]);
       if (ct == 0) ticket[pair] = 0;
       tc::named_sync(1, kAtSoft);
     };
@@ -501,7 +520,7 @@ static cudaError_t attn_tc_t(Ctx& c, const CUtensorMap& mq, void* out, int n_loc
   if (e != cudaSuccess) return e;
   const int npairs = c.p.b * c.p.h_kv;
   const int items = npairs * attn_tc_splits(c, n_loc);
-  const int grid = std::min(std::min(c.nsm, items), npairs * (kAtMaxSlots - 2));
+  const int grid = std::min(c.nsm, items);
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kAtD));
   return launch_pdl(kern, dim3(grid), dim3(kAtThreads), smem, st, mq, static_cast<const bf16*>(c.KV_out),
                     static_cast<const bf16*>(c.KV_slot), static_cast<const int32_t*>(c.sel_slot),
