@@ -73,13 +73,13 @@ size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 // Byte sizes of every device buffer of a context, in allocation order.
 struct Sizes {
   size_t A, Bt, L, K_out, V_out, K_loc, V_loc, slot_V, K_sparse, KV_out, KV_loc, KV_slot;
-  size_t min_cos, logits, score_part, attn_part, basis, rope_tab, q_buf;
+  size_t min_cos, logits, score_part, attn_part, basis, rope_tab;
   size_t out_ids, out_mask, sel, sel_slot, slot_chunk, miss_chunk, miss_slot;
   size_t miss_count, miss_base, hits, attn_count, counters, status;
   size_t total() const {
     const size_t v[] = {A, Bt, L, K_out, V_out, K_loc, V_loc, slot_V, K_sparse, KV_out, KV_loc, KV_slot,
                         min_cos, logits,
-                        score_part, attn_part, basis, rope_tab, q_buf, out_ids, out_mask, sel, sel_slot,
+                        score_part, attn_part, basis, rope_tab, out_ids, out_mask, sel, sel_slot,
                         slot_chunk, miss_chunk, miss_slot, miss_count, miss_base, hits, attn_count, counters,
                         status};
     size_t t = 0;
@@ -122,7 +122,6 @@ Sizes sizes_of(const shadowkv_params& p) {
   z.attn_part = b * hq * static_cast<size_t>(max_splits_of(p)) * (d + 2) * 4;
   z.basis = b * r * h * d * 4;
   z.rope_tab = d / 2 * 8;
-  z.q_buf = b * hq * d * E;
   z.out_ids = b * h * o * 4;
   z.out_mask = b * h * nw * 4;
   z.sel = z.sel_slot = z.slot_chunk = z.miss_chunk = z.miss_slot = b * h * k * 4;
@@ -241,7 +240,6 @@ skv_status create(const shadowkv_params* p, cudaStream_t st, shadowkv_ctx** out)
   c.attn_part = static_cast<float*>(take(z.attn_part));
   c.basis = static_cast<float*>(take(z.basis));
   c.rope_tab = static_cast<float2*>(take(z.rope_tab));
-  c.q_buf = take(z.q_buf);
   c.out_ids = static_cast<int32_t*>(take(z.out_ids));
   c.out_mask = static_cast<uint32_t*>(take(z.out_mask));
   c.sel = static_cast<int32_t*>(take(z.sel));
@@ -287,10 +285,6 @@ skv_status create(const shadowkv_params* p, cudaStream_t st, shadowkv_ctx** out)
   e = skv::make_rebuild_maps(c);
   if (e == cudaSuccess) e = skv::make_score_map(c);
   if (e == cudaSuccess) e = skv::make_attn_maps(c);
-  if (e == cudaSuccess && (c.tc_score || c.kv_rec)) {
-    e = skv::encode_q_map(c, c.q_buf, &c.mapQ);
-    c.q_map = e == cudaSuccess;
-  }
   if (e != cudaSuccess) return bail(cuda_fail(e, "encode TMA descriptors"));
 
   e = cudaStreamCreateWithFlags(&c.side, cudaStreamNonBlocking);
@@ -484,18 +478,19 @@ skv_status shadowkv_decode_step(shadowkv_ctx* h, const void* q, const void* k_ne
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int loc_row = c.p.w + c.n_app;
   const int n_loc = loc_row + (k_new ? 1 : 0);
-  // the queries move into the context's buffer, whose tensor map is fixed
-  CK(cudaMemcpyAsync(c.q_buf, q, static_cast<size_t>(c.p.b) * c.p.h_q * c.p.d * c.E,
-                     cudaMemcpyDeviceToDevice, st));
-  q = c.q_buf;
   CK(skv::launch_score(c, q, st));
   CK(skv::launch_select(c, k_new, v_new, loc_row, st));
-  CK(cudaEventRecord(c.ev_fork, st));
-  CK(cudaStreamWaitEvent(c.side, c.ev_fork, 0));
-  CK(skv::launch_fetch(c, c.side));
-  CK(cudaEventRecord(c.ev_join, c.side));
+  // the value fetch overlaps the key rebuild: CTAs of the rebuild's own
+  // launch, or a kernel on the side stream
+  const bool fused = skv::rebuild_fetches(c);
+  if (!fused) {
+    CK(cudaEventRecord(c.ev_fork, st));
+    CK(cudaStreamWaitEvent(c.side, c.ev_fork, 0));
+    CK(skv::launch_fetch(c, c.side));
+    CK(cudaEventRecord(c.ev_join, c.side));
+  }
   CK(skv::launch_rebuild(c, st));
-  CK(cudaStreamWaitEvent(st, c.ev_join, 0));
+  if (!fused) CK(cudaStreamWaitEvent(st, c.ev_join, 0));
   CK(skv::launch_attn(c, q, out, n_loc, st));
   if (k_new) ++c.n_app;
   ++c.t;

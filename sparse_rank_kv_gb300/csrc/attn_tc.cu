@@ -522,7 +522,9 @@ static cudaError_t attn_tc_t(Ctx& c, const CUtensorMap& mq, void* out, int n_loc
   const int items = npairs * attn_tc_splits(c, n_loc);
   const int grid = std::min(c.nsm, items);
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kAtD));
-  return launch_pdl(kern, dim3(grid), dim3(kAtThreads), smem, st, mq, static_cast<const bf16*>(c.KV_out),
+  // after a launch that also fetches values over the host link the
+  // attention's CTAs are not made resident early: they slow the fetch
+  return launch_ex(!rebuild_fetches(c), kern, dim3(grid), dim3(kAtThreads), smem, st, mq, static_cast<const bf16*>(c.KV_out),
                     static_cast<const bf16*>(c.KV_slot), static_cast<const int32_t*>(c.sel_slot),
                     static_cast<const bf16*>(c.KV_loc),
                     static_cast<bf16*>(out), c.attn_part, c.attn_count, c.p.o * c.p.c, c.p.k * c.p.c,
@@ -532,10 +534,8 @@ static cudaError_t attn_tc_t(Ctx& c, const CUtensorMap& mq, void* out, int n_loc
 cudaError_t launch_attn_tc(Ctx& c, const void* q, void* out, int n_loc, cudaStream_t st) {
   if (attn_tc_splits(c, n_loc) > c.max_splits) return cudaErrorInvalidValue;
   CUtensorMap mq;
-  if (q == c.q_buf && c.q_map) {
-    mq = c.mapQ;
-  } else {
-    const cudaError_t e = encode_q_map(c, q, &mq);
+  {
+    const cudaError_t e = q_map_for(c, q, &mq);
     if (e != cudaSuccess) return e;
   }
   switch (c.G) {

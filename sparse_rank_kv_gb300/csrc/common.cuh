@@ -574,4 +574,56 @@ __device__ __forceinline__ void block_topk(const uint32_t* keys, int n, int k, i
   __syncthreads();
 }
 
+// The step's value misses, for bf16 records with d = 128: thread h of nh
+// (a half-warp per 8-token group of a missed chunk) reads the group's values
+// from the mapped pinned host copy of V and writes the V^T half of the
+// chunk's cache-slot record (one 128-byte run per lane).  The miss list
+// holds (pair * n + chunk, pair * k + slot) per missed chunk.
+__device__ __forceinline__ void fetch_value_groups(const __nv_bfloat16* __restrict__ vcpu,
+                                                   __nv_bfloat16* __restrict__ KV_slot,
+                                                   const int32_t* __restrict__ miss_chunk,
+                                                   const int32_t* __restrict__ miss_slot, int total,
+                                                   int s, int n, int c, int k, int npairs, long long h,
+                                                   long long nh, int* __restrict__ status) {
+  const int q = threadIdx.x & 15;
+  if (total > npairs * k) {
+    if (h == 0) flag_error(status, DEV_BAD_COUNT);
+    total = npairs * k;
+  }
+  const int gpc = c >> 3;   // groups per chunk
+  const long long groups = static_cast<long long>(total) * gpc, step = nh >> 4;
+  // two groups per round, both read before either is written, so that a
+  // half-warp with two groups waits for the host link once
+  for (long long g0 = h >> 4; g0 < groups; g0 += 2 * step) {
+    uint4 in[2][8];
+    uint4* dst[2] = {nullptr, nullptr};
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const long long gi = g0 + u * step;
+      if (gi >= groups) break;
+      const int m = static_cast<int>(gi / gpc), gs = static_cast<int>(gi - static_cast<long long>(m) * gpc);
+      const int pc = miss_chunk[m], ps = miss_slot[m];
+      const int pair = pc / n, chunk = pc - pair * n;
+      const int slot = ps - pair * k;
+      if (pair < 0 || pair >= npairs || chunk < 0 || slot < 0 || slot >= k) {
+        if (q == 0) flag_error(status, DEV_BAD_SLOT);
+        continue;
+      }
+      const uint4* src = reinterpret_cast<const uint4*>(
+          vcpu + (static_cast<size_t>(pair) * s + static_cast<size_t>(chunk) * c + gs * 8) * 128);
+      dst[u] = reinterpret_cast<uint4*>(KV_slot + ((static_cast<size_t>(pair) * k + slot) * c + gs * 8) * 256 + 1024);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) in[u][t] = src[t * 16 + q];
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (dst[u] == nullptr) continue;
+      uint4 outv[8];
+      transpose8x8(in[u], outv);
+#pragma unroll
+      for (int r = 0; r < 8; ++r) dst[u][q * 8 + r] = outv[r];
+    }
+  }
+}
+
 }  // namespace skv

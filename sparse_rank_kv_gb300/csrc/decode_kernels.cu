@@ -305,34 +305,9 @@ __global__ void __launch_bounds__(kFetchWarps * 32)
 k_fetch_rec(const bf16* __restrict__ vcpu, bf16* __restrict__ KV_slot, const int32_t* __restrict__ miss_chunk,
               const int32_t* __restrict__ miss_slot, const int32_t* __restrict__ miss_total, int par, int s,
               int n, int c, int k, int npairs, int* __restrict__ status) {
-  const int lane = threadIdx.x & 31, q = lane & 15;
-  const int h0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 4;
-  const int nh = (gridDim.x * blockDim.x) >> 4;
-  int total = miss_total[par];
-  if (total > npairs * k) {
-    if (h0 == 0 && lane == 0) flag_error(status, DEV_BAD_COUNT);
-    total = npairs * k;
-  }
-  const int gpc = c >> 3;   // groups per chunk
-  for (int gi = h0; gi < total * gpc; gi += nh) {
-    const int m = gi / gpc, gs = gi - m * gpc;
-    const int pc = miss_chunk[m], ps = miss_slot[m];
-    const int pair = pc / n, chunk = pc - pair * n;
-    const int slot = ps - pair * k;
-    if (pair < 0 || pair >= npairs || chunk < 0 || slot < 0 || slot >= k) {
-      if (q == 0) flag_error(status, DEV_BAD_SLOT);
-      continue;
-    }
-    const uint4* src = reinterpret_cast<const uint4*>(
-        vcpu + (static_cast<size_t>(pair) * s + static_cast<size_t>(chunk) * c + gs * 8) * 128);
-    uint4* dst = reinterpret_cast<uint4*>(KV_slot + ((static_cast<size_t>(pair) * k + slot) * c + gs * 8) * 256 + 1024);
-    uint4 in[8], outv[8];
-#pragma unroll
-    for (int t = 0; t < 8; ++t) in[t] = src[t * 16 + q];
-    transpose8x8(in, outv);
-#pragma unroll
-    for (int r = 0; r < 8; ++r) dst[q * 8 + r] = outv[r];
-  }
+  fetch_value_groups(vcpu, KV_slot, miss_chunk, miss_slot, miss_total[par], s, n, c, k, npairs,
+                     static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x,
+                     static_cast<long long>(gridDim.x) * blockDim.x, status);
 }
 
 // Records of row-major [rows][128] bf16 keys and values (rows a multiple of

@@ -35,12 +35,13 @@ struct Timed {
   cudaEvent_t a, b;
 };
 
-// SMs reserved for the host-memory value fetch, which runs on a side stream
-// next to the key rebuild; the rebuild's grid leaves them free.  When only
-// the missed chunks are rebuilt (records) the rebuild is small and the fetch
-// gets more SMs.
+// SMs reserved for the host-memory value fetch, which runs next to the key
+// rebuild: on a side stream, the rebuild's grid leaving it these SMs, or
+// (records) as the first CTAs of the rebuild's own launch.  When only the
+// missed chunks are rebuilt (records) the rebuild is small and the fetch gets
+// more SMs.
 constexpr int kFetchSMs = 16;
-constexpr int kFetchSMsRec = 48;
+constexpr int kFetchSMsRec = 64;
 
 struct Ctx {
   shadowkv_params p{};
@@ -90,9 +91,9 @@ struct Ctx {
   int fetch_sms = kFetchSMs;
   void *KV_out = nullptr, *KV_loc = nullptr, *KV_slot = nullptr;
   int32_t* miss_base = nullptr;   // per (batch, KV head): start of its misses in the step's list
-  // the step's queries, copied from the caller's buffer so that their
-  // tensor map (mapQ, 16-row boxes) is encoded once
-  void* q_buf = nullptr;
+  // tensor map of the caller's query buffer (16-row boxes), encoded again
+  // only when the buffer's address changes
+  const void* q_enc = nullptr;
   CUtensorMap mapQ{};
   bool q_map = false;
   CUtensorMap mapL{};           // landmarks (b*h_kv*n x d) for the tensor-core score kernel
@@ -141,9 +142,11 @@ cudaError_t launch_attn(Ctx& c, const void* q, void* out, int n_loc, cudaStream_
 // Launches kern with programmatic stream serialization: it may begin while
 // the previous kernel of the stream finishes (it calls grid_dep_wait before
 // reading that kernel's results).
+// With pdl false it is a plain launch (the kernel's grid_dep_wait returns
+// at once).
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                       Args&&... args) {
+cudaError_t launch_ex(bool pdl, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                      Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -153,8 +156,13 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  return launch_ex(true, kern, grid, block, smem, st, std::forward<Args>(args)...);
 }
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per device, kernel and size
 cudaError_t set_smem_once(const void* func, int bytes);
@@ -164,6 +172,9 @@ cudaError_t launch_attn_pipe(Ctx& c, const void* q, void* out, int n_loc, cudaSt
 cudaError_t launch_build_mask(Ctx& c, cudaStream_t st);
 // rebuild.cu
 cudaError_t launch_rebuild(Ctx& c, cudaStream_t st);
+// true when launch_rebuild also moves the step's value misses (records with
+// the tensor-core rebuild): no separate fetch launch then
+bool rebuild_fetches(const Ctx& c);
 bool tc_rebuild_supported(const shadowkv_params& p);
 cudaError_t make_rebuild_maps(Ctx& c);   // encodes mapBt
 cudaError_t launch_tile_a(Ctx& c, int to_tiled, cudaStream_t st);   // no-op unless a_tiled
@@ -171,6 +182,8 @@ cudaError_t launch_pack_kv(Ctx& c, cudaStream_t st);                // records o
 bool attn_tc_supported(const shadowkv_params& p);
 cudaError_t launch_attn_tc(Ctx& c, const void* q, void* out, int n_loc, cudaStream_t st);
 cudaError_t encode_q_map(const Ctx& c, const void* q, CUtensorMap* map);
+// the query map for buffer q: the context's cached one, encoded when q differs
+cudaError_t q_map_for(Ctx& c, const void* q, CUtensorMap* map);
 // prefill_kernels.cu
 // Runs Algorithm 1 on the device.  v is a device pointer, or (v_mapped) the
 // mapped device address of pinned host memory.

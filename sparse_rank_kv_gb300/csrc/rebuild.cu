@@ -229,8 +229,22 @@ k_rebuild_pipe(const bf16* __restrict__ A, const __grid_constant__ CUtensorMap m
                const int32_t* __restrict__ miss_chunk, const int32_t* __restrict__ miss_slot,
                const int32_t* __restrict__ miss_base, const int32_t* __restrict__ hits,
                bf16* __restrict__ KV_slot, int n, int npairs, int h_kv, int s, int r, int c, int k,
-               int S, int NB, int NS, int* __restrict__ status) {
+               int S, int NB, int NS, const bf16* __restrict__ vcpu, const int32_t* __restrict__ miss_total,
+               int par, int nfetch, int* __restrict__ status) {
   extern __shared__ unsigned char smem_raw[];
+  if constexpr (REC) {
+    // the first nfetch CTAs move the step's value misses over the host link
+    // while the others rebuild the missed chunks' keys
+    if (static_cast<int>(blockIdx.x) < nfetch) {
+      tc::grid_dep_launch();
+      tc::grid_dep_wait();
+      fetch_value_groups(vcpu, KV_slot, miss_chunk, miss_slot, miss_total[par], s, n, c, k, npairs,
+                         static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x,
+                         static_cast<long long>(nfetch) * blockDim.x, status);
+      return;
+    }
+  }
+  const int cta = static_cast<int>(blockIdx.x) - nfetch, ncta = static_cast<int>(gridDim.x) - nfetch;
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int KB = (r + 31) / 32;
@@ -356,8 +370,8 @@ k_rebuild_pipe(const bf16* __restrict__ A, const __grid_constant__ CUtensorMap m
     __syncthreads();
     total = s_tp[npairs];
   }
-  lo = static_cast<int>(static_cast<long long>(blockIdx.x) * total / gridDim.x);
-  hi = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * total / gridDim.x);
+  lo = static_cast<int>(static_cast<long long>(cta) * total / ncta);
+  hi = static_cast<int>(static_cast<long long>(cta + 1) * total / ncta);
   // both are loaded one tile ahead
   int first = 0;
   RowInfo first_row{0, 0};
@@ -649,15 +663,22 @@ static cudaError_t rebuild_tc(Ctx& c, cudaStream_t st) {
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), ps.smem);
   if (e != cudaSuccess) return e;
   const int tiles = (c.p.k * c.p.c + kTcRows - 1) / kTcRows * npairs;
-  const int sms = c.nsm > 2 * c.fetch_sms ? c.nsm - c.fetch_sms : c.nsm;   // leave the fetch its SMs
-  const int grid = std::min(sms, tiles);
+  // records: the value fetch runs in the same launch, on its own CTAs;
+  // otherwise it runs on a side stream and the rebuild leaves it its SMs
+  const int nfetch = REC ? std::min(c.fetch_sms, c.nsm / 2) : 0;
+  const int sms = REC ? c.nsm - nfetch : c.nsm > 2 * c.fetch_sms ? c.nsm - c.fetch_sms : c.nsm;
+  const int grid = nfetch + std::min(sms, tiles);
   return launch_pdl(kern, dim3(grid), dim3(kPipeThreads), ps.smem, st, static_cast<const bf16*>(c.A),
                     c.mapBt, c.mapK, static_cast<const int32_t*>(c.sel),
                     static_cast<const float2*>(c.rope_tab), static_cast<const int32_t*>(c.miss_chunk),
                     static_cast<const int32_t*>(c.miss_slot), static_cast<const int32_t*>(c.miss_base),
                     static_cast<const int32_t*>(c.hits), static_cast<bf16*>(c.KV_slot), c.n, npairs, c.p.h_kv,
-                    c.p.s, c.p.r, c.p.c, c.p.k, ps.S, ps.NB, ps.NS, c.status);
+                    c.p.s, c.p.r, c.p.c, c.p.k, ps.S, ps.NB, ps.NS,
+                    static_cast<const bf16*>(REC ? c.v_cpu_dev : nullptr),
+                    static_cast<const int32_t*>(c.miss_count), static_cast<int>(c.t & 1), nfetch, c.status);
 }
+
+bool rebuild_fetches(const Ctx& c) { return c.tc_rebuild && !c.force_simt && c.kv_rec && c.a_tiled; }
 
 template <typename T, int D>
 static cudaError_t rebuild_simt(Ctx& c, cudaStream_t st) {

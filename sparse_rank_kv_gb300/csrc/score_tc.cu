@@ -84,6 +84,9 @@ k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUt
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the queries may come from the stream's previous kernel, and the previous
+  // step may still be reading the logits
+  tc::grid_dep_wait();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -217,9 +220,8 @@ cudaError_t make_score_map(Ctx& c) {
   return cudaSuccess;
 }
 
-// The queries live in the caller's buffer, so their descriptor is encoded for
-// every step: a 3D view {d, G, b*h_kv} read in boxes of 32 x 16 x 1, the rows
-// past G being zero-filled.
+// The queries live in the caller's buffer: a 3D view {d, G, b*h_kv} read in
+// boxes of 32 x 16 x 1, the rows past G being zero-filled.
 cudaError_t encode_q_map(const Ctx& c, const void* q, CUtensorMap* map) {
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
@@ -236,6 +238,18 @@ cudaError_t encode_q_map(const Ctx& c, const void* q, CUtensorMap* map) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t q_map_for(Ctx& c, const void* q, CUtensorMap* map) {
+  if (!c.q_map || q != c.q_enc) {
+    c.q_map = false;
+    const cudaError_t e = encode_q_map(c, q, &c.mapQ);
+    if (e != cudaSuccess) return e;
+    c.q_enc = q;
+    c.q_map = true;
+  }
+  *map = c.mapQ;
+  return cudaSuccess;
+}
+
 template <int D, int G>
 static cudaError_t score_tc_t(Ctx& c, const CUtensorMap& mq, cudaStream_t st) {
   const int smem = sc_smem_bytes(D);
@@ -244,9 +258,10 @@ static cudaError_t score_tc_t(Ctx& c, const CUtensorMap& mq, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const int total = c.p.b * c.p.h_kv * c.ntile;
   const int grid = total < c.nsm ? total : c.nsm;
-  kern<<<grid, kScThreads, smem, st>>>(c.mapL, mq, c.out_mask, c.logits, c.score_part, c.n, c.ntile,
-                                        total, 1.0f / sqrtf(static_cast<float>(D)), c.status);
-  return cudaGetLastError();
+  // the prologue overlaps the tail of the stream's previous kernel
+  return launch_pdl(kern, dim3(grid), dim3(kScThreads), static_cast<size_t>(smem), st, c.mapL, mq,
+                    static_cast<const uint32_t*>(c.out_mask), c.logits, c.score_part, c.n, c.ntile, total,
+                    1.0f / sqrtf(static_cast<float>(D)), c.status);
 }
 
 template <int D>
@@ -264,8 +279,7 @@ static cudaError_t score_tc_d(Ctx& c, const CUtensorMap& mq, cudaStream_t st) {
 cudaError_t launch_score_tc(Ctx& c, const void* q, cudaStream_t st) {
   if (!c.tc_score || c.force_simt) return cudaErrorNotSupported;
   CUtensorMap mq;
-  if (q == c.q_buf && c.q_map) mq = c.mapQ;
-  else if (encode_q_map(c, q, &mq) != cudaSuccess) return cudaErrorNotSupported;
+  if (q_map_for(c, q, &mq) != cudaSuccess) return cudaErrorNotSupported;
   return c.p.d == 128 ? score_tc_d<128>(c, mq, st) : score_tc_d<64>(c, mq, st);
 }
 
