@@ -173,10 +173,11 @@ constexpr int kTopkCand = 4096;   // boundary-bin candidates kept after the firs
 
 // Shared memory (ints) block_topk needs besides the keys.
 __host__ __device__ constexpr int topk_scratch_ints(int nthreads) {
-  // max of the radix path's needs and (values + block_kth scratch + scans)
-  return (nthreads / 32) * 256 + 256 + 64 + kTopkCand > 4 * nthreads + (nthreads / 32) * 256 + 256 + 48
+  // max of the radix path's needs and (values + their indices + block_kth
+  // scratch + scans)
+  return (nthreads / 32) * 256 + 256 + 64 + kTopkCand > 8 * nthreads + (nthreads / 32) * 256 + 256 + 48
              ? (nthreads / 32) * 256 + 256 + 64 + kTopkCand
-             : 4 * nthreads + (nthreads / 32) * 256 + 256 + 48;
+             : 8 * nthreads + (nthreads / 32) * 256 + 256 + 48;
 }
 
 // Radix version of block_topk below (same contract, no bitmap): radix select
@@ -434,6 +435,109 @@ __device__ __forceinline__ void block_kth(const uint32_t* v, int cnt, int kth, i
   *need_out = need;
 }
 
+// block_kth for at most 1024 values, computed by the block's first 256
+// threads alone (eight warps meeting at named barrier 1, four values per
+// thread): far fewer threads wait at each of the passes' barriers.  The
+// k-th largest lands in scratch[kKth8T] and the count of its equals within
+// the top kth in scratch[kKth8Need]; the caller synchronises the block before
+// reading them.  scratch holds kKth8Ints ints.
+constexpr int kKth8T = 8 * 256 + 256 + 4, kKth8Need = kKth8T + 1, kKth8Ints = 8 * 256 + 256 + 8;
+__device__ __forceinline__ void block_kth_256(const uint32_t* v, int cnt, int kth, int* scratch) {
+  const int tid = threadIdx.x;
+  if (tid >= 256) return;
+  const int lane = tid & 31, warp = tid >> 5;
+  int* whist = scratch;             // [8][256]
+  int* hist = scratch + 8 * 256;    // [256]
+  int* bc = hist + 256;             // broadcast slots
+  auto bar = []() { asm volatile("bar.sync 1, 256;" ::: "memory"); };
+  uint32_t x[4];
+  uint32_t lo = 0xffffffffu, hi = 0u;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int i = tid + q * 256;
+    x[q] = i < cnt ? v[i] : 0u;
+    if (x[q]) { lo = min(lo, x[q]); hi = max(hi, x[q]); }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  if (lane == 0) { whist[warp] = static_cast<int>(lo); whist[32 + warp] = static_cast<int>(hi); }
+  bar();
+  if (tid < 32) {
+    uint32_t m = tid < 8 ? static_cast<uint32_t>(whist[tid]) : 0xffffffffu;
+    uint32_t M = tid < 8 ? static_cast<uint32_t>(whist[32 + tid]) : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      m = min(m, __shfl_xor_sync(0xffffffffu, m, o));
+      M = max(M, __shfl_xor_sync(0xffffffffu, M, o));
+    }
+    if (tid == 0) { bc[2] = static_cast<int>(m); bc[3] = static_cast<int>(M); }
+  }
+  bar();
+  const uint32_t vmin = static_cast<uint32_t>(bc[2]);
+  const uint32_t span = static_cast<uint32_t>(bc[3]) - vmin;
+  int hb = span ? 32 - __clz(span) : 1;
+  uint32_t prefix = 0, pmask = 0;
+  int need = kth;
+  while (hb > 0) {
+    const int width = hb < 8 ? hb : 8;
+    const int shift = hb - width;
+    const uint32_t dmask = (1u << width) - 1u;
+    int* wh = whist + warp * 256;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) wh[i * 32 + lane] = 0;
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t r = x[q] - vmin;
+      if (x[q] && (r & pmask) == prefix) atomicAdd(&wh[(r >> shift) & dmask], 1);
+    }
+    bar();
+    {
+      int acc = 0;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) acc += whist[w * 256 + tid];
+      hist[tid] = acc;
+    }
+    bar();
+    if (tid < 32) {
+      int cnt8[8], sum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) { cnt8[i] = hist[255 - 8 * lane - i]; sum += cnt8[i]; }
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned hit = __ballot_sync(0xffffffffu, incl >= need);
+      const int first = __ffs(hit) - 1;
+      if (lane == first) {
+        int acc = incl - sum, digit = 255 - 8 * lane;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (acc + cnt8[i] >= need) { digit = 255 - 8 * lane - i; break; }
+          acc += cnt8[i];
+        }
+        bc[0] = digit;
+        bc[1] = need - acc;
+      }
+    }
+    bar();
+    // bc[0..1] are rewritten only after two more barriers of the next pass
+    prefix |= static_cast<uint32_t>(bc[0]) << shift;
+    pmask |= dmask << shift;
+    need = bc[1];
+    hb = shift;
+  }
+  if (tid == 0) {
+    bc[4] = static_cast<int>(vmin + prefix);
+    bc[5] = need;
+  }
+}
+
 // Block-wide selection of the k largest keys among keys[0..n) (shared
 // memory), ties broken toward the lower index; key 0 marks an excluded entry
 // and is never chosen when at least k keys are non-zero.  On return out[0..k)
@@ -458,9 +562,11 @@ __device__ __forceinline__ void block_topk(const uint32_t* keys, int n, int k, i
   const int nw = (n + 31) >> 5;
   const int cap = 4 * nthr;
   uint32_t* vals = reinterpret_cast<uint32_t*>(scratch);   // cap values
-  int* ks = scratch + cap;                                  // block_kth scratch
+  int* vidx = scratch + cap;                                // their indices
+  int* ks = vidx + cap;                                     // block_kth scratch
   int* tmp = ks + (nthr / 32) * 256 + 256 + 8;              // 40 ints for the scans
   int* cnt_slot = tmp + 36;                                 // survivor counter
+  int* eq_slot = tmp + 37;                                  // survivors equal to T
   // each warp owns a contiguous range of 32-key rows; lanes read consecutive
   // keys, so shared-memory reads are conflict-free
   const int rows = (n + 31) >> 5;
@@ -469,7 +575,10 @@ __device__ __forceinline__ void block_topk(const uint32_t* keys, int n, int k, i
   uint32_t T = 0;
   int need = 0;
   bool ok = true;
-  if (tid == 0) *cnt_slot = 0;
+  if (tid == 0) {
+    *cnt_slot = 0;
+    *eq_slot = 0;
+  }
   __syncthreads();
   uint32_t T0 = 1u;                  // keys >= T0 are gathered (all non-zero keys when n <= cap)
   if (n > cap) {
@@ -489,9 +598,9 @@ __device__ __forceinline__ void block_topk(const uint32_t* keys, int n, int k, i
     int r = static_cast<int>((3LL * k * S + 2LL * n - 1) / (2LL * n)) + 12;
     if (r > tot - 1) r = tot - 1;
     T0 = 0xffffffffu;                // no non-zero sample: no survivor, radix decides
-    int dummy;
-    if (tot > 0) block_kth(vals, tot, r + 1, ks, &T0, &dummy);
+    if (tot > 0) block_kth_256(vals, tot, r + 1, ks);
     __syncthreads();
+    if (tot > 0) T0 = static_cast<uint32_t>(ks[kKth8T]);
     if (tid == 0) *cnt_slot = 0;
     __syncthreads();
   }
@@ -505,15 +614,38 @@ __device__ __forceinline__ void block_topk(const uint32_t* keys, int n, int k, i
     if (lane == 0 && m) base = atomicAdd(cnt_slot, __popc(m));
     base = __shfl_sync(0xffffffffu, base, 0);
     const int pos = base + __popc(m & ((1u << lane) - 1u));
-    if (keep && pos < cap) vals[pos] = key;
+    if (keep && pos < cap) {
+      vals[pos] = key;
+      vidx[pos] = j;
+    }
   }
   __syncthreads();
   const int nsurv = *cnt_slot;
   ok = nsurv >= k && nsurv <= cap;
-  if (ok) block_kth(vals, nsurv, k, ks, &T, &need);
   for (int w = tid; w < nw; w += nthr) bits[w] = 0u;
-  __syncthreads();
+  if (ok && nsurv <= 1024) {
+    block_kth_256(vals, nsurv, k, ks);
+    __syncthreads();
+    T = static_cast<uint32_t>(ks[kKth8T]);
+    need = ks[kKth8Need];
+  } else if (ok) {
+    block_kth(vals, nsurv, k, ks, &T, &need);
+  }
+  // survivors equal to T: when the top k takes all of them (the usual case)
+  // the bitmap follows from the survivors alone
+  int eq_total = 0;
   if (ok) {
+    int eq = 0;
+    for (int i = tid; i < nsurv; i += nthr) eq += vals[i] == T;
+    eq = __reduce_add_sync(0xffffffffu, eq);
+    if (lane == 0 && eq) atomicAdd(eq_slot, eq);
+  }
+  __syncthreads();
+  if (ok) eq_total = *eq_slot;
+  if (ok && eq_total == need) {
+    for (int i = tid; i < nsurv; i += nthr)
+      if (vals[i] >= T) atomicOr(&bits[vidx[i] >> 5], 1u << (vidx[i] & 31));
+  } else if (ok) {
     // every key above T; the keys equal to T in index order until `need`
     int eq = 0;
     for (int row = r0; row < r1; ++row) {

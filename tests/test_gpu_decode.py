@@ -34,8 +34,11 @@ SMALL = CONFIGS["llama_b1_s32k"].with_(
 
 
 def run_parity(cfg, steps=None, group="max", cache=True, bsel=None, rows=True, append=True,
-               v_on_host=False, split=None):
-    st = synth.make_state(cfg, device="cuda")
+               v_on_host=False, split=None, st=None, sels=None):
+    """Decode `steps` steps of `cfg` (state `st`, else a random one) and check
+    each against the oracle; the selections are appended to `sels` if given."""
+    if st is None:
+        st = synth.make_state(cfg, device="cuda")
     if v_on_host:
         st["v"] = st["v"].cpu()
     p = binding.make_params(cfg, group_reduce=binding.GROUP_MAX if group == "max" else binding.GROUP_SUM)
@@ -61,6 +64,8 @@ def run_parity(cfg, steps=None, group="max", cache=True, bsel=None, rows=True, a
         qn = np64(q[sl])
         P, S2, _ = dec.scores(qn)
         check_selection(sel, S2, k, what=f"step {t} selection")
+        if sels is not None:
+            sels.append(sel.copy())
         res = dec.step(qn, np64(kn[sl]) if append else None, np64(vn[sl]) if append else None,
                        force_sel=sel)
         err = head_errors(np64(out[sl]), res.out)
@@ -223,4 +228,27 @@ def test_selection_with_massive_ties():
     hot = st["L"][:, :, :20].clone()
     st["L"].zero_()
     st["L"][:, :, 100:120] = hot
-    run_parity(cfg, steps=3)
+    run_parity(cfg, steps=3, st=st)
+
+
+def test_selection_ties_at_the_threshold():
+    """Landmarks in identical triples at 128K (sampled threshold): the k-th
+    key has equal keys on both sides of the cut, and the selection takes the
+    lowest-index copies of a triple first."""
+    cfg = CONFIGS["llama_b8_s128k"].with_(b=1, steps=3, seed=61)
+    st = synth.make_state(cfg, device="cuda")
+    m = (cfg.n - cfg.o) // 3 * 3
+    L = st["L"]
+    L[:, :, 1:m:3] = L[:, :, 0:m:3]
+    L[:, :, 2:m:3] = L[:, :, 0:m:3]
+    # the outliers lie past the triples, so every copy of a triple is a candidate
+    st["outlier_ids"][:] = torch.arange(m, m + cfg.o, device="cuda", dtype=torch.int32)
+    sels = []
+    run_parity(cfg, steps=3, rows=False, st=st, sels=sels)
+    for t, sel in enumerate(sels):
+        for row in sel.reshape(-1, cfg.k):
+            chosen = set(row.tolist())
+            for j in row:
+                if j < m:
+                    t0 = j - j % 3
+                    assert all(x in chosen for x in range(t0, j)), f"step {t}: chunk {j} without its lower copies"
