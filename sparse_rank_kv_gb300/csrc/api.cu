@@ -75,12 +75,12 @@ struct Sizes {
   size_t A, Bt, L, K_out, V_out, K_loc, V_loc, slot_V, K_sparse, KV_out, KV_loc, KV_slot;
   size_t min_cos, logits, score_part, attn_part, basis, rope_tab;
   size_t out_ids, out_mask, sel, sel_slot, slot_chunk, miss_chunk, miss_slot;
-  size_t miss_count, miss_base, hits, attn_count, counters, status;
+  size_t miss_count, miss_base, att_slot, at_ctr, hits, attn_count, counters, status;
   size_t total() const {
     const size_t v[] = {A, Bt, L, K_out, V_out, K_loc, V_loc, slot_V, K_sparse, KV_out, KV_loc, KV_slot,
                         min_cos, logits,
                         score_part, attn_part, basis, rope_tab, out_ids, out_mask, sel, sel_slot,
-                        slot_chunk, miss_chunk, miss_slot, miss_count, miss_base, hits, attn_count, counters,
+                        slot_chunk, miss_chunk, miss_slot, miss_count, miss_base, att_slot, at_ctr, hits, attn_count, counters,
                         status};
     size_t t = 0;
     for (size_t x : v) t += up(x);
@@ -126,6 +126,8 @@ Sizes sizes_of(const shadowkv_params& p) {
   z.out_mask = b * h * nw * 4;
   z.sel = z.sel_slot = z.slot_chunk = z.miss_chunk = z.miss_slot = b * h * k * 4;
   z.hits = z.attn_count = z.miss_base = b * h * 4;
+  z.att_slot = rec ? b * h * k * 4 : 0;
+  z.at_ctr = rec ? 8 * 4 : 0;
   z.miss_count = 2 * 4;   // compact miss-list length per step parity
   z.counters = 2 * 8;
   z.status = 4;
@@ -249,6 +251,8 @@ skv_status create(const shadowkv_params* p, cudaStream_t st, shadowkv_ctx** out)
   c.miss_slot = static_cast<int32_t*>(take(z.miss_slot));
   c.miss_count = static_cast<int32_t*>(take(z.miss_count));
   c.miss_base = static_cast<int32_t*>(take(z.miss_base));
+  c.att_slot = c.kv_rec ? static_cast<int32_t*>(take(z.att_slot)) : nullptr;
+  c.at_ctr = c.kv_rec ? static_cast<int32_t*>(take(z.at_ctr)) : nullptr;
   c.hits = static_cast<int32_t*>(take(z.hits));
   c.attn_count = static_cast<int32_t*>(take(z.attn_count));
   c.counters = static_cast<unsigned long long*>(take(z.counters));
@@ -263,6 +267,7 @@ skv_status create(const shadowkv_params* p, cudaStream_t st, shadowkv_ctx** out)
   if (e == cudaSuccess) e = cudaMemsetAsync(c.K_loc, 0, z.K_loc, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(c.V_loc, 0, z.V_loc, st);
   if (e == cudaSuccess && c.kv_rec) e = cudaMemsetAsync(c.KV_loc, 0, z.KV_loc, st);
+  if (e == cudaSuccess && c.kv_rec) e = cudaMemsetAsync(c.at_ctr, 0, z.at_ctr, st);
   if (e != cudaSuccess) return bail(cuda_fail(e, "fill slot table"));
 
   // RoPE frequency table: inv_freq_i / (2 pi) as an fp32 (hi, lo) pair
@@ -412,6 +417,7 @@ skv_status shadowkv_prefill(const shadowkv_params* p, const void* k_pre, const v
   if (e == cudaSuccess) e = skv::prefill_device(c, k_pre, v_src, st);
   if (e == cudaSuccess) e = skv::launch_tile_a(c, 1, st);
   if (e == cudaSuccess) e = skv::launch_pack_kv(c, st);
+  if (e == cudaSuccess) e = skv::launch_read_host_v(c, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) { s = cuda_fail(e, "prefill"); destroy(h); return s; }
   s = read_status(c);
@@ -458,6 +464,7 @@ skv_status shadowkv_load_state(const shadowkv_params* p, const shadowkv_state_in
     if (in->v_on_host) parallel_memcpy(c.v_cpu, in->V, c.v_bytes);
     else e = cudaMemcpyAsync(c.v_cpu, in->V, c.v_bytes, cudaMemcpyDeviceToHost, st);
   }
+  if (e == cudaSuccess) e = skv::launch_read_host_v(c, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) { s = cuda_fail(e, "load_state"); destroy(h); return s; }
   s = read_status(c);
@@ -504,6 +511,7 @@ skv_status shadowkv_rewind(shadowkv_ctx* h, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   CK(cudaStreamWaitEvent(st, c.ev_join, 0));   // the last fetch on the side stream
   CK(skv::launch_fill_i32(c, c.slot_chunk, -1, static_cast<size_t>(c.p.b) * c.p.h_kv * c.p.k, st));
+  if (c.at_ctr) CK(cudaMemsetAsync(c.at_ctr, 0, 8 * sizeof(int32_t), st));
   c.n_app = 0;
   return SKV_OK;
 }

@@ -3,33 +3,31 @@
 // over [outliers; RoPE(K_sparse); local window], the G query heads of a KV
 // head sharing every K/V row.
 //
-// Work items are 128-token pieces of one segment (outliers, rebuilt chunks,
-// local window) of one (batch, KV head); one persistent CTA per SM owns a
-// contiguous range of items.
-//   warp 0     : producer -- the head's q (TMA, 16 rows of which the rows
-//                past G read as zeros) into a 2-slot ring when the head
-//                changes; per item the keys and values by bulk copies into a
-//                3-stage ring.  Keys and values are stored by 8-token group
-//                in 4 KB records laid out as the tensor core's no-swizzle
-//                K-major tiles: K ([d/8][token%8][d%8], 2 KB), then V^T
-//                ([d/8][d%8][token%8], 2 KB); a selected chunk is one copy
-//                from its cache slot, the outliers or the local window one
-//                copy per item.
+// Work items are 128-token pieces of one (batch, KV head): its outliers, its
+// local window, its cache hits (16 chunks of 8 tokens per item), then its
+// missed chunks.  Items are taken from two step-wide counters: phase 0
+// (outliers, local window, hits) needs nothing the step's value fetch or key
+// rebuild produce, so it runs while they do (this kernel is launched with
+// programmatic dependent launch right behind them); phase 1 (the misses)
+// starts after griddepcontrol.wait.  Keys and values are stored by 8-token
+// group in 4 KB records laid out as the tensor core's no-swizzle K-major
+// tiles: K ([d/8][token%8][d%8], 2 KB), then V^T ([d/8][d%8][token%8], 2 KB).
+//   warp 0     : producer -- per item the keys and values by bulk copies
+//                (one per selected chunk from its cache slot, one for a piece
+//                of the outliers or local window) and the head's q (TMA, 16
+//                rows of which the rows past G read as zeros) into a 3-stage
+//                ring, with the item's description in the stage.
 //   warp 1     : tcgen05.mma.  S = K q^T (M = 128 tokens, N = 16, K = d) into
 //                one of two TMEM S buffers; after the softmax warps publish
-//                P, O = V^T P^T (M = d, N = 16, K = 128 tokens) into one of
-//                two TMEM O buffers.  The warp polls both queues and issues
-//                whichever product is ready, so P V never waits for the next
-//                item's loads.
-//   warps 2..5 : softmax and accumulation, thread = TMEM lane: for S the
-//                token row (scale, mask, head maxima by integer warp
-//                reductions, p = 2^(s - m), bf16 P^T into shared memory, head
-//                sums), for O the dimension d (running rescale and add).
-//                When the head changes (or the range ends) the CTA writes one
-//                partial (max, sum, sum p v) per query head in the slot of
-//                its first item of that head; the CTA that completes a head's
-//                last items (atomic count) combines the partials in slot
-//                order (the slots follow from the fixed item ranges).
+//                P, O = V^T P^T (M = d, N = 16, K = 16-token steps) into one
+//                of two TMEM O buffers, polling both queues.
+//   warps 2..5 : softmax, thread = TMEM lane: for S the token row (scale,
+//                mask, head maxima by integer warp reductions, p = 2^(s - m),
+//                bf16 P^T into shared memory, head sums), for O the dimension:
+//                the item's partial (max, sum, sum p v) per query head goes to
+//                the item's slot, and a ticket per head counts finished items.
+// When both counters are exhausted a CTA takes heads from a third counter and
+// merges each head's item partials once its ticket shows all of them done.
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
@@ -40,62 +38,61 @@ constexpr int kAtT = 128;                    // tokens per item
 constexpr int kAtD = 128;                    // head dimension handled here
 constexpr int kAtStages = 3;
 constexpr int kAtThreads = 192;
-constexpr int kAtSoft = 128;                 // softmax / accumulation threads
-constexpr int kAtStage = kAtT / 8 * 4096;   // 16 group records (K tile | V^T tile)
+constexpr int kAtSoft = 128;                 // softmax threads
+constexpr int kAtRec = kAtT / 8 * 4096;      // 16 group records (K tile | V^T tile)
 constexpr int kAtQBytes = 16 * kAtD * 2;     // q: 4 x [16 rows][64 B]
+constexpr int kAtStage = kAtRec + kAtQBytes;
 constexpr int kAtPBytes = 16 * kAtT * 2;     // P^T: 16 x 128 bf16
-__host__ __device__ constexpr int at_smem_bytes() {
-  return 1024 /* alignment slack */ + kAtStages * kAtStage + 2 * kAtQBytes + 2 * kAtPBytes +
-         1024 /* barriers, reductions */;
+constexpr int kAtMisc = 1024;                // barriers, item descriptions, reductions
+constexpr int kAtDone = 44;                  // finished items whose tickets are not yet counted
+__host__ __device__ constexpr int at_smem_bytes(int npairs) {
+  return 1024 /* alignment slack */ + kAtStages * kAtStage + 2 * kAtPBytes + kAtMisc + (3 * npairs + 2) * 4;
 }
 
-struct AtSeg {
-  int seg, t0, cnt;
+// An item: its head, kind (0 outliers, 1 local window, 2 hit chunks, 3 missed
+// chunks), first token (0, 1) or first position in the head's slot list (2,
+// 3), tokens, slot of its partial among the head's items, and the head's
+// item count.
+struct AtItem {
+  int pair, seg, t0, cnt, li, ntot;
 };
-__device__ __forceinline__ AtSeg at_item(int j, int i_out, int i_sp, int n_out, int n_sp, int n_loc) {
-  if (j < i_out) return {0, j * kAtT, min(kAtT, n_out - j * kAtT)};
-  j -= i_out;
-  if (j < i_sp) return {1, j * kAtT, min(kAtT, n_sp - j * kAtT)};
-  j -= i_sp;
-  return {2, j * kAtT, min(kAtT, n_loc - j * kAtT)};
-}
 
 template <int G>
 __global__ void __launch_bounds__(kAtThreads, 1)
 k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_out,
-          const bf16* __restrict__ KV_slot, const int32_t* __restrict__ sel_slot,
-          const bf16* __restrict__ KV_loc,
-          bf16* __restrict__ out, float* __restrict__ part, int32_t* __restrict__ ticket, int n_out,
-          int n_sp, int n_loc, int loc_cap, int c, int k, int npairs, int max_splits, float scale_log2,
+          const bf16* __restrict__ KV_slot, const int32_t* __restrict__ att_slot,
+          const int32_t* __restrict__ hits_in, const bf16* __restrict__ KV_loc,
+          bf16* __restrict__ out, float* __restrict__ part, int32_t* __restrict__ ticket,
+          int32_t* __restrict__ ctr, int32_t* __restrict__ ctr_next, int n_out, int n_loc,
+          int loc_cap, int c, int k, int npairs, int max_splits, float scale_log2,
           int* __restrict__ status) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  unsigned char* stages = smem;
-  unsigned char* qbuf = stages + kAtStages * kAtStage;    // [2][kAtQBytes]
-  unsigned char* pbuf = qbuf + 2 * kAtQBytes;             // [2][kAtPBytes]
+  unsigned char* stages = smem;                           // [kAtStages][records | q]
+  unsigned char* pbuf = stages + kAtStages * kAtStage;    // [2][kAtPBytes]
   unsigned char* misc = pbuf + 2 * kAtPBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(misc);     // [kAtStages]
   uint64_t* empty = full + kAtStages;                     // [kAtStages]
-  uint64_t* qfull = empty + kAtStages;                    // [2]
-  uint64_t* qempty = qfull + 2;                           // [2]
-  uint64_t* sfull = qempty + 2;                           // [2]
+  uint64_t* sfull = empty + kAtStages;                    // [2]
   uint64_t* sempty = sfull + 2;                           // [2]
   uint64_t* pfull = sempty + 2;                           // [2]
   uint64_t* ofull = pfull + 2;                            // [2]
   uint64_t* oempty = ofull + 2;                           // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 256);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(misc + 260);
-  int* s_last = reinterpret_cast<int*>(misc + 264);
-  float* red = reinterpret_cast<float*>(misc + 512);      // [2][4][8]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 192);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(misc + 196);
+  volatile int* s_end = reinterpret_cast<volatile int*>(misc + 200);    // items of this CTA, once known
+  int* s_task = reinterpret_cast<int*>(misc + 204);
+  int* s_ndone = reinterpret_cast<int*>(misc + 208);
+  int* s_done = reinterpret_cast<int*>(misc + 328);       // [kAtDone] heads of finished items
+  int* info = reinterpret_cast<int*>(misc + 256);         // [kAtStages][6] item descriptions
+  float* red = reinterpret_cast<float*>(misc + 512);      // [2][4][8] maxima, then sums at +32
+  int* s_p0 = reinterpret_cast<int*>(misc + kAtMisc);     // [npairs + 1] phase-0 item prefix
+  int* s_p1 = s_p0 + npairs + 1;                          // [npairs + 1] phase-1 item prefix
+  int* s_hits = s_p1 + npairs + 1;                        // [npairs]
 
-  const int i_out = (n_out + kAtT - 1) / kAtT, i_sp = (n_sp + kAtT - 1) / kAtT,
-            i_loc = (n_loc + kAtT - 1) / kAtT;
-  const int nsplit = i_out + i_sp + i_loc;
-  const int total = npairs * nsplit;
-  const int lo = static_cast<int>(static_cast<long long>(blockIdx.x) * total / gridDim.x);
-  const int hi = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * total / gridDim.x);
-  const int nit = hi - lo;
+  const int i_out = (n_out + kAtT - 1) / kAtT, i_loc = (n_loc + kAtT - 1) / kAtT;
+  const int cpi = kAtT / c;                               // chunks per item
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   tc::grid_dep_launch();
 
@@ -106,8 +103,6 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
       tc::mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&qfull[i], 1);
-      tc::mbar_init(&qempty[i], 1);
       tc::mbar_init(&sfull[i], 1);
       tc::mbar_init(&sempty[i], kAtSoft / 32);
       tc::mbar_init(&pfull[i], 1);
@@ -116,10 +111,47 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
     }
     tc::fence_mbar_init();
     *s_abort = 0;
+    *s_end = -1;
+    *s_ndone = 0;
+    // the next step's counters start at zero
+    if (blockIdx.x == 0) ctr_next[0] = ctr_next[1] = ctr_next[2] = 0;
   }
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, 64);
     tc::tmem_relinquish();
+  } else if (warp == 0) {
+    // item counts per head from its cache hits, as exclusive prefixes
+    int b0 = 0, b1 = 0;
+    for (int p0 = 0; p0 < npairs; p0 += 32) {
+      const int p = p0 + lane;
+      int h = p < npairs ? hits_in[p] : 0;
+      if (h < 0 || h > k) {
+        flag_error(status, DEV_BAD_COUNT);
+        h = min(max(h, 0), k);
+      }
+      const int n0 = p < npairs ? i_out + i_loc + (h + cpi - 1) / cpi : 0;
+      const int n1 = p < npairs ? (k - h + cpi - 1) / cpi : 0;
+      int x0 = n0, x1 = n1;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y0 = __shfl_up_sync(0xffffffffu, x0, o), y1 = __shfl_up_sync(0xffffffffu, x1, o);
+        if (lane >= o) {
+          x0 += y0;
+          x1 += y1;
+        }
+      }
+      if (p < npairs) {
+        s_p0[p] = b0 + x0 - n0;
+        s_p1[p] = b1 + x1 - n1;
+        s_hits[p] = h;
+      }
+      b0 += __shfl_sync(0xffffffffu, x0, 31);
+      b1 += __shfl_sync(0xffffffffu, x1, 31);
+    }
+    if (lane == 0) {
+      s_p0[npairs] = b0;
+      s_p1[npairs] = b1;
+    }
   }
   // the P rows past G are multiplied by zero values of V: start them at
   // zero so that they are finite (the producer does the same for the value
@@ -131,54 +163,108 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int T0 = s_p0[npairs], T1 = s_p1[npairs];
   auto abort_now = [&]() {
     if (!*s_abort) {
       *s_abort = 1;
       flag_error(status, DEV_TIMEOUT);
     }
   };
-  // the rebuild may still be finishing: its keys are read after this
-  tc::grid_dep_wait();
+  // the head whose items [base[p], base[p + 1]) contain x
+  auto head_of = [&](const int* base, int x) {
+    int a = 0, b = npairs;
+    while (b - a > 1) {
+      const int m = (a + b) >> 1;
+      if (base[m] <= x) a = m;
+      else b = m;
+    }
+    return a;
+  };
+  auto item_of = [&](int phase, int x) -> AtItem {
+    AtItem t;
+    if (phase == 0) {
+      const int p = head_of(s_p0, x), j = x - s_p0[p];
+      t.pair = p;
+      t.li = j;
+      if (j < i_out) {
+        t.seg = 0;
+        t.t0 = j * kAtT;
+        t.cnt = min(kAtT, n_out - t.t0);
+      } else if (j < i_out + i_loc) {
+        t.seg = 1;
+        t.t0 = (j - i_out) * kAtT;
+        t.cnt = min(kAtT, n_loc - t.t0);
+      } else {
+        t.seg = 2;
+        t.t0 = (j - i_out - i_loc) * cpi;
+        t.cnt = min(cpi, s_hits[p] - t.t0) * c;
+      }
+    } else {
+      const int p = head_of(s_p1, x), j = x - s_p1[p];
+      t.pair = p;
+      t.seg = 3;
+      t.t0 = s_hits[p] + j * cpi;
+      t.cnt = min(cpi, k - t.t0) * c;
+      t.li = s_p0[p + 1] - s_p0[p] + j;
+    }
+    t.ntot = s_p0[t.pair + 1] - s_p0[t.pair] + s_p1[t.pair + 1] - s_p1[t.pair];
+    return t;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    int prev = -1, nq = -1, lastA[kAtStages], lastQ[2] = {-1, -1};
+    int lastA[kAtStages];
 #pragma unroll
     for (int i = 0; i < kAtStages; ++i) lastA[i] = -1;
-    for (int it = 0; it < nit; ++it) {
-      const int item = lo + it, pair = item / nsplit, j = item - pair * nsplit;
-      const AtSeg sg = at_item(j, i_out, i_sp, n_out, n_sp, n_loc);
-      bool ok = true;
-      if (pair != prev) {
-        ++nq;
-        const int qs = nq & 1, use = nq >> 1;
-        if (lane == 0) ok = !*s_abort && tc::mbar_wait(&qempty[qs], (use & 1) ^ 1, kWaitLimit);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) {
-          if (lane == 0) abort_now();
-          break;
-        }
+    // item numbers are requested two items ahead, so the atomics' round
+    // trips overlap the copies
+    int phase = 0, x = 0, x1 = 0;
+    if (lane == 0) {
+      x = atomicAdd(&ctr[0], 1);
+      x1 = atomicAdd(&ctr[0], 1);
+    }
+    for (int it = 0;; ++it) {
+      x = __shfl_sync(0xffffffffu, x, 0);
+      if (phase == 0 && x >= T0) {
+        // the misses' keys and values come from the launch before this one
+        // (the number requested ahead is past T0 as well)
+        phase = 1;
+        tc::grid_dep_wait();
         if (lane == 0) {
-          tc::mbar_expect_tx(&qfull[qs], kAtQBytes);
-#pragma unroll
-          for (int kb = 0; kb < kAtD / 32; ++kb)
-            tc::tma_load_3d(qbuf + qs * kAtQBytes + kb * (16 * 64), &mapQ, &qfull[qs], kb * 32, 0, pair);
+          x = atomicAdd(&ctr[1], 1);
+          x1 = atomicAdd(&ctr[1], 1);
         }
-        lastQ[qs] = use;
-        prev = pair;
+        x = __shfl_sync(0xffffffffu, x, 0);
       }
       const int st = it % kAtStages, use = it / kAtStages;
+      const bool done = phase == 1 && x >= T1;
+      const AtItem t = done ? AtItem{-1, 0, 0, 0, 0, 0} : item_of(phase, x);
       // cache slots of the item's chunks (lane = chunk), loaded before the wait
-      const int ch0 = sg.t0 / c, nch = sg.seg == 1 ? sg.cnt / c : 0;
-      const int slot = lane < nch ? sel_slot[static_cast<size_t>(pair) * k + ch0 + lane] : 0;
+      const int nch = t.seg >= 2 ? t.cnt / c : 0;
+      const int slot = lane < nch ? att_slot[static_cast<size_t>(t.pair) * k + t.t0 + lane] : 0;
+      // the number after the next one, requested before this item's copies
+      int xn = 0;
+      if (lane == 0 && !done) xn = atomicAdd(&ctr[phase], 1);
+      bool ok = true;
       if (lane == 0) ok = !*s_abort && tc::mbar_wait(&empty[st], (use & 1) ^ 1, kWaitLimit);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
         if (lane == 0) abort_now();
         break;
       }
+      int* inf = info + st * 6;
+      if (done) {
+        // no more items: an empty stage tells the MMA warp (its previous
+        // item's copies have landed: the stage was released after them)
+        if (lane == 0) {
+          inf[0] = -1;
+          tc::mbar_arrive(&full[st]);
+        }
+        lastA[st] = -1;
+        break;
+      }
       unsigned char* sR = stages + st * kAtStage;
-      const int groups = (sg.cnt + 7) >> 3;
+      const int groups = (t.cnt + 7) >> 3;
       if ((groups & 1) && groups < kAtT / 8) {
         // P V runs over whole 16-token steps: the V^T half of the record
         // after an odd count of groups meets zero weights and must be finite
@@ -189,119 +275,108 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
         __syncwarp();
       }
       if (lane == 0) {
-        tc::mbar_expect_tx(&full[st], static_cast<uint32_t>(groups * 4096));
-        if (sg.seg == 0)
-          tc::bulk_load(sR, KV_out + (static_cast<size_t>(pair) * n_out + sg.t0) * 2 * kAtD,
+        inf[0] = t.pair;
+        inf[1] = t.cnt;
+        inf[2] = t.li;
+        inf[3] = t.ntot;
+        tc::mbar_expect_tx(&full[st], static_cast<uint32_t>(groups * 4096 + kAtQBytes));
+        tc::tma_load_4d(sR + kAtRec, &mapQ, &full[st], 0, 0, 0, t.pair);
+        if (t.seg == 0)
+          tc::bulk_load(sR, KV_out + (static_cast<size_t>(t.pair) * n_out + t.t0) * 2 * kAtD,
                         static_cast<uint32_t>(groups * 4096), &full[st]);
-        else if (sg.seg == 2)
-          tc::bulk_load(sR, KV_loc + (static_cast<size_t>(pair) * loc_cap + sg.t0) * 2 * kAtD,
+        else if (t.seg == 1)
+          tc::bulk_load(sR, KV_loc + (static_cast<size_t>(t.pair) * loc_cap + t.t0) * 2 * kAtD,
                         static_cast<uint32_t>(groups * 4096), &full[st]);
       }
       __syncwarp();
-      if (lane < nch)
-        tc::bulk_load(sR + lane * c * 512, KV_slot + (static_cast<size_t>(pair) * k + slot) * c * 2 * kAtD,
-                      static_cast<uint32_t>(c * 512), &full[st]);
+      if (lane < nch) {
+        if (slot < 0 || slot >= k) {
+          flag_error(status, DEV_BAD_SLOT);
+        } else {
+          tc::bulk_load(sR + lane * c * 512, KV_slot + (static_cast<size_t>(t.pair) * k + slot) * c * 2 * kAtD,
+                        static_cast<uint32_t>(c * 512), &full[st]);
+        }
+      }
       lastA[st] = use;
+      x = x1;
+      x1 = xn;
     }
-    if (lane == 0) {
+    // no copy may still be landing in this CTA's shared memory at exit
+    if (lane == 0)
       for (int i = 0; i < kAtStages; ++i)
-        if (lastA[i] >= 0) tc::mbar_wait(&full[i], lastA[i] & 1, kWaitLimit);
-      for (int i = 0; i < 2; ++i)
-        if (lastQ[i] >= 0) tc::mbar_wait(&qfull[i], lastQ[i] & 1, kWaitLimit);
-    }
+        if (lastA[i] >= 0 && !tc::mbar_wait(&full[i], lastA[i] & 1, kWaitLimit)) abort_now();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(128, 16);
-      // S of item i needs its K tile, the head's q and a free S buffer; O of
-      // item i needs its P and a free O buffer.  Whichever is ready is issued
-      // (polling), so P V never waits for the next item's loads.
-      int prev = -1, nq = -1, ns = 0, no = 0;
-      bool q_ready = false;
-      auto s_ready = [&](int it) -> bool {
-        const int item = lo + it, pair = item / nsplit;
-        if (pair != prev && !q_ready) {
-          if (!tc::mbar_test(&qfull[(nq + 1) & 1], ((nq + 1) >> 1) & 1)) return false;
-          q_ready = true;
-        }
-        return tc::mbar_test(&full[it % kAtStages], (it / kAtStages) & 1) &&
-               tc::mbar_test(&sempty[it & 1], ((it >> 1) & 1) ^ 1);
-      };
-      auto issue_s = [&](int it) {
-        const int item = lo + it, pair = item / nsplit;
-        if (pair != prev) {
-          ++nq;
-          prev = pair;
-          q_ready = false;
-        }
-        const int st = it % kAtStages, sb = it & 1;
-        tc::fence_after();
-        const uint32_t a0 = tc::smem_u32(stages + st * kAtStage);
-        const uint32_t b0 = tc::smem_u32(qbuf + (nq & 1) * kAtQBytes);
-        // K tiles: core matrices of 8 tokens x 8 dims; dim groups 128 B
-        // apart, token groups (records) 4 KB apart.  q: 64-byte swizzle.
-#pragma unroll
-        for (int kb = 0; kb < kAtD / 32; ++kb)
-#pragma unroll
-          for (int ks = 0; ks < 2; ++ks)
-            tc::mma_bf16(tmem + sb * 16, tc::desc_k_none(a0 + (kb * 2 + ks) * 256, 128, 4096),
-                         tc::desc_k_sw64(b0 + kb * (16 * 64) + ks * 32, 512), idesc, (kb | ks) != 0);
-        tc::mma_commit(&sfull[sb]);
-        const bool last_of_pair = it == nit - 1 || (item + 1) / nsplit != pair;
-        if (last_of_pair) tc::mma_commit(&qempty[nq & 1]);
-      };
-      auto o_ready = [&](int it) -> bool {
-        return tc::mbar_test(&pfull[it & 1], (it >> 1) & 1) &&
-               tc::mbar_test(&oempty[it & 1], ((it >> 1) & 1) ^ 1);
-      };
-      auto issue_o = [&](int it) {
-        const int st = it % kAtStages, b = it & 1;
-        const int item = lo + it, pair = item / nsplit;
-        const int nks = (at_item(item - pair * nsplit, i_out, i_sp, n_out, n_sp, n_loc).cnt + 15) >> 4;
-        tc::fence_after();
-        const uint32_t a0 = tc::smem_u32(stages + st * kAtStage + 2048);
-        const uint32_t b0 = tc::smem_u32(pbuf + b * kAtPBytes);
-        // V^T: core matrices of 8 dims x 8 tokens; dim groups 128 B apart,
-        // token groups (records) 4 KB apart.  P^T: 8 heads x 8 tokens; head
-        // groups 128 B apart, token groups 256 B apart.  16 tokens per MMA.
-#pragma unroll
-        for (int ks = 0; ks < kAtT / 16; ++ks)
-          if (ks < nks)
-            tc::mma_bf16(tmem + 32 + b * 16, tc::desc_k_none(a0 + ks * 8192, 4096, 128),
-                         tc::desc_k_none(b0 + ks * 512, 256, 128), idesc, ks != 0);
-        tc::mma_commit(&ofull[b]);
-        tc::mma_commit(&empty[st]);
-      };
+      int ns = 0, no = 0, nit = 0x7fffffff;
       uint64_t t_last = tc::globaltimer_ns();
       while (no < nit) {
         bool progressed = false;
-        if (ns < nit && ns < no + 2 && s_ready(ns)) {
-          issue_s(ns++);
-          progressed = true;
+        if (ns < nit && ns < no + 2) {
+          const int st = ns % kAtStages, sb = ns & 1;
+          if (tc::mbar_test(&full[st], (ns / kAtStages) & 1) &&
+              tc::mbar_test(&sempty[sb], ((ns >> 1) & 1) ^ 1)) {
+            tc::fence_after();
+            if (info[st * 6] < 0) {
+              // the producer has no more items: tell the softmax warps
+              nit = ns;
+              *s_end = ns;
+              tc::mbar_arrive(&sfull[sb]);
+            } else {
+              const uint32_t a0 = tc::smem_u32(stages + st * kAtStage);
+              const uint32_t b0 = a0 + kAtRec;
+              // K tiles: core matrices of 8 tokens x 8 dims; dim groups 128 B
+              // apart, token groups (records) 4 KB apart.  q: core matrices of
+              // 8 rows x 8 dims; dim groups 256 B apart, row groups 128 B apart.
+#pragma unroll
+              for (int kk = 0; kk < kAtD / 16; ++kk)
+                tc::mma_bf16(tmem + sb * 16, tc::desc_k_none(a0 + kk * 256, 128, 4096),
+                             tc::desc_k_none(b0 + kk * 512, 256, 128), idesc, kk != 0);
+              tc::mma_commit(&sfull[sb]);
+              ++ns;
+            }
+            progressed = true;
+          }
         }
-        if (no < ns && o_ready(no)) {
-          issue_o(no++);
+        if (no < ns && tc::mbar_test(&pfull[no & 1], (no >> 1) & 1) &&
+            tc::mbar_test(&oempty[no & 1], ((no >> 1) & 1) ^ 1)) {
+          const int st = no % kAtStages, b = no & 1;
+          const int nks = (info[st * 6 + 1] + 15) >> 4;
+          tc::fence_after();
+          const uint32_t a0 = tc::smem_u32(stages + st * kAtStage + 2048);
+          const uint32_t b0 = tc::smem_u32(pbuf + b * kAtPBytes);
+          // V^T: core matrices of 8 dims x 8 tokens; dim groups 128 B apart,
+          // token groups (records) 4 KB apart.  P^T: 8 heads x 8 tokens; head
+          // groups 128 B apart, token groups 256 B apart.  16 tokens per MMA.
+#pragma unroll
+          for (int ks = 0; ks < kAtT / 16; ++ks)
+            if (ks < nks)
+              tc::mma_bf16(tmem + 32 + b * 16, tc::desc_k_none(a0 + ks * 8192, 4096, 128),
+                           tc::desc_k_none(b0 + ks * 512, 256, 128), idesc, ks != 0);
+          tc::mma_commit(&ofull[b]);
+          tc::mma_commit(&empty[st]);
+          ++no;
           progressed = true;
         }
         if (progressed) {
           t_last = tc::globaltimer_ns();
         } else if (*s_abort || tc::globaltimer_ns() - t_last > kWaitLimit) {
           abort_now();
+          *s_end = ns;
+          tc::mbar_arrive(&sfull[ns & 1]);
           break;
         }
       }
       // every MMA issued has completed before TMEM is released
-      if (nit > 0) tc::mbar_wait(&ofull[(nit - 1) & 1], ((nit - 1) >> 1) & 1, kWaitLimit);
+      if (no > 0) tc::mbar_wait(&ofull[(no - 1) & 1], ((no - 1) >> 1) & 1, kWaitLimit);
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ softmax, accumulation
+    // ------------------------------------------------------------ softmax
     const int ct = tid - 64, quarter = warp & 3;
     const int row = quarter * 32 + lane;          // TMEM lane: token row for S, dimension for O
     const uint32_t tlane = static_cast<uint32_t>(quarter * 32) << 16;
-    float m_run[G], l_run[G], acc[G], m_hist[2][G], m_acc[G];
-    int cur = -1, seg_first = 0, items_in_pair = 0, pending = -1;
-    bool dead = false;
     auto load_cols = [&](uint32_t taddr, float* v) {
       if constexpr (G <= 4) {
         float t4[4];
@@ -312,10 +387,13 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
         tc::tmem_ld8(taddr, v);
       }
     };
-    // fold item j's P V (in TMEM O buffer j & 1) into the running sums
-    auto accumulate = [&](int j) {
+    bool dead = false;
+    // the pending item: its O buffer holds sum p v once ofull completes
+    int pj = -1, ppair = 0, pli = 0;
+    float pm[G], pl[G];
+    auto finish = [&]() {
       if (!dead) {
-        bool ok = !*s_abort && tc::mbar_wait(&ofull[j & 1], (j >> 1) & 1, kWaitLimit);
+        bool ok = !*s_abort && tc::mbar_wait(&ofull[pj & 1], (pj >> 1) & 1, kWaitLimit);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
           if (lane == 0) abort_now();
@@ -324,115 +402,35 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
       }
       if (dead) return;
       tc::fence_after();
-      float o[G];
-      load_cols(tmem + tlane + 32 + (j & 1) * 16, o);
+      float o[8];
+      load_cols(tmem + tlane + 32 + (pj & 1) * 16, o);
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&oempty[j & 1]);
+      if (lane == 0) tc::mbar_arrive(&oempty[pj & 1]);
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const float mj = m_hist[j & 1][g];
-        const float sc = m_acc[g] == -INFINITY ? 0.f : exp2f(m_acc[g] - mj);
-        acc[g] = acc[g] * sc + o[g];
-        m_acc[g] = mj;
-      }
-    };
-    auto lo_of = [&](int b) { return static_cast<int>(static_cast<long long>(b) * total / gridDim.x); };
-    auto finish_pair = [&](int pair) {
-      // this CTA's partial of the head, in the slot of its first item
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float* pp = part + ((static_cast<size_t>(pair) * G + g) * max_splits + seg_first) * (kAtD + 2);
-        pp[row] = acc[g];
+        float* pp = part + ((static_cast<size_t>(ppair) * G + g) * max_splits + pli) * (kAtD + 2);
+        pp[row] = o[g];
         if (ct == 0) {
-          pp[kAtD] = m_run[g];
-          pp[kAtD + 1] = l_run[g];
+          pp[kAtD] = pm[g];
+          pp[kAtD + 1] = pl[g];
         }
       }
-      __threadfence();
+      // the head's ticket counts the item once its partial is visible; the
+      // counts are published together (one fence) when the CTA's items end
+      if (ct == 0) s_done[(*s_ndone)++] = ppair;
+    };
+    auto publish = [&]() {
       tc::named_sync(1, kAtSoft);
-      if (ct == 0) *s_last = atomicAdd(&ticket[pair], items_in_pair) + items_in_pair == nsplit;
-      tc::named_sync(1, kAtSoft);
-      if (!*s_last) return;
-      __threadfence();
-      // CTAs cta_of(x0) .. cta_of(x1 - 1) hold the head's items [x0, x1),
-      // each its partial in the slot of its first item of the head.  Every
-      // thread loads the (max, sum, value) of all heads for up to U CTAs at
-      // once (one round trip) and merges them online.
-      const int x0 = pair * nsplit, x1 = x0 + nsplit;
-      const int nb = static_cast<int>(gridDim.x);
-      auto cta_of = [&](int x) {
-        return static_cast<int>((static_cast<long long>(x + 1) * nb - 1) / total);
-      };
-      const int b0 = cta_of(x0), b1 = cta_of(x1 - 1);
-      constexpr int U = G <= 4 ? 4 : 2;
-      const size_t pb = static_cast<size_t>(pair) * G * max_splits;
-      float M[G], den[G], num[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        M[g] = -INFINITY;
-        den[g] = 0.f;
-        num[g] = 0.f;
+      if (ct == 0 && *s_ndone > 0) {
+        __threadfence();
+        for (int i = 0; i < *s_ndone; ++i) atomicAdd(&ticket[s_done[i]], 1);
+        *s_ndone = 0;
       }
-      for (int bb = b0; bb <= b1; bb += U) {
-        float mv[U][G], lv[U][G], pv[U][G];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int slot = bb + u <= b1 ? max(lo_of(bb + u), x0) - x0 : -1;
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            if (slot >= 0) {
-              const float* pp = part + (pb + static_cast<size_t>(g) * max_splits + slot) * (kAtD + 2);
-              mv[u][g] = __ldcg(pp + kAtD);
-              lv[u][g] = __ldcg(pp + kAtD + 1);
-              pv[u][g] = __ldcg(pp + row);
-            } else {
-              mv[u][g] = -INFINITY;
-              lv[u][g] = 0.f;
-              pv[u][g] = 0.f;
-            }
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            if (mv[u][g] == -INFINITY) continue;
-            const float mn = fmaxf(M[g], mv[u][g]);
-            const float so = M[g] == -INFINITY ? 0.f : exp2f(M[g] - mn), ss = exp2f(mv[u][g] - mn);
-            den[g] = den[g] * so + lv[u][g] * ss;
-            num[g] = num[g] * so + pv[u][g] * ss;
-            M[g] = mn;
-          }
-      }
-#pragma unroll
-      for (int g = 0; g < G; ++g)
-        out[(static_cast<size_t>(pair) * G + g) * kAtD + row] = __float2bfloat16_rn(num[g] / den[g]);
-      if (ct == 0) ticket[pair] = 0;
       tc::named_sync(1, kAtSoft);
     };
-    for (int it = 0; it < nit; ++it) {
-      const int item = lo + it, pair = item / nsplit, j = item - pair * nsplit;
-      const AtSeg sg = at_item(j, i_out, i_sp, n_out, n_sp, n_loc);
-      if (pair != cur) {
-        if (cur >= 0) {
-          if (pending >= 0) accumulate(pending);
-          pending = -1;
-          finish_pair(cur);
-        }
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          m_run[g] = -INFINITY;
-          l_run[g] = 0.f;
-          acc[g] = 0.f;
-          m_acc[g] = -INFINITY;
-        }
-        cur = pair;
-        seg_first = j;
-        items_in_pair = 0;
-      }
-      ++items_in_pair;
-      const int sb = it & 1;
+    for (int it = 0;; ++it) {
+      const int sb = it & 1, st = it % kAtStages;
       if (!dead) {
         bool ok = !*s_abort && tc::mbar_wait(&sfull[sb], (it >> 1) & 1, kWaitLimit);
         ok = __all_sync(0xffffffffu, ok);
@@ -441,19 +439,18 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
           dead = true;
         }
       }
+      if (dead || *s_end == it) break;
+      // the item's description (its stage is complete and not yet reused)
+      if (!tc::mbar_wait(&full[st], (it / kAtStages) & 1, kWaitLimit) && lane == 0) abort_now();
+      const int pair = info[st * 6], cnt = info[st * 6 + 1], li = info[st * 6 + 2];
       float s[8];
-      if (!dead) {
-        tc::fence_after();
-        load_cols(tmem + tlane + sb * 16, s);
-        tc::fence_before();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&sempty[sb]);
-      } else {
-#pragma unroll
-        for (int g = 0; g < G; ++g) s[g] = 0.f;
-      }
-      const bool valid = row < sg.cnt;
-      float* rmax = red + (it & 1) * 64;            // [4][8] maxima, then [4][8] sums at +32
+      tc::fence_after();
+      load_cols(tmem + tlane + sb * 16, s);
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&sempty[sb]);
+      const bool valid = row < cnt;
+      float* rmax = red + (it & 1) * 64;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         s[g] = valid ? s[g] * scale_log2 : -INFINITY;
@@ -462,17 +459,13 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
       }
       tc::named_sync(1, kAtSoft);
       unsigned char* P = pbuf + sb * kAtPBytes;
-      float alpha[G];
+      float mi[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        float mi = rmax[g];
+        mi[g] = rmax[g];
 #pragma unroll
-        for (int w = 1; w < 4; ++w) mi = fmaxf(mi, rmax[w * 8 + g]);
-        const float m_new = fmaxf(m_run[g], mi);
-        alpha[g] = m_run[g] == -INFINITY ? 0.f : exp2f(m_run[g] - m_new);
-        m_run[g] = m_new;
-        m_hist[sb][g] = m_new;
-        const float p = valid ? exp2f(s[g] - m_new) : 0.f;
+        for (int w = 1; w < 4; ++w) mi[g] = fmaxf(mi[g], rmax[w * 8 + g]);
+        const float p = valid ? exp2f(s[g] - mi[g]) : 0.f;
         // P^T[g][row]: token group row/8 (256 B), head group g/8 (128 B), head row g%8 (16 B)
         *reinterpret_cast<bf16*>(P + (row >> 3) * 256 + (g >> 3) * 128 + (g & 7) * 16 + (row & 7) * 2) =
             __float2bfloat16_rn(p);
@@ -481,18 +474,108 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
       }
       tc::fence_proxy_async_smem();
       tc::named_sync(1, kAtSoft);
-      if (ct == 0 && !dead) tc::mbar_arrive(&pfull[sb]);
+      if (ct == 0) tc::mbar_arrive(&pfull[sb]);
+      float li_sum[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) li_sum[g] = rmax[32 + g] + rmax[40 + g] + rmax[48 + g] + rmax[56 + g];
+      if (pj >= 0) {
+        if (*s_ndone == kAtDone) publish();
+        finish();
+      }
+      pj = it;
+      ppair = pair;
+      pli = li;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const float z = rmax[32 + g] + rmax[40 + g] + rmax[48 + g] + rmax[56 + g];
-        l_run[g] = l_run[g] * alpha[g] + z;
+        pm[g] = mi[g];
+        pl[g] = li_sum[g];
       }
-      if (pending >= 0) accumulate(pending);
-      pending = it;
     }
-    if (cur >= 0) {
-      if (pending >= 0) accumulate(pending);
-      finish_pair(cur);
+    if (pj >= 0 && !dead) {
+      if (*s_ndone == kAtDone) publish();
+      finish();
+    }
+    if (!dead) publish();
+
+    // ------------------------------------------------------------ combine
+    // heads from the third counter; each waits for its ticket to show all of
+    // its items' partials, then merges them (weights 2^(m - M) / sum)
+    // [G][wcap] maxima, turned into weights, then [G][wcap] sums (P^T is no
+    // longer used)
+    float* w = reinterpret_cast<float*>(pbuf);
+    const int wcap = kAtPBytes / 4 / G;
+    float* lsum = w + G * wcap;
+    while (!dead) {
+      if (ct == 0) *s_task = atomicAdd(&ctr[2], 1);
+      tc::named_sync(1, kAtSoft);
+      const int pair = *s_task;
+      tc::named_sync(1, kAtSoft);
+      if (pair >= npairs) break;
+      const int ntot = s_p0[pair + 1] - s_p0[pair] + s_p1[pair + 1] - s_p1[pair];
+      if (ct == 0) {
+        bool ok = ntot <= wcap;
+        const uint64_t t0 = tc::globaltimer_ns();
+        while (ok) {
+          int v;
+          asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ticket + pair) : "memory");
+          if (v >= ntot) break;
+          if (tc::globaltimer_ns() - t0 > kWaitLimit) ok = false;
+        }
+        if (!ok) abort_now();
+      }
+      tc::named_sync(1, kAtSoft);
+      if (*s_abort) break;
+      const size_t pb = static_cast<size_t>(pair) * G * max_splits;
+      // every item's (max, sum) per query head, one round trip
+      for (int e = ct; e < G * ntot; e += kAtSoft) {
+        const int g = e / ntot, i = e - g * ntot;
+        const float* pp = part + (pb + static_cast<size_t>(g) * max_splits + i) * (kAtD + 2) + kAtD;
+        w[g * wcap + i] = __ldcg(pp);
+        lsum[g * wcap + i] = __ldcg(pp + 1);
+      }
+      tc::named_sync(1, kAtSoft);
+      if (warp - 2 < G) {
+        // warp g: M, the sum of 2^(m - M) l, then the weights 2^(m - M) / sum
+        for (int gg = warp - 2; gg < G; gg += 4) {
+          float M = -INFINITY;
+          for (int i = lane; i < ntot; i += 32) M = fmaxf(M, w[gg * wcap + i]);
+          M = warp_max(M);
+          float den = 0.f;
+          for (int i = lane; i < ntot; i += 32) den += exp2f(w[gg * wcap + i] - M) * lsum[gg * wcap + i];
+          den = warp_sum(den);
+          const float inv = 1.f / den;
+          for (int i = lane; i < ntot; i += 32) w[gg * wcap + i] = exp2f(w[gg * wcap + i] - M) * inv;
+        }
+      }
+      tc::named_sync(1, kAtSoft);
+      // sum over items of weight x partial: items outermost, so that the
+      // loads of all heads for 8 items are in flight together
+      float num[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) num[g] = 0.f;
+      const float* pr = part + pb * (kAtD + 2) + row;
+      int i = 0;
+      for (; i + 8 <= ntot; i += 8) {
+        float v[8][G];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+            v[u][g] = __ldcg(pr + (static_cast<size_t>(g) * max_splits + i + u) * (kAtD + 2));
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+#pragma unroll
+          for (int g = 0; g < G; ++g) num[g] = fmaf(w[g * wcap + i + u], v[u][g], num[g]);
+      }
+      for (; i < ntot; ++i)
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+          num[g] = fmaf(w[g * wcap + i], __ldcg(pr + (static_cast<size_t>(g) * max_splits + i) * (kAtD + 2)), num[g]);
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+        out[(static_cast<size_t>(pair) * G + g) * kAtD + row] = __float2bfloat16_rn(num[g]);
+      if (ct == 0) ticket[pair] = 0;
+      tc::named_sync(1, kAtSoft);
     }
   }
   tc::fence_before();
@@ -502,40 +585,85 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
 }
 
 // ---------------------------------------------------------------- host side
-bool attn_tc_supported(const shadowkv_params& p) {
-  return p.dtype == SKV_DTYPE_BF16 && p.d == kAtD && p.c % 8 == 0 && kAtT % p.c == 0 &&
-         static_cast<long long>(p.b) * p.h_kv <= 1024 && at_smem_bytes() <= 227 * 1024;
+// The queries as a 4D view {8 dims, G rows, d/8 dim groups, b*h_kv} (strides
+// 2 B, d*2 B, 16 B, G*d*2 B), read in boxes of 8 x 16 x 16 x 1: a head's q
+// lands as [d/8][16 rows][8 dims], the rows past G zero-filled.
+cudaError_t qa_map_for(Ctx& c, const void* q, CUtensorMap* map) {
+  if (!c.qa_map || q != c.qa_enc) {
+    c.qa_map = false;
+    if (reinterpret_cast<uintptr_t>(q) % 16) return cudaErrorMisalignedAddress;
+    void* fnp = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fnp, 12000, cudaEnableDefault, &qr) !=
+            cudaSuccess || fnp == nullptr)
+      return cudaErrorNotSupported;
+    using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+    const cuuint64_t dims[4] = {8, static_cast<cuuint64_t>(c.G), static_cast<cuuint64_t>(kAtD / 8),
+                                static_cast<cuuint64_t>(c.p.b) * c.p.h_kv};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kAtD) * 2, 16,
+                                   static_cast<cuuint64_t>(kAtD) * 2 * c.G};
+    const cuuint32_t box[4] = {8, 16, kAtD / 8, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = reinterpret_cast<EncodeFn>(fnp)(
+        &c.mapQa, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), dims, strides, box, estr,
+        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    c.qa_enc = q;
+    c.qa_map = true;
+  }
+  *map = c.mapQa;
+  return cudaSuccess;
 }
 
-int attn_tc_splits(const Ctx& c, int n_loc) {
-  const int n_out = c.p.o * c.p.c, n_sp = c.p.k * c.p.c;
-  return (n_out + kAtT - 1) / kAtT + (n_sp + kAtT - 1) / kAtT + (n_loc + kAtT - 1) / kAtT;
+// Items per head at most: outliers, local window, the hit chunks and the
+// missed chunks (whose split may add one item).
+static int at_items_max(const shadowkv_params& p, int n_loc) {
+  const int cpi = kAtT / p.c;
+  return (p.o * p.c + kAtT - 1) / kAtT + (n_loc + kAtT - 1) / kAtT + (p.k + cpi - 1) / cpi + 1;
+}
+
+bool attn_tc_supported(const shadowkv_params& p) {
+  const int npairs_max = 1024;
+  const int G = p.h_q / p.h_kv;
+  const int items = at_items_max(p, p.w + p.max_new);
+  return p.dtype == SKV_DTYPE_BF16 && p.d == kAtD && p.c % 8 == 0 && kAtT % p.c == 0 &&
+         static_cast<long long>(p.b) * p.h_kv <= npairs_max && at_smem_bytes(npairs_max) <= 227 * 1024 &&
+         G >= 1 && items * G <= kAtPBytes / 4;
 }
 
 template <int G>
 static cudaError_t attn_tc_t(Ctx& c, const CUtensorMap& mq, void* out, int n_loc, cudaStream_t st) {
-  const int smem = at_smem_bytes();
+  const int npairs = c.p.b * c.p.h_kv;
+  const int smem = at_smem_bytes(npairs);
   auto kern = k_attn_tc<G>;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
-  const int npairs = c.p.b * c.p.h_kv;
-  const int items = npairs * attn_tc_splits(c, n_loc);
-  const int grid = std::min(c.nsm, items);
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kAtD));
-  // after a launch that also fetches values over the host link the
-  // attention's CTAs are not made resident early: they slow the fetch
-  return launch_ex(!rebuild_fetches(c), kern, dim3(grid), dim3(kAtThreads), smem, st, mq, static_cast<const bf16*>(c.KV_out),
-                    static_cast<const bf16*>(c.KV_slot), static_cast<const int32_t*>(c.sel_slot),
-                    static_cast<const bf16*>(c.KV_loc),
-                    static_cast<bf16*>(out), c.attn_part, c.attn_count, c.p.o * c.p.c, c.p.k * c.p.c,
-                    n_loc, c.loc_cap, c.p.c, c.p.k, npairs, c.max_splits, scale_log2, c.status);
+  const int par = static_cast<int>(c.t & 1);
+  // each launch clears the other parity's counters for the next step; after
+  // a step on another attention path this parity's are cleared here
+  if (c.at_last != c.t - 1) {
+    e = cudaMemsetAsync(c.at_ctr + 4 * par, 0, 4 * sizeof(int32_t), st);
+    if (e != cudaSuccess) return e;
+  }
+  c.at_last = c.t;
+  // launched behind the value fetch and key rebuild: phase 0 overlaps them
+  return launch_pdl(kern, dim3(c.nsm), dim3(kAtThreads), static_cast<size_t>(smem), st, mq,
+                    static_cast<const bf16*>(c.KV_out), static_cast<const bf16*>(c.KV_slot),
+                    static_cast<const int32_t*>(c.att_slot), static_cast<const int32_t*>(c.hits),
+                    static_cast<const bf16*>(c.KV_loc), static_cast<bf16*>(out), c.attn_part, c.attn_count,
+                    c.at_ctr + 4 * par, c.at_ctr + 4 * (par ^ 1), c.p.o * c.p.c, n_loc, c.loc_cap, c.p.c,
+                    c.p.k, npairs, c.max_splits, scale_log2, c.status);
 }
 
 cudaError_t launch_attn_tc(Ctx& c, const void* q, void* out, int n_loc, cudaStream_t st) {
-  if (attn_tc_splits(c, n_loc) > c.max_splits) return cudaErrorInvalidValue;
+  if (at_items_max(c.p, n_loc) > c.max_splits) return cudaErrorInvalidValue;
   CUtensorMap mq;
   {
-    const cudaError_t e = q_map_for(c, q, &mq);
+    const cudaError_t e = qa_map_for(c, q, &mq);
     if (e != cudaSuccess) return e;
   }
   switch (c.G) {

@@ -78,7 +78,7 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part,
          int cache_on, int32_t* __restrict__ sel, int32_t* __restrict__ sel_slot,
          int32_t* __restrict__ slot_chunk, int32_t* __restrict__ miss_chunk,
          int32_t* __restrict__ miss_slot, int32_t* __restrict__ miss_total,
-         int32_t* __restrict__ miss_base, int par,
+         int32_t* __restrict__ miss_base, int32_t* __restrict__ att_slot, int par,
          int32_t* __restrict__ hits, unsigned long long* __restrict__ counters,
          const T* __restrict__ k_new, const T* __restrict__ v_new, T* __restrict__ K_loc,
          T* __restrict__ V_loc, T* __restrict__ KV_loc, int loc_row, int loc_cap,
@@ -251,6 +251,10 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part,
   const int mrank = block_exclusive_scan(is_miss, tmp, &nmiss);
   const int frank = block_exclusive_scan(is_free, tmp, &nfree);
   if (is_free) s_free[frank] = tid;
+  // the attention's order of the selected chunks' slots: hits first (each
+  // after the hits before it), then misses
+  if (att_slot != nullptr && tid < k && !is_miss)
+    att_slot[static_cast<size_t>(pair) * k + tid - mrank] = s_slot[tid];
   __syncthreads();
   if (nmiss != nfree) flag_error(status, DEV_BAD_COUNT);
   // reserve this head's range of the step's compact miss list; the block of
@@ -268,6 +272,7 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part,
     sc_row[slot] = s_sel[tid];
     miss_chunk[s_base + mrank] = pair * n + s_sel[tid];
     miss_slot[s_base + mrank] = pair * k + slot;
+    if (att_slot != nullptr) att_slot[static_cast<size_t>(pair) * k + (k - nmiss) + mrank] = slot;
   }
   __syncthreads();
   for (int i = tid; i < k; i += nthr) {
@@ -454,7 +459,7 @@ static cudaError_t select_t(Ctx& c, const void* k_new, const void* v_new, int lo
   return launch_pdl(kern, dim3(c.p.b * c.p.h_kv), dim3(kSelectThreads), smem, st,
       c.logits, c.score_part, c.out_mask, c.n, c.ntile, c.p.k, c.p.group_reduce,
       c.cache_on ? 1 : 0, c.sel, c.sel_slot, c.slot_chunk, c.miss_chunk, c.miss_slot,
-      c.miss_count, c.miss_base, static_cast<int>(c.t & 1), c.hits, c.counters, static_cast<const T*>(k_new),
+      c.miss_count, c.miss_base, c.att_slot, static_cast<int>(c.t & 1), c.hits, c.counters, static_cast<const T*>(k_new),
       static_cast<const T*>(v_new),
       static_cast<T*>(c.K_loc), static_cast<T*>(c.V_loc), static_cast<T*>(c.KV_loc), loc_row, c.loc_cap,
       c.status);

@@ -42,6 +42,9 @@ struct Timed {
 // more SMs.
 constexpr int kFetchSMs = 16;
 constexpr int kFetchSMsRec = 64;
+// CTAs of the record rebuild (missed chunks only): the attention's first
+// phase runs beside it on the remaining SMs
+constexpr int kRebuildSMsRec = 32;
 
 struct Ctx {
   shadowkv_params p{};
@@ -91,11 +94,19 @@ struct Ctx {
   int fetch_sms = kFetchSMs;
   void *KV_out = nullptr, *KV_loc = nullptr, *KV_slot = nullptr;
   int32_t* miss_base = nullptr;   // per (batch, KV head): start of its misses in the step's list
+  int32_t* att_slot = nullptr;    // per head: slots of its hits, then of its misses (attention order)
+  int32_t* at_ctr = nullptr;      // attention work counters, 4 per step parity
+  long long at_last = -2;         // step of the last tensor-core attention launch
   // tensor map of the caller's query buffer (16-row boxes), encoded again
   // only when the buffer's address changes
   const void* q_enc = nullptr;
   CUtensorMap mapQ{};
   bool q_map = false;
+  // the same queries for the attention: one 4D box per head lands in the
+  // no-swizzle K-major core-matrix order ([d/8][16 rows][8])
+  const void* qa_enc = nullptr;
+  CUtensorMap mapQa{};
+  bool qa_map = false;
   CUtensorMap mapL{};           // landmarks (b*h_kv*n x d) for the tensor-core score kernel
   bool tc_rebuild = false;      // shapes and dtype allow the tcgen05 rebuild
   bool tc_score = false;        // ... and the tcgen05 landmark scores
@@ -184,11 +195,18 @@ cudaError_t launch_attn_tc(Ctx& c, const void* q, void* out, int n_loc, cudaStre
 cudaError_t encode_q_map(const Ctx& c, const void* q, CUtensorMap* map);
 // the query map for buffer q: the context's cached one, encoded when q differs
 cudaError_t q_map_for(Ctx& c, const void* q, CUtensorMap* map);
+// attn_tc.cu: the attention's query map (one box per head), cached the same way
+cudaError_t qa_map_for(Ctx& c, const void* q, CUtensorMap* map);
 // prefill_kernels.cu
 // Runs Algorithm 1 on the device.  v is a device pointer, or (v_mapped) the
 // mapped device address of pinned host memory.
 cudaError_t prefill_device(Ctx& c, const void* k_pre, const void* v, cudaStream_t st);
 cudaError_t launch_transpose_b(Ctx& c, const void* B, cudaStream_t st);
 cudaError_t launch_fill_i32(Ctx& c, int32_t* p, int32_t v, size_t n, cudaStream_t st);
+// One read of the whole pinned host copy of V through its device mapping:
+// the decode steps' value fetches then do not pay the first GPU access to
+// each host page (measured on GB300: the first 32 steps after an offload ran
+// 40% slower without it).
+cudaError_t launch_read_host_v(Ctx& c, cudaStream_t st);
 
 }  // namespace skv

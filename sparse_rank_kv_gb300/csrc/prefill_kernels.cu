@@ -370,6 +370,27 @@ static int grid_for(size_t total, int threads, int cap) {
   return static_cast<int>(g < 1 ? 1 : g);
 }
 
+// Reads every 16 bytes of the pinned host copy of V through its device
+// mapping once.  The result only feeds a store under `keep`, which the host
+// passes as 0; it keeps the loads from being optimised away.
+__global__ void k_read_host(const uint4* __restrict__ p, size_t n, int keep, unsigned int* __restrict__ sink) {
+  unsigned int acc = 0;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const uint4 v = p[i];
+    acc ^= v.x ^ v.y ^ v.z ^ v.w;
+  }
+  if (keep) atomicXor(sink, acc);
+}
+
+cudaError_t launch_read_host_v(Ctx& c, cudaStream_t st) {
+  kbegin(c, K_MISC, st);
+  k_read_host<<<c.nsm, 1024, 0, st>>>(static_cast<const uint4*>(c.v_cpu_dev), c.v_bytes / 16, 0,
+                                      reinterpret_cast<unsigned int*>(c.status));
+  kend(c, K_MISC, st);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_fill_i32(Ctx& c, int32_t* p, int32_t v, size_t n, cudaStream_t st) {
   kbegin(c, K_MISC, st);
   k_fill_i32<<<grid_for(n, 256, 4096), 256, 0, st>>>(p, v, n);

@@ -236,8 +236,11 @@ k_rebuild_pipe(const bf16* __restrict__ A, const __grid_constant__ CUtensorMap m
     // the first nfetch CTAs move the step's value misses over the host link
     // while the others rebuild the missed chunks' keys
     if (static_cast<int>(blockIdx.x) < nfetch) {
-      tc::grid_dep_launch();
+      // the attention launched behind may start once the selection is
+      // complete (it reads the selection, not this launch's results, until
+      // its own wait)
       tc::grid_dep_wait();
+      tc::grid_dep_launch();
       fetch_value_groups(vcpu, KV_slot, miss_chunk, miss_slot, miss_total[par], s, n, c, k, npairs,
                          static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x,
                          static_cast<long long>(nfetch) * blockDim.x, status);
@@ -312,7 +315,7 @@ k_rebuild_pipe(const bf16* __restrict__ A, const __grid_constant__ CUtensorMap m
     const int slot = REC ? miss_slot[e] - t.pair * k : 0;
     return {chunk_at(e, t.pair) * c + (row % c), slot};
   };
-  tc::grid_dep_launch();
+  if (!REC) tc::grid_dep_launch();
   if (tid == 0) {
     tc::prefetch_tensormap(&mapBt);
     if (!REC) tc::prefetch_tensormap(&mapK);
@@ -344,6 +347,7 @@ k_rebuild_pipe(const bf16* __restrict__ A, const __grid_constant__ CUtensorMap m
   };
   // the selection may still be finishing: its chunk ids are read after this
   tc::grid_dep_wait();
+  if (REC) tc::grid_dep_launch();
   if constexpr (REC) {
     if (warp == 0) {
       // exclusive prefix of the heads' tile counts, 32 heads per round
@@ -666,7 +670,8 @@ static cudaError_t rebuild_tc(Ctx& c, cudaStream_t st) {
   // records: the value fetch runs in the same launch, on its own CTAs;
   // otherwise it runs on a side stream and the rebuild leaves it its SMs
   const int nfetch = REC ? std::min(c.fetch_sms, c.nsm / 2) : 0;
-  const int sms = REC ? c.nsm - nfetch : c.nsm > 2 * c.fetch_sms ? c.nsm - c.fetch_sms : c.nsm;
+  const int sms = REC ? std::min(kRebuildSMsRec, c.nsm - nfetch)
+                      : c.nsm > 2 * c.fetch_sms ? c.nsm - c.fetch_sms : c.nsm;
   const int grid = nfetch + std::min(sms, tiles);
   return launch_pdl(kern, dim3(grid), dim3(kPipeThreads), ps.smem, st, static_cast<const bf16*>(c.A),
                     c.mapBt, c.mapK, static_cast<const int32_t*>(c.sel),

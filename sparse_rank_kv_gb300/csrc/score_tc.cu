@@ -89,25 +89,26 @@ k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUt
   tc::grid_dep_wait();
 
   if (warp == 0) {
-    if (lane == 0) {
-      for (int i = 0; i < ntl; ++i) {
-        const int s = i % kScStages;
-        const uint32_t ph = (i / kScStages) & 1;
-        if (!tc::mbar_wait(&empty[s], ph ^ 1, kWaitLimit)) {
-          flag_error(status, DEV_TIMEOUT);
-          break;
-        }
-        const int tile = t_begin + i;
-        const int pair = tile / ntile, ti = tile - pair * ntile;
-        unsigned char* st = stages + s * STAGE;
-        tc::mbar_expect_tx(&full[s], STAGE);
-#pragma unroll
-        for (int kb = 0; kb < KB; ++kb)
-          tc::tma_load_2d(st + kb * (kScTile * 64), &mapL, &full[s], kb * 32, pair * n + ti * kScTile);
-#pragma unroll
-        for (int kb = 0; kb < KB; ++kb)
-          tc::tma_load_3d(st + A_BYTES + kb * (16 * 64), &mapQ, &full[s], kb * 32, 0, pair);
+    // lane 0 waits for the stage and arms its barrier; lanes 0..2KB-1 then
+    // issue one box each (landmark boxes, then q boxes), so the copies of a
+    // stage are not serialised behind one thread's issue
+    for (int i = 0; i < ntl; ++i) {
+      const int s = i % kScStages;
+      const uint32_t ph = (i / kScStages) & 1;
+      bool ok = true;
+      if (lane == 0) {
+        ok = tc::mbar_wait(&empty[s], ph ^ 1, kWaitLimit);
+        if (!ok) flag_error(status, DEV_TIMEOUT);
+        else tc::mbar_expect_tx(&full[s], STAGE);
       }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      const int tile = t_begin + i;
+      const int pair = tile / ntile, ti = tile - pair * ntile;
+      unsigned char* st = stages + s * STAGE;
+      if (lane < KB)
+        tc::tma_load_2d(st + lane * (kScTile * 64), &mapL, &full[s], lane * 32, pair * n + ti * kScTile);
+      else if (lane < 2 * KB)
+        tc::tma_load_3d(st + A_BYTES + (lane - KB) * (16 * 64), &mapQ, &full[s], (lane - KB) * 32, 0, pair);
     }
   } else if (warp == 1) {
     if (lane == 0) {
