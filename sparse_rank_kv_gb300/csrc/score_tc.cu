@@ -44,8 +44,9 @@ __global__ void __launch_bounds__(kScThreads, 1)
 k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUtensorMap mapQ,
            const uint32_t* __restrict__ mask, float* __restrict__ P, float2* __restrict__ part, int n,
            int ntile, int total_tiles, float scale, int* __restrict__ status) {
-  constexpr int KB = D / 32;
-  constexpr int A_BYTES = KB * kScTile * 64;
+  constexpr int KB = D / 32;                  // q boxes of 32 dims (64-byte swizzle)
+  constexpr int KA = D / 64;                  // landmark boxes of 64 dims (128-byte swizzle)
+  constexpr int A_BYTES = KA * kScTile * 128;
   constexpr int STAGE = sc_stage_bytes(D);
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -105,10 +106,10 @@ k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUt
       const int tile = t_begin + i;
       const int pair = tile / ntile, ti = tile - pair * ntile;
       unsigned char* st = stages + s * STAGE;
-      if (lane < KB)
-        tc::tma_load_2d(st + lane * (kScTile * 64), &mapL, &full[s], lane * 32, pair * n + ti * kScTile);
-      else if (lane < 2 * KB)
-        tc::tma_load_3d(st + A_BYTES + (lane - KB) * (16 * 64), &mapQ, &full[s], (lane - KB) * 32, 0, pair);
+      if (lane < KA)
+        tc::tma_load_2d(st + lane * (kScTile * 128), &mapL, &full[s], lane * 64, pair * n + ti * kScTile);
+      else if (lane < KA + KB)
+        tc::tma_load_3d(st + A_BYTES + (lane - KA) * (16 * 64), &mapQ, &full[s], (lane - KA) * 32, 0, pair);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -125,14 +126,13 @@ k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUt
         tc::fence_after();
         const uint32_t a0 = tc::smem_u32(stages + s * STAGE);
         const uint32_t b0 = a0 + A_BYTES;
+        // K steps of 16 dims: landmarks in 128-byte swizzled boxes of 64
+        // dims (+32 B per step inside a box), q in 64-byte swizzled boxes of
+        // 32 dims
 #pragma unroll
-        for (int kb = 0; kb < KB; ++kb) {
-#pragma unroll
-          for (int ks = 0; ks < 2; ++ks) {
-            tc::mma_bf16(tmem + a * 16, tc::desc_k_sw64(a0 + kb * (kScTile * 64) + ks * 32, 512),
-                         tc::desc_k_sw64(b0 + kb * (16 * 64) + ks * 32, 512), idesc, (kb | ks) != 0);
-          }
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc::mma_bf16(tmem + a * 16, tc::desc_k_sw128(a0 + (kk >> 2) * (kScTile * 128) + (kk & 3) * 32, 1024),
+                       tc::desc_k_sw64(b0 + (kk >> 1) * (16 * 64) + (kk & 1) * 32, 512), idesc, kk != 0);
         tc::mma_commit(&empty[s]);
         tc::mma_commit(&tfull[a]);
       }
@@ -211,10 +211,10 @@ cudaError_t make_score_map(Ctx& c) {
   const cuuint64_t rows = static_cast<cuuint64_t>(c.p.b) * c.p.h_kv * c.n;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(c.p.d), rows};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(c.p.d) * 2};
-  const cuuint32_t box[2] = {32, kScTile};
+  const cuuint32_t box[2] = {64, kScTile};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(&c.mapL, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.L, dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   c.tc_score = true;

@@ -276,6 +276,14 @@ __device__ __forceinline__ uint64_t desc_k_sw64(uint32_t saddr, uint32_t sbo) {
          (static_cast<uint64_t>(4) << 61);
 }
 
+// The same for the 128-byte swizzle: rows of 128 bytes (64 bf16 of K), 8-row
+// groups `sbo` bytes apart (1024 for a dense tile); layout 2.
+__device__ __forceinline__ uint64_t desc_k_sw128(uint32_t saddr, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+
 // Shared-memory matrix descriptor of a K-major operand without swizzle: core
 // matrices of 8 rows x 16 bytes (128 contiguous bytes); `lbo` = byte stride
 // between core matrices along K, `sbo` = byte stride between 8-row groups
