@@ -118,49 +118,20 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part,
     }
   }
   tc::grid_dep_wait();   // the logits and partials of the score kernel
-  // log-sum-exp of each query head over the candidate chunks from the (max,
-  // sum of exp) partials of 32 landmarks (4 per 128-landmark score tile):
-  // nthr / 32 / G warps per head, each merging its share online, then one
-  // thread per head merging the warps'
-  {
-    const int wph = (nthr >> 5) / G;
-    const int g = warp / wph, wi = warp - g * wph;
-    float m = -INFINITY, z = 0.f;
-    if (g < G) {
-      const float2* pp = part + (static_cast<size_t>(pair) * G + g) * ntile * 4;
-      for (int t = wi * 32 + lane; t < 4 * ntile; t += wph * 32) {
-        const float2 v = __ldcg(pp + t);
-        if (v.y > 0.f) {
-          const float mn = fmaxf(m, v.x);
-          z = z * __expf(m - mn) + v.y * __expf(v.x - mn);
-          m = mn;
-        }
-      }
+  // log-sum-exp of each query head over the candidate chunks (4 partials
+  // of 32 landmarks per 128-landmark score tile): a warp per head
+  for (int g = warp; g < G; g += nthr / 32) {
+    const float2* pp = part + (static_cast<size_t>(pair) * G + g) * ntile * 4;
+    float m = -INFINITY;
+    for (int t = lane; t < 4 * ntile; t += 32) m = fmaxf(m, pp[t].x);
+    m = warp_max(m);
+    float z = 0.f;
+    for (int t = lane; t < 4 * ntile; t += 32) {
+      const float2 v = pp[t];
+      if (v.y > 0.f) z += v.y * __expf(v.x - m);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, m, o), z2 = __shfl_xor_sync(0xffffffffu, z, o);
-      const float mn = fmaxf(m, m2);
-      if (mn != -INFINITY) {
-        z = z * __expf(m - mn) + z2 * __expf(m2 - mn);
-        m = mn;
-      }
-    }
-    float2* wred = reinterpret_cast<float2*>(scratch);   // [G][wph]
-    if (lane == 0 && g < G) wred[g * wph + wi] = make_float2(m, z);
-    __syncthreads();
-    if (tid < G) {
-      float M = -INFINITY, Z = 0.f;
-      for (int w = 0; w < wph; ++w) {
-        const float2 v = wred[tid * wph + w];
-        const float mn = fmaxf(M, v.x);
-        if (mn != -INFINITY) {
-          Z = Z * __expf(M - mn) + v.y * __expf(v.x - mn);
-          M = mn;
-        }
-      }
-      lse[tid] = M + __logf(Z);
-    }
+    z = warp_sum(z);
+    if (lane == 0) lse[g] = m + __logf(z);
   }
   __syncthreads();
   // selection keys: S2 per chunk, 0 for outliers

@@ -44,8 +44,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
 k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUtensorMap mapQ,
            const uint32_t* __restrict__ mask, float* __restrict__ P, float2* __restrict__ part, int n,
            int ntile, int total_tiles, float scale, int* __restrict__ status) {
-  constexpr int KB = D / 32;                  // q boxes of 32 dims (64-byte swizzle)
-  constexpr int KA = D / 64;                  // landmark boxes of 64 dims (128-byte swizzle)
+  constexpr int KA = D / 64;                  // landmark and q boxes of 64 dims (128-byte swizzle)
   constexpr int A_BYTES = KA * kScTile * 128;
   constexpr int STAGE = sc_stage_bytes(D);
   extern __shared__ unsigned char smem_raw[];
@@ -108,8 +107,8 @@ k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUt
       unsigned char* st = stages + s * STAGE;
       if (lane < KA)
         tc::tma_load_2d(st + lane * (kScTile * 128), &mapL, &full[s], lane * 64, pair * n + ti * kScTile);
-      else if (lane < KA + KB)
-        tc::tma_load_3d(st + A_BYTES + (lane - KA) * (16 * 64), &mapQ, &full[s], (lane - KA) * 32, 0, pair);
+      else if (lane < 2 * KA)
+        tc::tma_load_3d(st + A_BYTES + (lane - KA) * (16 * 128), &mapQ, &full[s], (lane - KA) * 64, 0, pair);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -126,13 +125,12 @@ k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUt
         tc::fence_after();
         const uint32_t a0 = tc::smem_u32(stages + s * STAGE);
         const uint32_t b0 = a0 + A_BYTES;
-        // K steps of 16 dims: landmarks in 128-byte swizzled boxes of 64
-        // dims (+32 B per step inside a box), q in 64-byte swizzled boxes of
-        // 32 dims
+        // K steps of 16 dims: landmarks and q in 128-byte swizzled boxes of
+        // 64 dims (+32 B per step inside a box)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           tc::mma_bf16(tmem + a * 16, tc::desc_k_sw128(a0 + (kk >> 2) * (kScTile * 128) + (kk & 3) * 32, 1024),
-                       tc::desc_k_sw64(b0 + (kk >> 1) * (16 * 64) + (kk & 1) * 32, 512), idesc, kk != 0);
+                       tc::desc_k_sw128(b0 + (kk >> 2) * (16 * 128) + (kk & 3) * 32, 1024), idesc, kk != 0);
         tc::mma_commit(&empty[s]);
         tc::mma_commit(&tfull[a]);
       }
@@ -222,7 +220,7 @@ cudaError_t make_score_map(Ctx& c) {
 }
 
 // The queries live in the caller's buffer: a 3D view {d, G, b*h_kv} read in
-// boxes of 32 x 16 x 1, the rows past G being zero-filled.
+// 128-byte swizzled boxes of 64 x 16 x 1, the rows past G being zero-filled.
 cudaError_t encode_q_map(const Ctx& c, const void* q, CUtensorMap* map) {
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
@@ -231,10 +229,10 @@ cudaError_t encode_q_map(const Ctx& c, const void* q, CUtensorMap* map) {
                               static_cast<cuuint64_t>(c.p.b) * c.p.h_kv};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(c.p.d) * 2,
                                  static_cast<cuuint64_t>(c.p.d) * 2 * c.G};
-  const cuuint32_t box[3] = {32, 16, 1};
+  const cuuint32_t box[3] = {64, 16, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box,
-                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
