@@ -25,8 +25,10 @@
  *     call (prefill copies what it needs).
  *   - stream is a cudaStream_t passed as void* (NULL = the legacy default
  *     stream).  Work is enqueued on it in order; calls return before the GPU
- *     finishes unless stated otherwise.  The decode step also uses one
- *     library-owned side stream, joined back to `stream` before it returns.
+ *     finishes unless stated otherwise.  With bf16, d = 128 contexts the
+ *     decode step's kernels all run on `stream`, chained with programmatic
+ *     dependent launch; other contexts also use one library-owned side
+ *     stream, joined back to `stream` before the call returns.
  *   - Every entry point returns an skv_status; on failure
  *     shadowkv_last_error() (thread-local) describes the cause.  No entry point
  *     aborts the process, traps the GPU, or falls back to the CPU.
@@ -153,9 +155,11 @@ skv_status shadowkv_load_state(const shadowkv_params* p, const shadowkv_state_in
  * selects the top-k chunks per KV head (ties to the lower index), rebuilds
  * their keys as RoPE(Gather(A, I) B) at their token positions, takes their
  * values from the GPU chunk cache (hits of the previous step) or from pinned
- * host memory (misses, fetched on the side stream while the keys are
- * rebuilt), and writes softmax(q K^T / sqrt(d)) V over
- * [outliers; rebuilt chunks; local window].  Asynchronous on `stream`.
+ * host memory (misses, fetched while the keys are rebuilt), and writes
+ * softmax(q K^T / sqrt(d)) V over [outliers; rebuilt chunks; local window].
+ * The kernels read q in place through tensor maps: q must be 16-byte aligned
+ * (else SKV_ERR_INVALID_ARG before any work is enqueued) and must not change
+ * before the step has completed on `stream`.  Asynchronous on `stream`.
  */
 skv_status shadowkv_decode_step(shadowkv_ctx* ctx, const void* q, const void* k_new,
                                 const void* v_new, void* out, void* stream);

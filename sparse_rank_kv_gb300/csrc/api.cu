@@ -478,6 +478,8 @@ skv_status shadowkv_decode_step(shadowkv_ctx* h, const void* q, const void* k_ne
   if (!h) return fail(SKV_ERR_INVALID_ARG, "ctx is NULL");
   if (!q || !out) return fail(SKV_ERR_INVALID_ARG, "q and out must be non-NULL");
   if ((k_new == nullptr) != (v_new == nullptr)) return fail(SKV_ERR_INVALID_ARG, "k_new and v_new must both be given or both NULL");
+  if (reinterpret_cast<uintptr_t>(q) % 16)
+    return fail(SKV_ERR_INVALID_ARG, "q must be 16-byte aligned (it is read through tensor maps)");
   skv::Ctx& c = h->c;
   if (k_new && c.n_app >= c.p.max_new)
     return fail(SKV_ERR_STATE, "local window full: %d tokens appended (max_new)", c.n_app);

@@ -301,3 +301,24 @@ def test_steps_do_not_run_into_wait_limits():
         torch.cuda.synchronize()
         assert time.perf_counter() - t0 < 0.5, f"step {t} took {time.perf_counter() - t0:.2f} s"
     ctx.check()
+
+
+def test_misaligned_queries_are_rejected_before_any_work():
+    """q is read in place through tensor maps: a q that is not 16-byte aligned
+    is refused with an argument error and the context's state is untouched."""
+    cfg = SMALL.with_(steps=2, seed=63)
+    st = synth.make_state(cfg, device="cuda")
+    ctx = binding.load_state(binding.make_params(cfg), st)
+    out = torch.empty(cfg.b, cfg.h_q, cfg.d, dtype=torch.bfloat16, device="cuda")
+    q = st["q"][0].contiguous()
+    buf = torch.empty(q.numel() + 8, dtype=q.dtype, device="cuda")
+    qm = buf[1:1 + q.numel()].view_as(q)
+    qm.copy_(q)
+    before = ctx.stats()
+    with pytest.raises(binding.ShadowKVError) as ei:
+        ctx.decode_step(qm, st["k_new"][0], st["v_new"][0], out)
+    assert ei.value.code == 1
+    after = ctx.stats()
+    assert after.hits == before.hits and after.misses == before.misses and after.launches == before.launches
+    ctx.decode_step(q, st["k_new"][0], st["v_new"][0], out)
+    ctx.check()
