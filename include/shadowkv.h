@@ -234,7 +234,11 @@ skv_status shadowkv_attention_noalloc(const shadowkv_params* p, const void* q, c
 int shadowkv_num_kernels(void);
 const char* shadowkv_kernel_name(int id);
 /* With SKV_OPT_TIMING on: total milliseconds and launch count per kernel id
- * since the last reset (arrays of n entries).  Synchronizes. */
+ * since the last reset (arrays of n entries).  Synchronizes.  With K/V
+ * records (bf16, d = 128) the value fetch runs inside the "rebuild" launch,
+ * and "fetch" counts no launches.  The events recorded between launches
+ * remove the overlap between consecutive kernels, so the per-kernel times sum
+ * to more than a step takes with timing off. */
 skv_status shadowkv_kernel_times(shadowkv_ctx* ctx, double* ms, long long* launches, int n);
 skv_status shadowkv_reset_timers(shadowkv_ctx* ctx);
 

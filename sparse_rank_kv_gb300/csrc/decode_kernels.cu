@@ -4,8 +4,9 @@
 //             against the previous step's GPU-resident chunks, and the
 //             local-window append of the new token
 //   k_fetch   Gather(V_CPU, I) for the chunks that missed the cache, read
-//             zero-copy from pinned host memory on the side stream
-// (the attention kernel is in attn.cu, the key rebuild in rebuild.cu)
+//             zero-copy from pinned host memory on the side stream (row-major
+//             contexts; with K/V records the rebuild's launch does the fetch)
+// (the attention kernels are in attn*.cu, the key rebuild in rebuild.cu)
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"

@@ -17,9 +17,9 @@ namespace skv {
 enum KernelId {
   K_SCORE = 0,      // landmark scores P = q L^T / sqrt(d) and per-tile softmax stats
   K_SELECT,         // S2, top-k, cache set difference, local-window append
-  K_FETCH,          // value misses from pinned host memory into cache slots
-  K_REBUILD,        // RoPE(Gather(A, I) B)
-  K_ATTN,           // split-KV attention + last-block combine
+  K_FETCH,          // value misses from pinned host memory into cache slots (side stream)
+  K_REBUILD,        // RoPE(Gather(A, I) B); with K/V records also the value fetch
+  K_ATTN,           // attention over [outliers; rebuilt chunks; local window] and its merge
   K_CHUNKSTATS,     // prefill: RoPE, chunk means, min cosine
   K_OUTLIERS,       // prefill: ArgTopK(-min cos, o) + mask
   K_GATHER,         // prefill: outlier / local-window rows
