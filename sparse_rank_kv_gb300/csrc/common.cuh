@@ -604,19 +604,29 @@ __device__ __forceinline__ void block_topk(const uint32_t* keys, int n, int k, i
     if (tid == 0) *cnt_slot = 0;
     __syncthreads();
   }
-  // gather the survivors (keys >= T0, non-zero) while they fit in `vals`
-  for (int row = r0; row < r1; ++row) {
-    const int j = row * 32 + lane;
-    const uint32_t key = j < n ? keys[j] : 0u;
-    const bool keep = key != 0u && key >= T0;
-    const unsigned m = __ballot_sync(0xffffffffu, keep);
+  // gather the survivors (keys >= T0, non-zero) while they fit in `vals`:
+  // each warp counts its rows' survivors, reserves one range, then stores
+  {
+    int wcnt = 0;
+    for (int row = r0; row < r1; ++row) {
+      const int j = row * 32 + lane;
+      const uint32_t key = j < n ? keys[j] : 0u;
+      wcnt += __popc(__ballot_sync(0xffffffffu, key != 0u && key >= T0));
+    }
     int base = 0;
-    if (lane == 0 && m) base = atomicAdd(cnt_slot, __popc(m));
+    if (lane == 0 && wcnt) base = atomicAdd(cnt_slot, wcnt);
     base = __shfl_sync(0xffffffffu, base, 0);
-    const int pos = base + __popc(m & ((1u << lane) - 1u));
-    if (keep && pos < cap) {
-      vals[pos] = key;
-      vidx[pos] = j;
+    for (int row = r0; row < r1; ++row) {
+      const int j = row * 32 + lane;
+      const uint32_t key = j < n ? keys[j] : 0u;
+      const bool keep = key != 0u && key >= T0;
+      const unsigned m = __ballot_sync(0xffffffffu, keep);
+      const int pos = base + __popc(m & ((1u << lane) - 1u));
+      if (keep && pos < cap) {
+        vals[pos] = key;
+        vidx[pos] = j;
+      }
+      base += __popc(m);
     }
   }
   __syncthreads();
