@@ -51,10 +51,9 @@ __host__ __device__ constexpr int at_smem_bytes(int npairs) {
 
 // An item: its head, kind (0 outliers, 1 local window, 2 hit chunks, 3 missed
 // chunks), first token (0, 1) or first position in the head's slot list (2,
-// 3), tokens, slot of its partial among the head's items, and the head's
-// item count.
+// 3), tokens, and the slot of its partial among the head's items.
 struct AtItem {
-  int pair, seg, t0, cnt, li, ntot;
+  int pair, seg, t0, cnt, li;
 };
 
 template <int G>
@@ -85,7 +84,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
   int* s_task = reinterpret_cast<int*>(misc + 204);
   int* s_ndone = reinterpret_cast<int*>(misc + 208);
   int* s_done = reinterpret_cast<int*>(misc + 328);       // [kAtDone] heads of finished items
-  int* info = reinterpret_cast<int*>(misc + 256);         // [kAtStages][6] item descriptions
+  int* info = reinterpret_cast<int*>(misc + 256);         // [kAtStages][6]: head (-1: no more), tokens, partial slot
   float* red = reinterpret_cast<float*>(misc + 512);      // [2][4][8] maxima, then sums at +32
   int* s_p0 = reinterpret_cast<int*>(misc + kAtMisc);     // [npairs + 1] phase-0 item prefix
   int* s_p1 = s_p0 + npairs + 1;                          // [npairs + 1] phase-1 item prefix
@@ -207,7 +206,6 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
       t.cnt = min(cpi, k - t.t0) * c;
       t.li = s_p0[p + 1] - s_p0[p] + j;
     }
-    t.ntot = s_p0[t.pair + 1] - s_p0[t.pair] + s_p1[t.pair + 1] - s_p1[t.pair];
     return t;
   };
 
@@ -238,7 +236,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
       }
       const int st = it % kAtStages, use = it / kAtStages;
       const bool done = phase == 1 && x >= T1;
-      const AtItem t = done ? AtItem{-1, 0, 0, 0, 0, 0} : item_of(phase, x);
+      const AtItem t = done ? AtItem{-1, 0, 0, 0, 0} : item_of(phase, x);
       // cache slots of the item's chunks (lane = chunk), loaded before the wait
       const int nch = t.seg >= 2 ? t.cnt / c : 0;
       const int slot = lane < nch ? att_slot[static_cast<size_t>(t.pair) * k + t.t0 + lane] : 0;
@@ -278,7 +276,6 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
         inf[0] = t.pair;
         inf[1] = t.cnt;
         inf[2] = t.li;
-        inf[3] = t.ntot;
         tc::mbar_expect_tx(&full[st], static_cast<uint32_t>(groups * 4096 + kAtQBytes));
         tc::tma_load_4d(sR + kAtRec, &mapQ, &full[st], 0, 0, 0, t.pair);
         if (t.seg == 0)
