@@ -412,12 +412,19 @@ skv_status shadowkv_prefill(const shadowkv_params* p, const void* k_pre, const v
     parallel_memcpy(c.v_cpu, v, c.v_bytes);
     v_src = c.v_cpu_dev;
   } else {
-    e = cudaMemcpyAsync(c.v_cpu, v, c.v_bytes, cudaMemcpyDeviceToHost, st);
+    // the offload to pinned host memory (and its read pass) runs on the side
+    // stream beside the prefill kernels, which read the device copy of V
+    e = cudaEventRecord(c.ev_fork, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(c.side, c.ev_fork, 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(c.v_cpu, v, c.v_bytes, cudaMemcpyDeviceToHost, c.side);
+    if (e == cudaSuccess) e = skv::launch_read_host_v(c, c.side);
+    if (e == cudaSuccess) e = cudaEventRecord(c.ev_join, c.side);
   }
   if (e == cudaSuccess) e = skv::prefill_device(c, k_pre, v_src, st);
   if (e == cudaSuccess) e = skv::launch_tile_a(c, 1, st);
   if (e == cudaSuccess) e = skv::launch_pack_kv(c, st);
-  if (e == cudaSuccess) e = skv::launch_read_host_v(c, st);
+  if (e == cudaSuccess && v_on_host) e = skv::launch_read_host_v(c, st);
+  if (e == cudaSuccess && !v_on_host) e = cudaStreamWaitEvent(st, c.ev_join, 0);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) { s = cuda_fail(e, "prefill"); destroy(h); return s; }
   s = read_status(c);
