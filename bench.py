@@ -55,11 +55,22 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def hbm_bytes_per_step(cfg, E, n_loc):
-    """Algorithmic HBM bytes of one decode step: landmarks, gathered A rows, B,
-    outlier K/V, cached V of the selected chunks, local-window K/V."""
-    per_pair = (cfg.n * cfg.d + cfg.k * cfg.c * cfg.r + cfg.r * cfg.d
-                + 2 * cfg.o * cfg.c * cfg.d + cfg.k * cfg.c * cfg.d + 2 * n_loc * cfg.d)
+def hbm_bytes_per_step(cfg, E, n_loc, alpha=0.0, records=False):
+    """Algorithmic HBM bytes of one decode step.
+
+    Row-major contexts follow the pages' step: landmarks, A rows of every
+    selected chunk, B, outlier K/V, cached V of the selected chunks,
+    local-window K/V.  With K/V records (bf16, d = 128) a cache slot keeps its
+    chunk's rebuilt keys, so a step with hit rate `alpha` reads A rows of the
+    missed chunks only, reads the keys and values of every selected chunk,
+    and writes the missed chunks' rebuilt keys and fetched values."""
+    sel = cfg.k * cfg.c                       # selected tokens per (batch, KV head)
+    common = cfg.n * cfg.d + cfg.r * cfg.d + 2 * cfg.o * cfg.c * cfg.d + 2 * n_loc * cfg.d
+    if records:
+        miss = (1.0 - alpha) * sel
+        per_pair = common + miss * cfg.r + 2 * sel * cfg.d + 2 * miss * cfg.d
+    else:
+        per_pair = common + sel * cfg.r + sel * cfg.d
     return E * cfg.b * cfg.h_kv * per_pair
 
 
@@ -315,7 +326,8 @@ def run_ours(args, cfg):
     if rank == 0:
         hbm_gbs, peak_src = peaks()
         n_loc_avg = cfg.w + W + (K + 1) / 2.0
-        hbm = hbm_bytes_per_step(cfg, E, n_loc_avg)
+        records = cfg.dtype == "bf16" and cfg.d == 128 and cfg.c % 8 == 0 and 128 % cfg.c == 0
+        hbm = hbm_bytes_per_step(cfg, E, n_loc_avg, alpha, records)
         link = misses / K * cfg.c * cfg.d * E
         fetch_ms, fetch_n = kt["fetch"]
         fetch_in = "fetch launch"
