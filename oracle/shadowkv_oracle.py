@@ -43,7 +43,7 @@ import numpy as np
 
 __all__ = [
     "rope", "n_chunks", "chunk_landmarks", "chunk_min_cosine", "argtopk",
-    "svd_factors", "prefill", "OracleState", "OracleDecoder",
+    "svd_factors", "prefill", "attention", "OracleState", "OracleDecoder",
     "equivalent_bandwidth", "subspace_similarity", "hit_count",
 ]
 
@@ -189,6 +189,19 @@ def prefill(k_pre, v, c: int, r: int, o: int, w: int, theta: float) -> OracleSta
         V_cpu=np.asarray(v), min_cos=m)
 
 
+# --------------------------------------------------------------------------
+# Algorithm 2 step 4: attention over the concatenated keys and values.
+# --------------------------------------------------------------------------
+def attention(q, K, V) -> np.ndarray:
+    """softmax(q K^T / sqrt(d)) V for a group of queries sharing K and V
+    (reading R7).  q (..., G, d); K, V (..., T, d) -> (..., G, d)."""
+    q, K, V = _f64(q), _f64(K), _f64(V)
+    d = q.shape[-1]
+    logits = np.einsum("...gd,...td->...gt", q, K) / np.sqrt(d)
+    p = np.exp(logits - logits.max(axis=-1, keepdims=True))
+    return np.einsum("...gt,...td->...gd", p / p.sum(axis=-1, keepdims=True), V)
+
+
 @dataclass
 class StepResult:
     P: np.ndarray        # (b, h_q, n) q.L / sqrt(d); NaN at outlier chunks
@@ -266,11 +279,7 @@ class OracleDecoder:
                 Vs = _f64(st.V_cpu[bi, hi][r_])                           # step 3 (value)
                 Katt = np.concatenate([_f64(st.K_out[bi, hi]), Ks, K_loc[bi, hi]])
                 Vatt = np.concatenate([_f64(st.V_out[bi, hi]), Vs, V_loc[bi, hi]])
-                for g in range(G):
-                    qh = q[bi, hi * G + g]
-                    logits = Katt @ qh / np.sqrt(d)                       # reading R7
-                    p = np.exp(logits - logits.max())
-                    out[bi, hi * G + g] = (p / p.sum()) @ Vatt
+                out[bi, hi * G:(hi + 1) * G] = attention(q[bi, hi * G:(hi + 1) * G], Katt, Vatt)
                 if self.prev_sel is not None:
                     hits[bi, hi] = hit_count(self.prev_sel[bi, hi], sel[bi, hi])
         self.prev_sel = sel

@@ -310,3 +310,45 @@ def test_rebuilt_keys_equal_post_rope_keys_at_full_rank():
     for hi in range(h):
         rows = (res.sel[0, hi][:, None] * c + np.arange(c)).ravel()
         np.testing.assert_allclose(res.K_sparse[0, hi], K_rope[0, hi, rows], atol=1e-10)
+
+
+# ------------------------------------------------ attention (Alg. 2 step 4)
+def test_attention_equals_library_sdpa():
+    # an independent implementation: torch's scaled dot-product attention in
+    # float64, each query of the group against the shared keys and values
+    rng = np.random.default_rng(14)
+    q = rng.standard_normal((3, 4, 16)) * 3
+    K = rng.standard_normal((3, 37, 16))
+    V = rng.standard_normal((3, 37, 16))
+    got = O.attention(q, K, V)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q), torch.from_numpy(K), torch.from_numpy(V)).numpy()
+    np.testing.assert_allclose(got, ref, atol=1e-12)
+
+
+def test_attention_closed_forms():
+    rng = np.random.default_rng(15)
+    q = rng.standard_normal((2, 8))
+    V = rng.standard_normal((5, 8))
+    # one token: the output is its value, whatever the query
+    np.testing.assert_allclose(O.attention(q, rng.standard_normal((1, 8)), V[:1]), np.tile(V[:1], (2, 1)),
+                               atol=1e-15)
+    # equal keys: uniform weights, the output is the mean value
+    K = np.tile(rng.standard_normal((1, 8)), (5, 1))
+    np.testing.assert_allclose(O.attention(q, K, V), np.tile(V.mean(0), (2, 1)), atol=1e-14)
+    # a key with logit 8 ln 2 above the others (scale 1/sqrt(d)): weight 256 : 1
+    qv = np.zeros((1, 4))
+    qv[0, 0] = 2.0
+    K = np.zeros((3, 4))
+    K[1, 0] = 8 * np.log(2.0)
+    V = np.eye(3, 4)
+    np.testing.assert_allclose(O.attention(qv, K, V)[0, :3], np.array([1, 256, 1]) / 258.0, atol=1e-14)
+
+
+def test_attention_ignores_token_order():
+    rng = np.random.default_rng(16)
+    q = rng.standard_normal((4, 16))
+    K = rng.standard_normal((50, 16))
+    V = rng.standard_normal((50, 16))
+    perm = rng.permutation(50)
+    np.testing.assert_allclose(O.attention(q, K, V), O.attention(q, K[perm], V[perm]), atol=1e-13)
