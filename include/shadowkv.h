@@ -182,8 +182,10 @@ enum {
   SKV_OPT_TIMING = 1,       /* 1: time each kernel with CUDA events on its stream */
   SKV_OPT_SPLIT_TOKENS = 2, /* tokens per attention split (multiple of 32 in 32..256 whose K/V
                                rows fit in shared memory; default 128).  Setting it selects the
-                               classic split-KV attention kernel; by default bf16 contexts use
-                               the pipelined (TMA-fed, 64-token items) kernel */
+                               classic split-KV attention kernel.  By default bf16 contexts
+                               with d = 128 and c a multiple of 8 dividing 128 use the
+                               tensor-core attention over K/V records; other bf16 contexts
+                               use the pipelined (TMA-fed, 64-token items) kernel */
   SKV_OPT_CUDA_CORES = 3    /* 1: compute the landmark scores and rebuild the keys with the
                                CUDA-core kernels even where the tensor-core (tcgen05) kernels
                                apply (bf16; for the rebuild also c a multiple of 8 dividing 128
@@ -217,8 +219,13 @@ skv_status shadowkv_check(shadowkv_ctx* ctx);
  *   K, V     : device, b x h_kv x n_tokens x d, post-RoPE keys and values.
  *   out      : device, b x h_q x d; out = softmax(q K^T / sqrt(d)) V, query
  *              head g reading KV head g / G.
- * Needs b * h_q * ceil(n_tokens / 128) * (d + 2) * 4 bytes of partials plus
- * 256 bytes of tickets; larger problems return SKV_ERR_UNSUPPORTED.
+ * K and V must be 16-byte aligned (their rows are copied 16 bytes at a time)
+ * and q and out aligned to their element size; otherwise SKV_ERR_INVALID_ARG
+ * is returned before anything is enqueued.
+ * Needs P = b * h_q * ceil(n_tokens / 128) * (d + 2) * 4 bytes of partials
+ * and T = b * h_kv * 4 bytes of tickets, each rounded up to 256 bytes; when
+ * P + T exceeds SKV_NOALLOC_SCRATCH_BYTES the call returns
+ * SKV_ERR_UNSUPPORTED.
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture.  Every call shares the one array and clears the

@@ -342,8 +342,9 @@ cudaError_t launch_attn(Ctx& c, const void* q, void* out, int n_loc, cudaStream_
 }  // namespace skv
 
 // ============================================= attention without allocation
-// Scratch of shadowkv_attention_noalloc: split partials, then 256 bytes of
-// tickets.  One copy per device, alive until the process exits.
+// Scratch of shadowkv_attention_noalloc: the split partials, then (from the
+// next 256-byte boundary) one completion ticket per (batch, KV head).  One
+// copy per device, alive until the process exits.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SKV_NOALLOC_SCRATCH_BYTES];
 
 namespace {
@@ -415,17 +416,25 @@ extern "C" skv_status shadowkv_attention_noalloc(const shadowkv_params* p, const
   if (p->d != 64 && p->d != 128) return set_error(SKV_ERR_UNSUPPORTED, "d must be 64 or 128");
   if (p->dtype != SKV_DTYPE_F32 && p->dtype != SKV_DTYPE_BF16)
     return set_error(SKV_ERR_INVALID_ARG, "bad dtype");
+  // K and V rows are copied to shared memory 16 bytes at a time; q and out
+  // are read and written element by element
+  const size_t E = p->dtype == SKV_DTYPE_BF16 ? 2 : 4;
+  if (reinterpret_cast<uintptr_t>(K) % 16 || reinterpret_cast<uintptr_t>(V) % 16)
+    return set_error(SKV_ERR_INVALID_ARG, "K and V must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(q) % E || reinterpret_cast<uintptr_t>(out) % E)
+    return set_error(SKV_ERR_INVALID_ARG, "q and out must be aligned to their element size");
   if (n_tokens < 1) return set_error(SKV_ERR_INVALID_ARG, "n_tokens must be >= 1");
   const int nsplit = (n_tokens + 127) / 128;
   const size_t part_bytes = static_cast<size_t>(p->b) * p->h_q * nsplit * (p->d + 2) * sizeof(float);
   const size_t ticket_bytes = static_cast<size_t>(p->b) * p->h_kv * sizeof(int32_t);
-  const size_t part_room = (static_cast<size_t>(SKV_NOALLOC_SCRATCH_BYTES) - 256) & ~static_cast<size_t>(255);
-  if (part_bytes > part_room || ticket_bytes > 256) {
+  const size_t part_room = (part_bytes + 255) & ~static_cast<size_t>(255);
+  const size_t ticket_room = (ticket_bytes + 255) & ~static_cast<size_t>(255);
+  if (part_room + ticket_room > static_cast<size_t>(SKV_NOALLOC_SCRATCH_BYTES)) {
     char msg[200];
     snprintf(msg, sizeof(msg),
              "attention_noalloc needs %zu bytes of partials and %zu of tickets; the static scratch "
-             "holds %zu and 256",
-             part_bytes, ticket_bytes, part_room);
+             "holds %zu in all",
+             part_room, ticket_room, static_cast<size_t>(SKV_NOALLOC_SCRATCH_BYTES));
     return set_error(SKV_ERR_UNSUPPORTED, msg);
   }
   void* base = nullptr;

@@ -96,3 +96,22 @@ def test_kernel_names(lib):
     names = binding.kernel_names()
     assert names[:5] == ["score", "select", "fetch", "rebuild", "attention"]
     assert len(set(names)) == len(names)
+
+
+def test_noalloc_alignment_is_checked_on_the_host(lib):
+    """The no-alloc attention refuses K/V that are not 16-byte aligned, and q
+    or out not aligned to their element size, before any CUDA call (the
+    pointers here are never dereferenced: n_tokens = 0 would be refused next)."""
+    p = binding.make_params(CONFIGS["llama_b1_s32k"])
+    ok, k_bad, q_bad = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x10008), ctypes.c_void_p(0x10001)
+    f = lib.shadowkv_attention_noalloc
+    assert f(ctypes.byref(p), ok, k_bad, ok, 0, ok, None) == 1
+    assert "16-byte aligned" in lib.shadowkv_last_error().decode()
+    assert f(ctypes.byref(p), ok, ok, k_bad, 0, ok, None) == 1
+    assert "16-byte aligned" in lib.shadowkv_last_error().decode()
+    assert f(ctypes.byref(p), q_bad, ok, ok, 0, ok, None) == 1
+    assert "element size" in lib.shadowkv_last_error().decode()
+    assert f(ctypes.byref(p), ok, ok, ok, 0, q_bad, None) == 1
+    assert "element size" in lib.shadowkv_last_error().decode()
+    assert f(ctypes.byref(p), ok, ok, ok, 0, ok, None) == 1
+    assert "n_tokens" in lib.shadowkv_last_error().decode()

@@ -3,15 +3,18 @@
 Callers that cannot allocate device memory -- an engine that gives all of it
 to its own pool at start-up, or a decode loop recorded into a CUDA graph --
 run the split-KV attention on keys and values they already hold; the
-library's scratch for the split partials is a static device array.  This file
-is collected last on purpose, so that a failure here does not hide the other
-GPU tests; it must also pass alone in a fresh process.
+library's scratch for the split partials and tickets is a static device
+array.  This file is collected last on purpose, so that a failure here does
+not hide the other GPU tests; it must also pass alone in a fresh process.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
 
-from helpers import TOL, head_errors
+from helpers import TOL, head_errors, np64
+from oracle import shadowkv_oracle as O
 from sparse_rank_kv_gb300 import binding, build, synth
 from sparse_rank_kv_gb300.synth import CONFIGS
 
@@ -48,12 +51,16 @@ def _step_inputs(ctx, cfg, n_loc):
     return K, V
 
 
-def test_noalloc_attention_matches_decode_step_twice():
+def test_noalloc_attention_matches_decode_step_and_oracle_twice():
+    """Two calls in a row (they share the static scratch and its tickets):
+    each output matches the decode step's attention over the same keys and
+    values, and the oracle's softmax(q K^T / sqrt(d)) V on them."""
     cfg = CFG
     st = synth.make_state(cfg, device="cuda")
     p = binding.make_params(cfg)
     ctx = binding.load_state(p, st)
-    for t in range(2):          # two calls in a row share the static scratch
+    G = cfg.h_q // cfg.h_kv
+    for t in range(2):
         q = st["q"][t].contiguous()
         ref = torch.empty(cfg.b, cfg.h_q, cfg.d, dtype=torch.bfloat16, device="cuda")
         ctx.decode_step(q, st["k_new"][t], st["v_new"][t], ref)
@@ -62,21 +69,39 @@ def test_noalloc_attention_matches_decode_step_twice():
         got = torch.empty_like(ref)
         binding.attention_noalloc(p, q, K, V, got)
         torch.cuda.synchronize()
-        err = head_errors(got.float().cpu().numpy().astype(np.float64),
-                          ref.float().cpu().numpy().astype(np.float64))
-        assert err.max() <= TOL["bf16"], f"call {t}: {err.max():.3g}"
+        err = head_errors(np64(got), np64(ref))
+        assert err.max() <= TOL["bf16"], f"call {t}: {err.max():.3g} against the decode step"
+        orc = O.attention(np64(q).reshape(cfg.b, cfg.h_kv, G, cfg.d), np64(K), np64(V))
+        err = head_errors(np64(got), orc.reshape(cfg.b, cfg.h_q, cfg.d))
+        assert err.max() <= TOL["bf16"], f"call {t}: {err.max():.3g} against the oracle"
     ctx.check()
 
 
 def test_noalloc_rejects_oversized_problems():
     p = binding.make_params(CFG.with_(b=64, h_q=64, h_kv=8))
     q = torch.empty(1, device="cuda")
+    ptr = ctypes.c_void_p(q.data_ptr())
+    rc = binding.lib().shadowkv_attention_noalloc(ctypes.byref(p), ptr, ptr, ptr, 1 << 20, ptr, None)
     with pytest.raises(binding.ShadowKVError) as ei:
-        binding.lib()  # loaded
-        import ctypes
-        rc = binding.lib().shadowkv_attention_noalloc(ctypes.byref(p), ctypes.c_void_p(q.data_ptr()),
-                                                      ctypes.c_void_p(q.data_ptr()),
-                                                      ctypes.c_void_p(q.data_ptr()), 1 << 20,
-                                                      ctypes.c_void_p(q.data_ptr()), None)
         binding._check(rc)
     assert ei.value.code == 7 and "static scratch" in str(ei.value)
+
+
+def test_noalloc_rejects_misaligned_keys_before_any_work():
+    """K and V are copied 16 bytes at a time: an offset view is refused on
+    the host.  n_tokens = 0 would be refused too, after the alignment check,
+    so no kernel can run here whichever check answers."""
+    p = binding.make_params(CFG)
+    buf = torch.zeros(4096, dtype=torch.bfloat16, device="cuda")
+    good = ctypes.c_void_p(buf.data_ptr())
+    bad = ctypes.c_void_p(buf.data_ptr() + 2)
+    for K, V in ((bad, good), (good, bad)):
+        rc = binding.lib().shadowkv_attention_noalloc(ctypes.byref(p), good, K, V, 0, good, None)
+        with pytest.raises(binding.ShadowKVError) as ei:
+            binding._check(rc)
+        assert ei.value.code == 1 and "16-byte aligned" in str(ei.value)
+    odd = ctypes.c_void_p(buf.data_ptr() + 1)
+    rc = binding.lib().shadowkv_attention_noalloc(ctypes.byref(p), odd, good, good, 0, good, None)
+    with pytest.raises(binding.ShadowKVError) as ei:
+        binding._check(rc)
+    assert ei.value.code == 1 and "element size" in str(ei.value)
