@@ -33,6 +33,10 @@ reason, in the design notes of the repository):
       step's selection; hits_t = |I_t  intersect  I_{t-1}|; step 0 has none.
   R10 The equivalent-bandwidth example leaves the hit rate unprinted;
       alpha = 0.6 (the page's "about 60%") reproduces 7.2 TB/s.
+  R11 K_sparse (Algorithm 2 step 3) is a tensor of the workload's element
+      type, like A, B, L, the outliers, the local window and V: its exact
+      value RoPE(Gather(A, I) B) is rounded to that type (round to nearest,
+      ties to even) before the attention.  key_dtype="f64" keeps it exact.
 """
 from __future__ import annotations
 
@@ -44,7 +48,7 @@ import numpy as np
 __all__ = [
     "rope", "n_chunks", "chunk_landmarks", "chunk_min_cosine", "argtopk",
     "svd_factors", "prefill", "attention", "OracleState", "OracleDecoder",
-    "equivalent_bandwidth", "subspace_similarity", "hit_count",
+    "equivalent_bandwidth", "subspace_similarity", "hit_count", "store",
 ]
 
 
@@ -190,6 +194,27 @@ def prefill(k_pre, v, c: int, r: int, o: int, w: int, theta: float) -> OracleSta
 
 
 # --------------------------------------------------------------------------
+# Element types of materialised tensors (reading R11).
+# --------------------------------------------------------------------------
+def store(x, dtype: str) -> np.ndarray:
+    """x rounded to the element type `dtype` ("f64", "f32" or "bf16"), returned
+    as float64.  bf16 keeps the upper 16 bits of the float32 value, rounded
+    to nearest with ties to even (float64 -> float32 first)."""
+    x = _f64(x)
+    if dtype == "f64":
+        return x
+    x32 = np.ascontiguousarray(x.astype(np.float32))
+    if dtype == "f32":
+        return x32.astype(np.float64)
+    if dtype != "bf16":
+        raise ValueError(dtype)
+    u = x32.view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    u = ((u + 0x7FFF + lsb) >> 16) << 16
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+# --------------------------------------------------------------------------
 # Algorithm 2 step 4: attention over the concatenated keys and values.
 # --------------------------------------------------------------------------
 def attention(q, K, V) -> np.ndarray:
@@ -219,6 +244,7 @@ class OracleDecoder:
     h_q: int
     k: int
     group_reduce: str = "max"
+    key_dtype: str = "f64"          # element type of K_sparse (reading R11)
     t: int = 0
     prev_sel: Optional[np.ndarray] = None
     app_K: list = field(default_factory=list)
@@ -274,7 +300,7 @@ class OracleDecoder:
             for hi in range(h):
                 r_ = rows[bi, hi]
                 Ks = _f64(A[bi][r_]) @ _f64(st.B[bi, hi])                 # step 3 (key)
-                Ks = rope(Ks, r_, st.theta)                               # step 4 RoPE
+                Ks = store(rope(Ks, r_, st.theta), self.key_dtype)        # step 4 RoPE
                 K_sparse[bi, hi] = Ks
                 Vs = _f64(st.V_cpu[bi, hi][r_])                           # step 3 (value)
                 Katt = np.concatenate([_f64(st.K_out[bi, hi]), Ks, K_loc[bi, hi]])

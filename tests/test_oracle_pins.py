@@ -352,3 +352,32 @@ def test_attention_ignores_token_order():
     V = rng.standard_normal((50, 16))
     perm = rng.permutation(50)
     np.testing.assert_allclose(O.attention(q, K, V), O.attention(q, K[perm], V[perm]), atol=1e-13)
+
+
+# ------------------------------------------- element types (reading R11)
+def test_store_bf16_matches_library_conversion_and_rounds_ties_to_even():
+    rng = np.random.default_rng(17)
+    x = (rng.standard_normal(20000) * np.exp(rng.uniform(-20, 20, 20000))).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.store(x, "bf16"), ref)
+    # bf16 keeps 8 significant bits: 1 + k 2^-7 is exact; halfway cases go to even k
+    assert O.store(1.0 + 2.0 ** -7, "bf16") == 1.0 + 2.0 ** -7
+    assert O.store(1.0 + 2.0 ** -8, "bf16") == 1.0
+    assert O.store(1.0 + 3 * 2.0 ** -8, "bf16") == 1.0 + 2.0 ** -6
+    assert O.store(-(1.0 + 3 * 2.0 ** -8), "bf16") == -(1.0 + 2.0 ** -6)
+    assert O.store(1.0 + 2.0 ** -30, "f32") == 1.0 and O.store(1.0 + 2.0 ** -30, "f64") == 1.0 + 2.0 ** -30
+
+
+def test_rebuilt_keys_are_stored_in_the_key_type():
+    rng = np.random.default_rng(18)
+    b, h, d, c, w, o, k = 1, 2, 8, 2, 4, 1, 3
+    n = 8
+    s = n * c + w
+    st = O.prefill(rng.standard_normal((b, h, s, d)), rng.standard_normal((b, h, s, d)), c=c, r=4, o=o, w=w,
+                   theta=1e4)
+    q = rng.standard_normal((b, h, d))
+    exact = O.OracleDecoder(st, h_q=h, k=k).step(q)
+    rounded = O.OracleDecoder(st, h_q=h, k=k, key_dtype="bf16").step(q)
+    np.testing.assert_array_equal(rounded.K_sparse, O.store(exact.K_sparse, "bf16"))
+    assert np.array_equal(rounded.sel, exact.sel)
+    assert np.abs(rounded.out - exact.out).max() < 0.05 * np.abs(exact.out).max()
