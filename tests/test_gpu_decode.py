@@ -48,7 +48,8 @@ def run_parity(cfg, steps=None, group="max", cache=True, bsel=None, rows=True, a
     if split:
         ctx.set_option(binding.OPT_SPLIT_TOKENS, split)
     sl = slice(None) if bsel is None else slice(bsel, bsel + 1)
-    dec = O.OracleDecoder(oracle_state(st, cfg, bsel), h_q=cfg.h_q, k=cfg.k, group_reduce=group)
+    dec = O.OracleDecoder(oracle_state(st, cfg, bsel), h_q=cfg.h_q, k=cfg.k, group_reduce=group,
+                          key_dtype=cfg.dtype)
     b, h, hq, d, k, c, n = cfg.b, cfg.h_kv, cfg.h_q, cfg.d, cfg.k, cfg.c, cfg.n
     dt = synth.torch_dtype(cfg.dtype)
     T = cfg.steps if steps is None else steps

@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import TOL, check_selection, head_errors, np64
+from helpers import TOL, check_selection, ey_bound, head_errors, np64
 from oracle import shadowkv_oracle as O
 from sparse_rank_kv_gb300 import binding, build, synth
 from sparse_rank_kv_gb300.synth import CONFIGS
@@ -70,26 +70,8 @@ def check_stats_and_gathers(cfg, ctx, inp, ost):
     assert np.array_equal(vcpu, V), "pinned host copy of V"
 
 
-def ey_bound(cfg):
-    """Allowed err^2 / opt^2 of the rank-r factors.
-
-    Gap case (true rank >= r): the top-r subspace is well separated and the
-    factors must be Eckart-Young optimal to 1%.  Flat noise floor (true rank
-    R < r): the last m = r - R directions lie in an isotropic noise floor whose
-    eigenvalues spread up to the Marchenko-Pastur edge sigma^2 (1 + sqrt(D/s))^2;
-    the factors must do no worse than m arbitrary noise directions would, i.e.
-    err^2 <= opt^2 (1 + m ((1 + sqrt(D/s))^2 - 1) / (D - r)).
-    """
-    D = cfg.h_kv * cfg.d
-    m = cfg.r - cfg.rank_true
-    if m <= 0:
-        return 1.01
-    g = (1.0 + np.sqrt(D / cfg.s)) ** 2 - 1.0
-    return 1.0 + m * g / (D - cfg.r)
-
-
 def factor_errors(cfg, ctx, inp):
-    """Per sequence: (err_basis^2, err_stored^2, opt^2, |M|^2) where err_basis is
+    """Per sequence: (err_basis^2, err_stored^2, opt^2, |M|^2, sigma^2) where err_basis is
     |M - M X^T X| for the GPU's fp32 orthonormal basis X (the SVD's own
     quality), err_stored is |M - A B| for the stored factors, and opt^2 is the
     Eckart-Young optimum sum_{i>r} sigma_i^2."""
@@ -105,7 +87,7 @@ def factor_errors(cfg, ctx, inp):
         err_basis = float(((M - (M @ X[bi].T) @ X[bi]) ** 2).sum())
         err_stored = float(((M - A[bi] @ B) ** 2).sum())
         sig = np.linalg.svd(M.numpy(), compute_uv=False)
-        out.append((err_basis, err_stored, float(np.sum(sig[r:] ** 2)), float(np.sum(sig ** 2))))
+        out.append((err_basis, err_stored, float(np.sum(sig[r:] ** 2)), float(np.sum(sig ** 2)), sig ** 2))
     return out
 
 
@@ -113,10 +95,10 @@ def check_factors(cfg, ctx, inp, bound=None):
     """Eckart-Young on the fp32 basis; the stored factors may add at most the
     rounding of A and B to the storage type: |M - A B| <= |M - M X^T X| + 3u|M|
     (u = 2^-8 for bf16, 2^-24 for fp32)."""
-    bound = ey_bound(cfg) if bound is None else bound
     u = 2.0 ** -8 if cfg.dtype == "bf16" else 2.0 ** -24
-    for eb, es, opt, tot in factor_errors(cfg, ctx, inp):
-        assert eb <= bound * opt + 1e-9 * tot, ("basis", eb / opt, bound)
+    for eb, es, opt, tot, lam in factor_errors(cfg, ctx, inp):
+        bd = ey_bound(cfg, lam) if bound is None else bound
+        assert eb <= bd * opt + 1e-9 * tot, ("basis", eb / opt, bd)
         assert np.sqrt(es) <= np.sqrt(eb) + 3 * u * np.sqrt(tot), ("stored", es / opt)
 
 
@@ -161,7 +143,7 @@ def test_exact_low_rank_is_reconstructed_to_fp32_roundoff():
     cfg = CONFIGS["tiny_f32_s1k"].with_(r=24, rank_true=24, seed=53)
     inp = synth.make_inputs(cfg, device="cuda", noise=0.0)
     ctx = gpu_prefill(cfg, inp)
-    for eb, es, _, tot in factor_errors(cfg, ctx, inp):
+    for eb, es, _, tot, _ in factor_errors(cfg, ctx, inp):
         assert np.sqrt(es / tot) <= 1e-5 and np.sqrt(eb / tot) <= 1e-5
 
 
