@@ -115,8 +115,9 @@ skv_status shadowkv_footprint(const shadowkv_params* p, size_t* device_bytes,
  * keys of each sequence viewed as an s x (h_kv d) matrix, the post-RoPE keys
  * and values of the outlier chunks and of the local window, and copies V to
  * library-owned pinned host memory.  On success *out owns everything; k_pre
- * and v may be freed once `stream` has passed the call (the call synchronizes
- * `stream` before returning when v is on the host).
+ * and v may be freed once the call returns (it synchronizes `stream`).  The
+ * prefill's kernels are timed with CUDA events whatever SKV_OPT_TIMING says;
+ * shadowkv_kernel_times reports them until shadowkv_reset_timers.
  */
 skv_status shadowkv_prefill(const shadowkv_params* p, const void* k_pre, const void* v,
                             int v_on_host, void* stream, shadowkv_ctx** out);
@@ -196,6 +197,20 @@ skv_status shadowkv_set_option(shadowkv_ctx* ctx, int option, long long value);
 
 /* Synchronizes the context's streams and reads the cumulative counters. */
 skv_status shadowkv_get_stats(shadowkv_ctx* ctx, shadowkv_stats* out);
+
+/* Which storage layout and kernels the context uses; they follow from the
+ * parameters (and SKV_OPT_CUDA_CORES / SKV_OPT_SPLIT_TOKENS).  Host-only. */
+typedef struct shadowkv_layout {
+  int kv_records;       /* keys and values of every 8-token group in one 4 KB record;
+                           cache slots keep their rebuilt keys, so a step rebuilds
+                           only the chunks it fetches */
+  int a_tiled;          /* A's chunked region in 8-token core-matrix groups */
+  int tc_score;         /* landmark scores on the tensor cores (tcgen05) */
+  int tc_rebuild;       /* key rebuild on the tensor cores */
+  int tc_attention;     /* attention on the tensor cores over K/V records */
+  int fetch_in_rebuild; /* value fetch runs as CTAs of the rebuild launch (one stream) */
+} shadowkv_layout;
+skv_status shadowkv_get_layout(const shadowkv_ctx* ctx, shadowkv_layout* out);
 
 /* Synchronizes and reads the device status word (kernel bounds checks);
  * SKV_ERR_DEVICE_CHECK if any kernel recorded a violation. */

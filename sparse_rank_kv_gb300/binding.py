@@ -56,6 +56,12 @@ class StateIn(ctypes.Structure):
                 ("V_loc", ctypes.c_void_p), ("V", ctypes.c_void_p), ("v_on_host", ctypes.c_int)]
 
 
+class Layout(ctypes.Structure):
+    _fields_ = [("kv_records", ctypes.c_int), ("a_tiled", ctypes.c_int), ("tc_score", ctypes.c_int),
+                ("tc_rebuild", ctypes.c_int), ("tc_attention", ctypes.c_int),
+                ("fetch_in_rebuild", ctypes.c_int)]
+
+
 class Stats(ctypes.Structure):
     _fields_ = [("steps", ctypes.c_longlong), ("hits", ctypes.c_longlong),
                 ("misses", ctypes.c_longlong), ("link_bytes", ctypes.c_longlong),
@@ -87,6 +93,7 @@ def lib() -> ctypes.CDLL:
             "shadowkv_set_option": (I, [V, I, ctypes.c_longlong]),
             "shadowkv_get_stats": (I, [V, P(Stats)]),
             "shadowkv_check": (I, [V]),
+            "shadowkv_get_layout": (I, [V, P(Layout)]),
             "shadowkv_num_kernels": (I, []),
             "shadowkv_kernel_name": (ctypes.c_char_p, [I]),
             "shadowkv_kernel_times": (I, [V, P(ctypes.c_double), P(ctypes.c_longlong), I]),
@@ -193,6 +200,11 @@ class Context:
 
     def check(self):
         _check(lib().shadowkv_check(self._h))
+
+    def layout(self) -> dict:
+        lay = Layout()
+        _check(lib().shadowkv_get_layout(self._h, ctypes.byref(lay)))
+        return {name: bool(getattr(lay, name)) for name, _ in Layout._fields_}
 
     def kernel_times(self):
         n = num_kernels()

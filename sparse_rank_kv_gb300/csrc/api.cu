@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -65,7 +66,7 @@ skv_status cuda_fail(cudaError_t e, const char* what) {
 
 const char* kKernelNames[skv::K_NUM] = {
     "score", "select", "fetch", "rebuild", "attention", "chunkstats",
-    "outliers", "gather", "svd_mx", "svd_ztm", "orth", "misc"};
+    "outliers", "gather", "svd_gram", "svd_iter", "orth", "misc", "svd_a"};
 
 constexpr size_t kAlign = 256;
 size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -186,6 +187,40 @@ void parallel_memcpy(void* dst, const void* src, size_t bytes) {
   for (auto& x : th) x.join();
 }
 
+// Pinned, device-mapped host memory for V: an aligned allocation whose pages
+// several threads touch first, then registered with the driver (mapped,
+// portable).  Registering touched pages is far cheaper than cudaHostAlloc
+// of the same size, which faults and pins every page on one thread.
+cudaError_t pinned_alloc(void** out, size_t bytes) {
+  *out = nullptr;
+  const size_t align = size_t(2) << 20;
+  const size_t n = (bytes + align - 1) / align * align;
+  void* p = std::aligned_alloc(align, n);
+  if (!p) return cudaErrorMemoryAllocation;
+  const unsigned nt = std::max(1u, std::min(16u, std::thread::hardware_concurrency()));
+  std::vector<std::thread> th;
+  for (unsigned t = 0; t < nt; ++t)
+    th.emplace_back([=] {
+      const size_t per = (n / nt + 4095) / 4096 * 4096;
+      const size_t a = std::min(n, per * t), b = std::min(n, a + per);
+      if (a < b) std::memset(static_cast<char*>(p) + a, 0, b - a);
+    });
+  for (auto& x : th) x.join();
+  cudaError_t e = cudaHostRegister(p, n, cudaHostRegisterMapped | cudaHostRegisterPortable);
+  if (e != cudaSuccess) {
+    std::free(p);
+    return e;
+  }
+  *out = p;
+  return cudaSuccess;
+}
+
+void pinned_free(void* p) {
+  if (!p) return;
+  cudaHostUnregister(p);
+  std::free(p);
+}
+
 void destroy(shadowkv_ctx* h) {
   if (!h) return;
   skv::Ctx& c = h->c;
@@ -198,7 +233,7 @@ void destroy(shadowkv_ctx* h) {
   if (c.ev_join) cudaEventDestroy(c.ev_join);
   if (c.side) cudaStreamDestroy(c.side);
   if (c.arena) cudaFree(c.arena);
-  if (c.v_cpu) cudaFreeHost(c.v_cpu);
+  pinned_free(c.v_cpu);
   delete h;
 }
 
@@ -282,8 +317,8 @@ skv_status create(const shadowkv_params* p, cudaStream_t st, shadowkv_ctx** out)
 
   // pinned, mapped host copy of V
   c.v_bytes = static_cast<size_t>(p->b) * p->h_kv * p->s * p->d * c.E;
-  e = cudaHostAlloc(&c.v_cpu, c.v_bytes, cudaHostAllocMapped | cudaHostAllocPortable);
-  if (e != cudaSuccess) { c.v_cpu = nullptr; return bail(cuda_fail(e, "cudaHostAlloc(V)")); }
+  e = pinned_alloc(&c.v_cpu, c.v_bytes);
+  if (e != cudaSuccess) return bail(cuda_fail(e, "pinned host memory for V"));
   e = cudaHostGetDevicePointer(&c.v_cpu_dev, c.v_cpu, 0);
   if (e != cudaSuccess) return bail(cuda_fail(e, "cudaHostGetDevicePointer(V)"));
 
@@ -406,6 +441,9 @@ skv_status shadowkv_prefill(const shadowkv_params* p, const void* k_pre, const v
   s = create(p, st, &h);
   if (s != SKV_OK) return s;
   skv::Ctx& c = h->c;
+  // the prefill's kernels are always timed (CUDA events on their streams);
+  // shadowkv_kernel_times reports them until the next reset
+  c.timing_on = true;
   const void* v_src = v;
   cudaError_t e = cudaSuccess;
   if (v_on_host) {
@@ -426,6 +464,7 @@ skv_status shadowkv_prefill(const shadowkv_params* p, const void* k_pre, const v
   if (e == cudaSuccess && v_on_host) e = skv::launch_read_host_v(c, st);
   if (e == cudaSuccess && !v_on_host) e = cudaStreamWaitEvent(st, c.ev_join, 0);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  c.timing_on = false;
   if (e != cudaSuccess) { s = cuda_fail(e, "prefill"); destroy(h); return s; }
   s = read_status(c);
   if (s != SKV_OK) { destroy(h); return s; }
@@ -569,6 +608,18 @@ skv_status shadowkv_get_stats(shadowkv_ctx* h, shadowkv_stats* out) {
   out->misses = static_cast<long long>(cnt[1]);
   out->link_bytes = out->misses * static_cast<long long>(c.p.c) * c.p.d * c.E;
   out->launches = c.launches;
+  return SKV_OK;
+}
+
+skv_status shadowkv_get_layout(const shadowkv_ctx* h, shadowkv_layout* out) {
+  if (!h || !out) return fail(SKV_ERR_INVALID_ARG, "NULL argument");
+  const skv::Ctx& c = h->c;
+  out->kv_records = c.kv_rec ? 1 : 0;
+  out->a_tiled = c.a_tiled ? 1 : 0;
+  out->tc_score = c.tc_score && !c.force_simt ? 1 : 0;
+  out->tc_rebuild = c.tc_rebuild && !c.force_simt ? 1 : 0;
+  out->tc_attention = c.kv_rec && !c.force_simt && !c.split_set ? 1 : 0;
+  out->fetch_in_rebuild = skv::rebuild_fetches(c) ? 1 : 0;
   return SKV_OK;
 }
 

@@ -17,6 +17,7 @@ enum : int {
   DEV_BAD_OUTLIER = 3,
   DEV_BAD_COUNT = 4,
   DEV_TIMEOUT = 5,      // a bounded mbarrier wait gave up
+  DEV_NUMERIC = 6,      // the SVD's orthonormalisation met a non-positive pivot
 };
 
 // Nanoseconds a bounded mbarrier wait lasts before a kernel gives up and

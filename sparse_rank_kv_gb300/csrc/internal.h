@@ -23,10 +23,11 @@ enum KernelId {
   K_CHUNKSTATS,     // prefill: RoPE, chunk means, min cosine
   K_OUTLIERS,       // prefill: ArgTopK(-min cos, o) + mask
   K_GATHER,         // prefill: outlier / local-window rows
-  K_GRAM,           // prefill: M X^T products (range and A)
-  K_GEMM,           // prefill: (M X^T)^T M split-K partials
-  K_ORTH,           // prefill: Gram-Schmidt orthonormalisation
+  K_GRAM,           // prefill: Gram matrix M^T M (tensor cores); CUDA-core path: M X^T
+  K_GEMM,           // prefill: X G of the subspace iteration; CUDA-core path: (M X^T)^T M
+  K_ORTH,           // prefill: orthonormalisation (CholeskyQR; CUDA-core path: Gram-Schmidt)
   K_MISC,           // prefill: reductions, transposes, fills
+  K_SVD_A,          // prefill: the factor A = M X^T
   K_NUM
 };
 
@@ -208,5 +209,12 @@ cudaError_t launch_fill_i32(Ctx& c, int32_t* p, int32_t v, size_t n, cudaStream_
 // each host page (measured on GB300: the first 32 steps after an offload ran
 // 40% slower without it).
 cudaError_t launch_read_host_v(Ctx& c, cudaStream_t st);
+// b x r x D seeded standard-normal starting bases (the SVD's random start)
+cudaError_t launch_random_basis(Ctx& c, float* X, cudaStream_t st);
+// svd_tc.cu: the tensor-core SVD of bf16 contexts (Gram matrix + subspace
+// iteration); svd_tc_basis writes the orthonormal basis to c.basis
+bool svd_tc_supported(const shadowkv_params& p);
+size_t svd_tc_workspace_bytes(const shadowkv_params& p, int nsm);
+cudaError_t svd_tc_basis(Ctx& c, const void* K, void* ws, cudaStream_t st);   // K: bf16 keys
 
 }  // namespace skv

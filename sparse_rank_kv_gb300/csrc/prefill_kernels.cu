@@ -452,8 +452,42 @@ static cudaError_t prefill_stats(Ctx& c, const T* K, const T* V, cudaStream_t st
   return cudaGetLastError();
 }
 
+cudaError_t launch_random_basis(Ctx& c, float* X, cudaStream_t st) {
+  const size_t n_x = static_cast<size_t>(c.p.r) * c.p.h_kv * c.p.d;
+  for (int bb = 0; bb < c.p.b; ++bb) {
+    kbegin(c, K_MISC, st);
+    k_random_basis<<<grid_for(n_x, 256, 1024), 256, 0, st>>>(X + bb * n_x, c.p.r, c.p.h_kv * c.p.d, c.p.seed, bb);
+    kend(c, K_MISC, st);
+  }
+  return cudaGetLastError();
+}
+
+// bf16 contexts whose shapes the tensor-core SVD takes: the basis and
+// A = M X^T (svd_tc.cu), then B^T per head.  One workspace allocation for
+// the whole batch.
+static cudaError_t prefill_svd_tc(Ctx& c, const bf16* K, cudaStream_t st) {
+  const int d = c.p.d, h = c.p.h_kv, r = c.p.r, D = h * d;
+  void* ws = nullptr;
+  SKV_TRY(cudaMalloc(&ws, svd_tc_workspace_bytes(c.p, c.nsm)));
+  cudaError_t err = svd_tc_basis(c, K, ws, st);
+  const size_t n_x = static_cast<size_t>(r) * D;
+  for (int bb = 0; bb < c.p.b && err == cudaSuccess; ++bb) {
+    const float* X = c.basis + bb * n_x;
+    kbegin(c, K_MISC, st);
+    k_basis_to_bt<bf16><<<grid_for(n_x, 256, 1024), 256, 0, st>>>(X, static_cast<bf16*>(c.Bt) + bb * n_x, r, D);
+    kend(c, K_MISC, st);
+    err = cudaGetLastError();
+  }
+  cudaError_t e2 = cudaStreamSynchronize(st);
+  cudaFree(ws);
+  return err != cudaSuccess ? err : e2;
+}
+
 template <typename T>
 static cudaError_t prefill_svd(Ctx& c, const T* K, cudaStream_t st) {
+  if constexpr (sizeof(T) == 2) {
+    if (svd_tc_supported(c.p) && !c.force_simt) return prefill_svd_tc(c, K, st);
+  }
   const int s = c.p.s, d = c.p.d, h = c.p.h_kv, r = c.p.r, D = h * d;
   const int dshift = d == 128 ? 7 : 6;
   const int nsm = num_sms(c);
