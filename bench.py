@@ -5,15 +5,26 @@ Metric: decode tokens/s per layer (b tokens per decode step) on the batch-8,
 dominant kernel against the measured GB300 peak.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--config NAME] [--batch B] [--no-cpu-baseline]
+                    [--config NAME] [--batch B] [--sweep B1,B2,...] [--chunk C]
+                    [--budget PCT] [--q-sigma S] [--layers L] [--no-cpu-baseline]
 
 One "step" is one decode step through the C ABI (Algorithm 2: landmark
 scores, top-k, set-difference value fetch from pinned host memory, key
 rebuild with RoPE, attention), for every sequence of the batch, with all
 inputs resident in HBM.  Prefill (Algorithm 1) runs once before timing and
-is reported separately.  Under torchrun each rank runs its own full batch on
-its own GPU (weak scaling, no collective on the data path); rank 0 prints
-one JSON line.  `--impl reference` times the CPU oracle instead.
+is reported separately (wall time, and its kernels' CUDA-event times).
+Under torchrun each rank runs its own full batch on its own GPU (weak
+scaling, no collective on the data path); rank 0 prints one JSON line.
+
+  --sweep 8,16,24,48   one JSON line per batch size (the 60K batch sweep)
+  --chunk/--budget     chunk size c and sparse budget k*c/s in percent
+  --q-sigma S          query drift per step (larger: fewer cache hits)
+  --layers L           L layers, each its own context and cache, decoded back
+                       to back on one stream; reported per layer
+With the 256K workload (prefill plus decode) the line also carries the SVD's
+reconstruction error over the Eckart-Young optimum and the subspace
+similarity <H1, H2> / r of the two sequences' bases.
+`--impl reference` times the CPU oracle instead.
 """
 from __future__ import annotations
 
@@ -21,12 +32,10 @@ import argparse
 import ctypes
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess
 import sys
-import threading
 import time
 
 import numpy as np
@@ -42,6 +51,8 @@ METRIC = "ShadowKV decode tokens/s per layer at 128K; achieved HBM GB/s vs GB300
 UNIT = "tokens/s/layer"
 DEFAULT_CONFIG = "llama_b8_s128k"
 FALLBACK_HBM_GBS = 6800.0
+_WARM = False
+PREFILL_KERNELS = ("chunkstats", "outliers", "gather", "svd_gram", "svd_iter", "orth", "misc", "svd_a")
 
 
 # ----------------------------------------------------------------- helpers
@@ -56,14 +67,15 @@ def peaks():
 
 
 def hbm_bytes_per_step(cfg, E, n_loc, alpha=0.0, records=False):
-    """Algorithmic HBM bytes of one decode step.
+    """HBM bytes of one decode step.
 
-    Row-major contexts follow the pages' step: landmarks, A rows of every
-    selected chunk, B, outlier K/V, cached V of the selected chunks,
-    local-window K/V.  With K/V records (bf16, d = 128) a cache slot keeps its
-    chunk's rebuilt keys, so a step with hit rate `alpha` reads A rows of the
-    missed chunks only, reads the keys and values of every selected chunk,
-    and writes the missed chunks' rebuilt keys and fetched values."""
+    records=False: the algorithmic bytes of the pages' step -- landmarks, A
+    rows of every selected chunk, B, outlier K/V, cached V of the selected
+    chunks, local-window K/V.  records=True: the traffic of the K/V-record
+    layout, where a cache slot keeps its chunk's rebuilt keys, so a step with
+    hit rate `alpha` reads A rows of the missed chunks only, reads the keys
+    and values of every selected chunk, and writes the missed chunks'
+    rebuilt keys and fetched values."""
     sel = cfg.k * cfg.c                       # selected tokens per (batch, KV head)
     common = cfg.n * cfg.d + cfg.r * cfg.d + 2 * cfg.o * cfg.c * cfg.d + 2 * n_loc * cfg.d
     if records:
@@ -74,71 +86,92 @@ def hbm_bytes_per_step(cfg, E, n_loc, alpha=0.0, records=False):
     return E * cfg.b * cfg.h_kv * per_pair
 
 
-class ClockSampler:
-    """Samples SM clock and throttle reasons through NVML (read-only queries)
-    in a background thread; falls back to nvidia-smi."""
-    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
-               0x4: "sw_power_cap", 0x80: "hw_power_brake_slowdown"}
+def score_bytes(cfg, E):
+    """(algorithmic, written) bytes of one landmark-score launch: the landmarks
+    read, and the logits plus per-tile softmax partials the kernel writes for
+    the selection (implementation overhead, not in the pages' byte count)."""
+    land = E * cfg.b * cfg.h_kv * cfg.n * cfg.d
+    extra = 4 * cfg.b * cfg.h_q * cfg.n + 8 * 4 * cfg.b * cfg.h_q * ((cfg.n + 127) // 128)
+    return land, extra
 
-    def __init__(self, index: int, period_s: float = 0.001):
+
+def apply_overrides(cfg, chunk=None, budget=None, q_sigma=None, batch=None):
+    """The workload with its chunk size, sparse budget (percent of s),
+    query drift or batch replaced; k = round(budget * s / c) chunks."""
+    pct = 100.0 * cfg.k * cfg.c / cfg.s
+    if chunk:
+        cfg = cfg.with_(c=chunk)
+    if chunk or budget:
+        pct = budget if budget else pct
+        cfg = cfg.with_(k=max(1, int(round(pct / 100.0 * cfg.s / cfg.c))))
+    if q_sigma is not None:
+        cfg = cfg.with_(q_sigma=q_sigma)
+    if batch:
+        cfg = cfg.with_(b=batch)
+    return cfg
+
+
+_SAMPLER = r"""
+import ctypes, json, signal, sys, time
+idx, period = int(sys.argv[1]), float(sys.argv[2])
+REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+           0x4: "sw_power_cap", 0x80: "hw_power_brake_slowdown"}
+samples, reasons, mx = [], set(), None
+stop = []
+signal.signal(signal.SIGTERM, lambda *a: stop.append(1))
+try:
+    nv = ctypes.CDLL("libnvidia-ml.so.1")
+    ok = nv.nvmlInit_v2() == 0
+except OSError:
+    ok = False
+if ok:
+    h = ctypes.c_void_p()
+    ok = nv.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(h)) == 0
+if ok:
+    m = ctypes.c_uint()
+    if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(m)) == 0:
+        mx = m.value
+    clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+    print("ready", flush=True)
+    while not stop:
+        if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+            samples.append(clk.value)
+        if nv.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(rs)) == 0:
+            for bit, name in REASONS.items():
+                if rs.value & bit:
+                    reasons.add(name)
+        time.sleep(period)
+else:
+    print("ready", flush=True)
+    while not stop:
+        time.sleep(period)
+print(json.dumps({"samples": samples, "reasons": sorted(reasons), "max": mx}), flush=True)
+"""
+
+
+class ClockSampler:
+    """Samples the SM clock and throttle reasons through NVML (read-only
+    queries) in a separate process, so that the sampling never competes with
+    the launching thread for the interpreter lock."""
+
+    def __init__(self, index: int, period_s: float = 0.0005):
         self.index, self.period = index, period_s
         self.samples, self.reasons, self.max_mhz = [], set(), None
-        self._stop = threading.Event()
-        self._nvml = None
-        try:
-            nv = ctypes.CDLL("libnvidia-ml.so.1")
-            if nv.nvmlInit_v2() == 0:
-                h = ctypes.c_void_p()
-                if nv.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(h)) == 0:
-                    self._nvml, self._h = nv, h
-                    mx = ctypes.c_uint()
-                    if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
-                        self.max_mhz = mx.value
-        except OSError:
-            self._nvml = None
-
-    def _poll(self):
-        nv, h = self._nvml, getattr(self, "_h", None)
-        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
-        while not self._stop.is_set():
-            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
-                self.samples.append(clk.value)
-            if nv.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(rs)) == 0:
-                for bit, name in self.REASONS.items():
-                    if rs.value & bit:
-                        self.reasons.add(name)
-            time.sleep(self.period)
 
     def __enter__(self):
-        if self._nvml is not None:
-            self._t = threading.Thread(target=self._poll, daemon=True)
-            self._t.start()
-        else:
-            q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
-                 "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-                 "clocks_event_reasons.sw_power_cap")
-            self._p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
-                                        "--format=csv,noheader,nounits", "-lms", "100"],
-                                       stdout=subprocess.PIPE, text=True)
+        self._p = subprocess.Popen([sys.executable, "-c", _SAMPLER, str(self.index), str(self.period)],
+                                   stdout=subprocess.PIPE, text=True)
+        self._p.stdout.readline()          # NVML is up before the timed region starts
         return self
 
     def __exit__(self, *a):
-        if self._nvml is not None:
-            self._stop.set()
-            self._t.join()
-            return
         self._p.terminate()
-        out = self._p.communicate()[0]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 6 or not f[0].isdigit():
-                continue
-            self.samples.append(int(f[0]))
-            self.max_mhz = int(f[1])
-            for nm, v in zip(names, f[2:]):
-                if v.lower() == "active":
-                    self.reasons.add(nm)
+        out = self._p.communicate(timeout=30)[0].strip().splitlines()
+        try:
+            rec = json.loads(out[-1])
+        except (IndexError, ValueError):
+            return
+        self.samples, self.reasons, self.max_mhz = rec["samples"], set(rec["reasons"]), rec["max"]
 
     def summary(self):
         med = statistics.median(self.samples) if self.samples else None
@@ -192,6 +225,41 @@ def dist_env():
     return ws, rank, local
 
 
+def svd_report(inp, ctx, cfg, dev):
+    """Quality of the prefill's rank-r factors, measured with torch in float64
+    on the device (a report, not part of the path): for sequence 0,
+    |M - A B|^2 and |M - M X^T X|^2 over the Eckart-Young optimum
+    sum_{i>r} sigma_i^2 (all from the Gram matrix of M), and the subspace
+    similarity <H1, H2> / r = |X_0 X_1^T|_F^2 / r of sequences 0 and 1."""
+    b, h, s, d, r = cfg.b, cfg.h_kv, cfg.s, cfg.d, cfg.r
+    D = h * d
+    X = ctx.export("SVD_BASIS").view(b, r, D).to(dev, torch.float64)
+    A = ctx.export("A").view(b, s, r)[0].to(dev, torch.float64)
+    B = ctx.export("BT").view(b, h, d, r)[0].to(dev, torch.float64).permute(2, 0, 1).reshape(r, D)
+    M = inp["k_pre"][0].to(torch.float64).permute(1, 0, 2).reshape(s, D)
+    G = M.T @ M
+    tot = float(torch.trace(G))
+    lam = torch.linalg.eigvalsh(G)
+    opt = float(lam[:-r].sum())
+    X0 = X[0]
+    Q = X0 @ G @ X0.T
+    eb = tot - 2.0 * float(torch.trace(Q)) + float(((X0 @ X0.T) * Q.T).sum())
+    es = tot - 2.0 * float(((A.T @ M) * B).sum()) + float(((A.T @ A) * (B @ B.T)).sum())
+    rep = {"sequence": 0, "err2_over_opt2_stored": es / opt, "err2_over_opt2_basis": eb / opt,
+           "rel_err_stored": (es / tot) ** 0.5, "rel_err_optimal": (opt / tot) ** 0.5}
+    m = r - cfg.rank_true
+    if m > 0:
+        # the same with the r - R directions past the keys' true rank R drawn
+        # at random from the noise subspace (expected value)
+        noise = lam[:D - cfg.rank_true]
+        rep["err2_over_opt2_random_noise_directions"] = float(noise.sum() - m * noise.mean()) / opt
+    if b > 1:
+        rep["subspace_similarity_seq01"] = float((X[0] @ X[1].T).pow(2).sum()) / r
+        rep["subspace_similarity_random_expectation"] = r / D
+    del M, G
+    return rep
+
+
 # ----------------------------------------------------------- CPU oracle leg
 def oracle_decode_timing(cfg, steps: int, warmup: int, seed: int = 0):
     """Times the CPU oracle's decode step on one sequence of cfg (all KV heads)."""
@@ -216,31 +284,74 @@ def oracle_decode_timing(cfg, steps: int, warmup: int, seed: int = 0):
 
 
 # ------------------------------------------------------------------ our arm
+def link_bulk_gbs(dev):
+    """Best pinned-host -> device copy rate (GB/s) over three copy sizes."""
+    best = {}
+    for mb in (4, 32, 256):
+        nbytes = mb << 20
+        hbuf = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+        dbuf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        for _ in range(2):
+            dbuf.copy_(hbuf, non_blocking=True)
+        torch.cuda.synchronize()
+        reps = max(3, 1024 // mb)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            dbuf.copy_(hbuf, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        best[f"{mb}MB"] = reps * nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9
+        del hbuf, dbuf
+    return best
+
+
 def run_ours(args, cfg):
     ws, rank, local = dist_env()
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     K, W = args.steps, args.warmup
+    L = max(1, args.layers)
     # decode steps appended per pass; every pass starts from the same rewound state
     max_new = W + K
     run_cfg = cfg.with_(steps=max_new)
     E = 2 if cfg.dtype == "bf16" else 4
     dt = synth.torch_dtype(cfg.dtype)
-
-    inp = synth.make_inputs(run_cfg, device=dev)
-    p = binding.make_params(run_cfg)
     stream = torch.cuda.current_stream()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    ctx = binding.prefill(p, inp["k_pre"], inp["v"], stream)
-    torch.cuda.synchronize()
-    prefill_ms = (time.perf_counter() - t0) * 1e3
-    del inp["k_pre"], inp["v"]
-    torch.cuda.empty_cache()
-    q, kn, vn = inp["q"], inp["k_new"], inp["v_new"]
+
+    # the first launch of each kernel in a process loads its module: a small
+    # prefill of the same kind (same d, G, r, c, dtype) keeps that out of the
+    # timed prefill
+    global _WARM
+    if not _WARM:
+        o_w = min(cfg.o, 4096 // cfg.c // 4)
+        warm = run_cfg.with_(b=1, s=cfg.w + 4096, o=o_w, k=min(cfg.k, 4096 // cfg.c - o_w))
+        wi = synth.make_inputs(warm, device=dev)
+        binding.prefill(binding.make_params(warm), wi["k_pre"], wi["v"], stream).close()
+        del wi
+        _WARM = True
+
+    # ---- prefill: one context (its own cache) per layer
+    ctxs, prefill_ms, prefill_kernels, svd = [], [], None, None
+    for layer in range(L):
+        inp = synth.make_inputs(run_cfg.with_(seed=run_cfg.seed + 1000 * layer), device=dev)
+        p = binding.make_params(run_cfg)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        ctx = binding.prefill(p, inp["k_pre"], inp["v"], stream)
+        torch.cuda.synchronize()
+        prefill_ms.append((time.perf_counter() - t0) * 1e3)
+        if layer == 0:
+            kt = ctx.kernel_times()
+            prefill_kernels = {k_: {"ms": v[0], "launches": v[1]} for k_, v in kt.items()
+                               if v[1] and k_ in PREFILL_KERNELS}
+            if args.svd_report and rank == 0:
+                svd = svd_report(inp, ctx, cfg, dev)
+            q, kn, vn = inp["q"], inp["k_new"], inp["v_new"]
+        ctx.reset_timers()
+        ctxs.append(ctx)
+        del inp
+        torch.cuda.empty_cache()
+    layout = ctxs[0].layout()
     out = torch.empty(cfg.b, cfg.h_q, cfg.d, dtype=dt, device=dev)
 
     def barrier():
@@ -248,137 +359,156 @@ def run_ours(args, cfg):
             import torch.distributed as dist
             dist.barrier()
 
-    def decode_pass(timing: bool):
-        ctx.rewind(stream)
-        ctx.set_option(binding.OPT_TIMING, 1 if timing else 0)
-        for t in range(W):
-            ctx.decode_step(q[t], kn[t], vn[t], out, stream)
-        ctx.reset_timers()
-        st0 = ctx.stats()
+    def steps(t0, t1):
+        for t in range(t0, t1):
+            for ctx in ctxs:
+                ctx.decode_step(q[t], kn[t], vn[t], out, stream)
+
+    def decode_pass(timing: bool, cache: bool = True):
+        for ctx in ctxs:
+            ctx.rewind(stream)
+            ctx.set_option(binding.OPT_TIMING, 1 if timing else 0)
+            ctx.set_option(binding.OPT_CACHE, 1 if cache else 0)
+        steps(0, W)
+        for ctx in ctxs:
+            ctx.reset_timers()
+        st0 = [ctx.stats() for ctx in ctxs]
         barrier()
         torch.cuda.synchronize()
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ev0.record(stream)
-        for t in range(W, W + K):
-            ctx.decode_step(q[t], kn[t], vn[t], out, stream)
+        steps(W, W + K)
         ev1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        st1 = ctx.stats()
+        st1 = [ctx.stats() for ctx in ctxs]
         ms = ev0.elapsed_time(ev1)
-        kt = ctx.kernel_times() if timing else None
-        ctx.set_option(binding.OPT_TIMING, 0)
-        return ms, st0, st1, kt
+        kt = ctxs[0].kernel_times() if timing else None
+        for ctx in ctxs:
+            ctx.set_option(binding.OPT_TIMING, 0)
+            ctx.set_option(binding.OPT_CACHE, 1)
+        hits = sum(b_.hits - a_.hits for a_, b_ in zip(st0, st1))
+        misses = sum(b_.misses - a_.misses for a_, b_ in zip(st0, st1))
+        launches = sum(b_.launches - a_.launches for a_, b_ in zip(st0, st1))
+        return ms, hits, misses, launches, kt
 
-    # 1) the headline: K decode steps, inputs resident, no per-kernel events
+    # 1) the headline: K decode steps (of every layer), inputs resident, no per-kernel events
     with ClockSampler(local) as clk:
-        ms, st0, st1, _ = decode_pass(False)
+        ms, hits, misses, launches, _ = decode_pass(False)
     ms = max_over_ranks(ms, dev)
-    ms_step = ms / K
-    hits = st1.hits - st0.hits
-    misses = st1.misses - st0.misses
+    ms_step = ms / K / L                      # per layer
     alpha = hits / max(1, hits + misses)
-    launches = st1.launches - st0.launches
 
     # 2) the same K steps with CUDA events around every kernel on its stream
-    ms_t, _, _, kt = decode_pass(True)
+    ms_t, _, _, _, kt = decode_pass(True)
+    # 3) the cache forced off: every selected chunk crosses the host link,
+    #    which times the fetch's own access pattern at full size
+    _, _, miss_off, _, kt_off = decode_pass(True, cache=False)
 
-    # 3) end to end through the C ABI from pinned host buffers
-    ctx.rewind(stream)
-    qh = q.cpu().pin_memory()
-    knh, vnh = kn.cpu().pin_memory(), vn.cpu().pin_memory()
+    # 4) end to end through the C ABI from pinned host buffers: per step one
+    #    host -> device copy of (q, k_new, v_new), the step of every layer, a
+    #    device -> host copy of the output, and a wait for it
+    for ctx in ctxs:
+        ctx.rewind(stream)
+    nq, nk = q[0].numel(), kn[0].numel()
+    per = nq + 2 * nk
+    host = torch.empty(W + K, per, dtype=dt).pin_memory()
+    host[:, :nq].copy_(q.reshape(W + K, nq))
+    host[:, nq:nq + nk].copy_(kn.reshape(W + K, nk))
+    host[:, nq + nk:].copy_(vn.reshape(W + K, nk))
+    blk = torch.empty(per, dtype=dt, device=dev)
+    qd, knd, vnd = blk[:nq].view_as(q[0]), blk[nq:nq + nk].view_as(kn[0]), blk[nq + nk:].view_as(vn[0])
     outh = torch.empty(out.shape, dtype=dt).pin_memory()
-    qd, knd, vnd = torch.empty_like(q[0]), torch.empty_like(kn[0]), torch.empty_like(vn[0])
-    for t in range(W):
-        ctx.decode_step(q[t], kn[t], vn[t], out, stream)
+    steps(0, W)
     torch.cuda.synchronize()
     barrier()
     t0 = time.perf_counter()
     for t in range(W, W + K):
-        qd.copy_(qh[t], non_blocking=True)
-        knd.copy_(knh[t], non_blocking=True)
-        vnd.copy_(vnh[t], non_blocking=True)
-        ctx.decode_step(qd, knd, vnd, out, stream)
+        blk.copy_(host[t], non_blocking=True)
+        for ctx in ctxs:
+            ctx.decode_step(qd, knd, vnd, out, stream)
         outh.copy_(out, non_blocking=True)
         stream.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, dev)
     barrier()
-    h2d = (qd.numel() + knd.numel() + vnd.numel()) * E
+    h2d = per * E
     d2h = out.numel() * E
 
-    # host link: bulk pinned -> device copy
-    nbytes = 256 << 20
-    hbuf = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
-    dbuf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-    for _ in range(2):
-        dbuf.copy_(hbuf, non_blocking=True)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(5):
-        dbuf.copy_(hbuf, non_blocking=True)
-    e1.record()
-    torch.cuda.synchronize()
-    bulk_gbs = 5 * nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9
-
-    ctx.check()
+    bulk = link_bulk_gbs(dev)
+    for ctx in ctxs:
+        ctx.check()
     result = None
     if rank == 0:
         hbm_gbs, peak_src = peaks()
         n_loc_avg = cfg.w + W + (K + 1) / 2.0
-        records = cfg.dtype == "bf16" and cfg.d == 128 and cfg.c % 8 == 0 and 128 % cfg.c == 0
-        hbm = hbm_bytes_per_step(cfg, E, n_loc_avg, alpha, records)
-        link = misses / K * cfg.c * cfg.d * E
-        fetch_ms, fetch_n = kt["fetch"]
-        fetch_in = "fetch launch"
-        if fetch_n == 0:
-            # K/V records: the fetch runs as CTAs of the rebuild launch, whose
-            # time (bound by the host link) is an upper bound on the fetch's
-            fetch_ms, fetch_n = kt["rebuild"]
-            fetch_in = "rebuild launch (fetch CTAs inside it)"
-        fetch_gbs = link * fetch_n / max(1, K) / (fetch_ms / max(1, fetch_n) * 1e-3) / 1e9 if fetch_ms > 0 else 0.0
-        link_gbs = max(bulk_gbs, fetch_gbs)
+        hbm = hbm_bytes_per_step(cfg, E, n_loc_avg)
+        hbm_rec = hbm_bytes_per_step(cfg, E, n_loc_avg, alpha, records=True) if layout["kv_records"] else None
+        link = misses / K / L * cfg.c * cfg.d * E
+        fetch_kid = "rebuild" if layout["fetch_in_rebuild"] else "fetch"
+        fetch_in = "rebuild launch (fetch CTAs inside it)" if layout["fetch_in_rebuild"] else "fetch launch"
+
+        def rate(kts, nmiss):
+            ms_, n_ = kts[fetch_kid]
+            byts = nmiss / K / L * cfg.c * cfg.d * E
+            return byts / (ms_ / max(1, n_) * 1e-3) / 1e9 if ms_ > 0 else 0.0
+
+        fetch_gbs = rate(kt, misses)
+        fetch_off_gbs = rate(kt_off, miss_off)
+        link_gbs = max(max(bulk.values()), fetch_gbs, fetch_off_gbs)
         t_roof = hbm / (hbm_gbs * 1e9) + link / (link_gbs * 1e9)
         score_ms, score_n = kt["score"]
-        # landmarks read + logits P and per-tile softmax partials written
-        score_bytes = (E * cfg.b * cfg.h_kv * cfg.n * cfg.d + 4 * cfg.b * cfg.h_q * cfg.n
-                       + 8 * 4 * cfg.b * cfg.h_q * ((cfg.n + 127) // 128))
-        achieved = score_bytes / (score_ms / score_n * 1e-3) / 1e9
-        traffic = traffic_from_profile("score_kernel_b8_s128k.md", "score_tc.cu")
+        land, extra = score_bytes(cfg, E)
+        score_s = score_ms / score_n * 1e-3
+        achieved = land / score_s / 1e9
+        traffic = traffic_from_profile("score_kernel_b8_s128k.md", "score_tc.cu") \
+            if (cfg.b, cfg.s, cfg.c) == (8, 131072, 8) else None
         per_kernel = {k_: {"ms_per_step": v[0] / K, "launches": v[1]} for k_, v in kt.items() if v[1]}
         value = job_tokens_per_s(ws, cfg.b, ms_step)
+        pct = 100.0 * cfg.k * cfg.c / cfg.s
+        step_roof = {"hbm_bytes": hbm, "link_bytes": link, "hbm_gbs": hbm_gbs, "link_gbs": link_gbs,
+                     "bulk_h2d_gbs": bulk, "fetch_gbs": fetch_gbs, "fetch_gbs_cache_off": fetch_off_gbs,
+                     "fetch_timed_in": fetch_in, "t_roof_us": t_roof * 1e6, "t_step_us": ms_step * 1e3,
+                     "frac": t_roof / (ms_step * 1e-3),
+                     "bytes": "pages' step (L, A rows of every selected chunk, B, outliers, cached V, local)"}
+        if hbm_rec is not None:
+            t_rec = hbm_rec / (hbm_gbs * 1e9) + link / (link_gbs * 1e9)
+            step_roof.update({"hbm_bytes_records": hbm_rec, "frac_records": t_rec / (ms_step * 1e-3)})
         result = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
             "warmup": W, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
             "config": {"workload": f"{cfg.name}: ShadowKV decode, b={cfg.b} h_q={cfg.h_q} "
                                    f"h_kv={cfg.h_kv} d={cfg.d} s={cfg.s} c={cfg.c} r={cfg.r} "
-                                   f"k={cfg.k} o={cfg.o} w={cfg.w}",
+                                   f"k={cfg.k} ({pct:.2f}% budget) o={cfg.o} w={cfg.w} "
+                                   f"q_sigma={cfg.q_sigma}" + (f", {L} layers" if L > 1 else ""),
                        "global_batch": ws * cfg.b, "seq_len": cfg.s,
                        "parallelism": f"batch replicas x{ws}" if ws > 1 else "single GPU",
-                       "l2": "inputs larger than L2 (landmarks %.0f MB, A %.0f MB per step)" % (
+                       "l2": "inputs larger than L2 (landmarks %.0f MB, A %.0f MB per layer)" % (
                            E * cfg.b * cfg.h_kv * cfg.n * cfg.d / 1e6, E * cfg.b * cfg.s * cfg.r / 1e6)},
             "roofline": {"bound": "hbm", "kernel": "score", "achieved": achieved,
                          "peak": hbm_gbs, "unit": "GB/s", "frac": achieved / hbm_gbs,
                          "peak_source": peak_src, "traffic": traffic,
-                         "algorithmic_bytes_per_launch": score_bytes},
-            "step_roofline": {"hbm_bytes": hbm, "link_bytes": link, "hbm_gbs": hbm_gbs,
-                              "link_gbs": link_gbs, "bulk_h2d_gbs": bulk_gbs,
-                              "fetch_gbs": fetch_gbs, "fetch_timed_in": fetch_in, "t_roof_us": t_roof * 1e6,
-                              "t_step_us": ms_step * 1e3, "frac": t_roof / (ms_step * 1e-3)},
-            "per_kernel_ms": per_kernel, "timed_with_kernel_events_ms_per_step": ms_t / K,
-            "alpha_hit_rate": alpha,
+                         "algorithmic_bytes_per_launch": land,
+                         "extra_written_bytes_per_launch": extra,
+                         "frac_with_written": (land + extra) / score_s / 1e9 / hbm_gbs},
+            "step_roofline": step_roof,
+            "per_kernel_ms": per_kernel, "timed_with_kernel_events_ms_per_step": ms_t / K / L,
+            "alpha_hit_rate": alpha, "layout": layout,
             "equivalent_bandwidth_TBps": 2 * cfg.s * cfg.d * E * cfg.b * cfg.h_kv / (ms_step * 1e-3) / 1e12,
-            "prefill_ms": prefill_ms,
-            "e2e": {"value": job_tokens_per_s(ws, cfg.b, e2e_s * 1e3 / K), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+            "prefill_ms": prefill_ms[0], "prefill_kernels": prefill_kernels,
+            "prefill_kernels_ms": sum(v["ms"] for v in prefill_kernels.values()),
+            "e2e": {"value": job_tokens_per_s(ws, cfg.b, e2e_s * 1e3 / K / L), "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches,
             "clocks": clk.summary(),
         }
-    ctx.close()
-    if ws > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+        if svd is not None:
+            result["svd"] = svd
+        if L > 1:
+            result["layers"] = L
+            result["prefill_ms_per_layer"] = prefill_ms
+    for ctx in ctxs:
+        ctx.close()
     return result
 
 
@@ -390,14 +520,21 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(CONFIGS))
     ap.add_argument("--batch", type=int, default=None)
+    ap.add_argument("--sweep", default=None, help="comma-separated batch sizes, one line each")
+    ap.add_argument("--chunk", type=int, default=None)
+    ap.add_argument("--budget", type=float, default=None, help="sparse budget k*c/s in percent")
+    ap.add_argument("--q-sigma", type=float, default=None)
+    ap.add_argument("--layers", type=int, default=1)
+    ap.add_argument("--svd-report", action="store_true",
+                    help="SVD error and subspace similarity (on by default for the 256K workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    cfg = CONFIGS[args.config]
-    if args.batch:
-        cfg = cfg.with_(b=args.batch)
-    ws, rank, _ = dist_env()
+    if args.config == "llama_b2_s256k":
+        args.svd_report = True
+    cfg = apply_overrides(CONFIGS[args.config], args.chunk, args.budget, args.q_sigma, args.batch)
+    ws, rank, local = dist_env()
 
     if args.impl == "reference":
         if rank != 0:
@@ -416,15 +553,26 @@ def main():
         }))
         return
 
-    res = run_ours(args, cfg)
-    if res is None:
-        return
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    batches = [int(x) for x in args.sweep.split(",")] if args.sweep else [cfg.b]
+    cpu = None
     if ws == 1 and not args.no_cpu_baseline:
         tot, n, cores = oracle_decode_timing(cfg, 3, 1)
-        res["cpu_baseline"] = {"value": n / tot, "unit": UNIT, "cores": cores, "kind": "oracle",
-                               "sample": f"1 of {cfg.b} sequences (all {cfg.h_kv} KV heads), "
-                                         f"{n} decode steps of the same shape"}
-    print(json.dumps(res))
+        cpu = {"value": n / tot, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"1 sequence (all {cfg.h_kv} KV heads), {n} decode steps of the same shape"}
+    for b in batches:
+        res = run_ours(args, cfg.with_(b=b))
+        if res is None:
+            continue
+        if cpu is not None:
+            res["cpu_baseline"] = cpu
+        print(json.dumps(res), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
 
 
 if __name__ == "__main__":
