@@ -345,7 +345,10 @@ def run_ours(args, cfg):
             prefill_kernels = {k_: {"ms": v[0], "launches": v[1]} for k_, v in kt.items()
                                if v[1] and k_ in PREFILL_KERNELS}
             if args.svd_report and rank == 0:
-                svd = svd_report(inp, ctx, cfg, dev)
+                # kept for the report, which runs after the timed passes: its
+                # fp64 products on the device are followed by stalls of some
+                # hundreds of microseconds in the next kernels
+                svd_keys = inp["k_pre"]
             q, kn, vn = inp["q"], inp["k_new"], inp["v_new"]
         ctx.reset_timers()
         ctxs.append(ctx)
@@ -406,8 +409,9 @@ def run_ours(args, cfg):
     _, _, miss_off, _, kt_off = decode_pass(True, cache=False)
 
     # 4) end to end through the C ABI from pinned host buffers: per step one
-    #    host -> device copy of (q, k_new, v_new), the step of every layer, a
-    #    device -> host copy of the output, and a wait for it
+    #    host -> device copy of (q, k_new, v_new), the step of every layer
+    #    with the last layer's attention writing its output straight into
+    #    pinned host memory (over the host link), and a wait for it
     for ctx in ctxs:
         ctx.rewind(stream)
     nq, nk = q[0].numel(), kn[0].numel()
@@ -425,9 +429,8 @@ def run_ours(args, cfg):
     t0 = time.perf_counter()
     for t in range(W, W + K):
         blk.copy_(host[t], non_blocking=True)
-        for ctx in ctxs:
-            ctx.decode_step(qd, knd, vnd, out, stream)
-        outh.copy_(out, non_blocking=True)
+        for li, ctx in enumerate(ctxs):
+            ctx.decode_step(qd, knd, vnd, outh if li == L - 1 else out, stream)
         stream.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, dev)
     barrier()
@@ -437,6 +440,9 @@ def run_ours(args, cfg):
     bulk = link_bulk_gbs(dev)
     for ctx in ctxs:
         ctx.check()
+    if args.svd_report and rank == 0:
+        svd = svd_report({"k_pre": svd_keys}, ctxs[0], cfg, dev)
+        del svd_keys
     result = None
     if rank == 0:
         hbm_gbs, peak_src = peaks()
@@ -512,6 +518,43 @@ def run_ours(args, cfg):
     return result
 
 
+def run_prefill(args, cfg):
+    """Algorithm 1 alone: a warm-up prefill of the same kind, then the
+    workload's prefill, timed on the host around the C-ABI call (which
+    synchronizes), with its kernels' CUDA-event times."""
+    _, _, local = dist_env()
+    dev = torch.device("cuda", local)
+    run_cfg = cfg.with_(steps=1)
+    stream = torch.cuda.current_stream()
+    o_w = min(cfg.o, 4096 // cfg.c // 4)
+    warm = run_cfg.with_(b=1, s=cfg.w + 4096, o=o_w, k=min(cfg.k, 4096 // cfg.c - o_w))
+    wi = synth.make_inputs(warm, device=dev)
+    binding.prefill(binding.make_params(warm), wi["k_pre"], wi["v"], stream).close()
+    del wi
+    inp = synth.make_inputs(run_cfg, device=dev)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    ctx = binding.prefill(binding.make_params(run_cfg), inp["k_pre"], inp["v"], stream)
+    wall = (time.perf_counter() - t0) * 1e3
+    kt = ctx.kernel_times()
+    kern = {k_: {"ms": v[0], "launches": v[1]} for k_, v in kt.items() if v[1] and k_ in PREFILL_KERNELS}
+    E = 2 if cfg.dtype == "bf16" else 4
+    D = cfg.h_kv * cfg.d
+    res = {"metric": "ShadowKV prefill (Algorithm 1) wall time", "value": wall, "unit": "ms",
+           "higher_is_better": False, "dtype": cfg.dtype, "data": "synthetic",
+           "config": {"workload": f"{cfg.name}: ShadowKV prefill, b={cfg.b} h_kv={cfg.h_kv} d={cfg.d} "
+                                  f"s={cfg.s} c={cfg.c} r={cfg.r} o={cfg.o} w={cfg.w}"},
+           "prefill_kernels": kern, "prefill_kernels_ms": sum(v["ms"] for v in kern.values()),
+           "key_bytes": E * cfg.b * cfg.s * D, "value_bytes_offloaded": E * cfg.b * cfg.s * D,
+           "gram_flops": cfg.b * cfg.s * D * (D + 128), "factor_flops": 4 * cfg.b * cfg.s * D * cfg.r,
+           "layout": ctx.layout()}
+    if args.svd_report:
+        res["svd"] = svd_report(inp, ctx, cfg, dev)
+    ctx.check()
+    ctx.close()
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -527,6 +570,8 @@ def main():
     ap.add_argument("--layers", type=int, default=1)
     ap.add_argument("--svd-report", action="store_true",
                     help="SVD error and subspace similarity (on by default for the 256K workload)")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time Algorithm 1 alone (after a warm-up prefill) and print its line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -557,6 +602,11 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
+    if args.prefill_only:
+        res = run_prefill(args, cfg)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        return
     batches = [int(x) for x in args.sweep.split(",")] if args.sweep else [cfg.b]
     cpu = None
     if ws == 1 and not args.no_cpu_baseline:

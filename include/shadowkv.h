@@ -149,7 +149,9 @@ skv_status shadowkv_load_state(const shadowkv_params* p, const shadowkv_state_in
  *   q     : device, b x h_q x d, post-RoPE queries of the new token.
  *   k_new : device, b x h_kv x d, post-RoPE key of the new token, or NULL.
  *   v_new : device, b x h_kv x d, its value (NULL iff k_new is NULL).
- *   out   : device, b x h_q x d, attention output.
+ *   out   : device, b x h_q x d, attention output; it may also be the device
+ *           address of mapped pinned host memory (the result is then written
+ *           over the host link, with no separate copy).
  * With k_new given, the token is appended to the local window first (at most
  * max_new times; then SKV_ERR_STATE).  Step t (0-based) scores
  * P = q L^T / sqrt(d) over the non-outlier chunks, forms S2 (group_reduce),

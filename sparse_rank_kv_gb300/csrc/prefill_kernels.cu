@@ -370,28 +370,27 @@ static int grid_for(size_t total, int threads, int cap) {
   return static_cast<int>(g < 1 ? 1 : g);
 }
 
-// Reads every 16 bytes of the pinned host copy of V through its device
-// mapping once.  The result only feeds a store under `keep`, which the host
-// passes as 0; it keeps the loads from being optimised away.
-__global__ void k_read_host(const uint4* __restrict__ p, size_t n, int keep, unsigned int* __restrict__ sink) {
+// Reads 16 bytes of every 4 KB page of the pinned host copy of V through its
+// device mapping: the first GPU access to a host page is slow, and this moves
+// that cost out of the decode steps' value fetches.  The result only feeds a
+// store under `keep`, which the host passes as 0; it keeps the loads from
+// being optimised away.
+__global__ void k_read_host(const unsigned char* __restrict__ p, size_t pages, int keep,
+                            unsigned int* __restrict__ sink) {
   unsigned int acc = 0;
   const size_t nt = static_cast<size_t>(gridDim.x) * blockDim.x;
-  // four reads in flight per thread, so that a quarter of the SMs keep the
-  // host link busy
-  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += 4 * nt) {
-    uint4 v[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) v[u] = i + u * nt < n ? p[i + u * nt] : make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) acc ^= v[u].x ^ v[u].y ^ v[u].z ^ v[u].w;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < pages; i += nt) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p + (i << 12));
+    acc ^= v.x ^ v.y ^ v.z ^ v.w;
   }
   if (keep) atomicXor(sink, acc);
 }
 
 cudaError_t launch_read_host_v(Ctx& c, cudaStream_t st) {
+  const size_t pages = (c.v_bytes + 4095) >> 12;
   kbegin(c, K_MISC, st);
-  k_read_host<<<(c.nsm + 3) / 4, 1024, 0, st>>>(static_cast<const uint4*>(c.v_cpu_dev), c.v_bytes / 16, 0,
-                                      reinterpret_cast<unsigned int*>(c.status));
+  k_read_host<<<grid_for(pages, 256, 4 * c.nsm), 256, 0, st>>>(static_cast<const unsigned char*>(c.v_cpu_dev), pages,
+                                                              0, reinterpret_cast<unsigned int*>(c.status));
   kend(c, K_MISC, st);
   return cudaGetLastError();
 }

@@ -6,10 +6,11 @@
 //
 //   persistent: one CTA per SM, each owning a contiguous range of 128-row
 //               landmark tiles (a tile never spans two KV heads)
-//   warp 0    : TMA producer -- per tile, d/32 boxes of 128 landmark rows x
-//               32 columns and d/32 boxes of the head's q (16 rows; rows past
+//   warp 0    : TMA producer -- per tile, d/64 boxes of 128 landmark rows x
+//               64 columns and d/64 boxes of the head's q (16 rows; rows past
 //               G are zero-filled by TMA) into a 5-stage shared-memory ring,
-//               K-major with the 64-byte swizzle
+//               K-major with the 128-byte swizzle; lanes 0..2d/64-1 issue one
+//               box each
 //   warp 1    : tcgen05.mma (M=128, N=16, K=16) x (d/16) per tile into one of
 //               eight TMEM accumulators; commits free the ring slot and publish
 //               the accumulator

@@ -12,8 +12,8 @@
 // seeded Gaussian start, each orthonormalisation a shifted CholeskyQR3
 // (Fukaya, Kannan, Nakatsukasa, Zhang and Yamamoto, "Shifted Cholesky QR for
 // computing the QR factorization of ill-conditioned matrices", SIAM J. Sci.
-// Comput. 42 (2020)): a first pass with a small diagonal shift in fp64, then
-// two plain passes in fp32.  A = M X^T and B = X (split per KV head) follow;
+// Comput. 42 (2020)): a first pass whose Gram matrix and Cholesky factor are
+// fp64, with a small diagonal shift, then two plain passes in fp32.  A = M X^T and B = X (split per KV head) follow;
 // only the product A B is unique.
 //
 //   k_transpose_m  K (b h_kv) x s x d -> MT b x D x s (tokens contiguous), so
@@ -29,7 +29,7 @@
 //   k_gemm_xg      Y = X G (fp32, 64 x 64 tiles)
 //   k_syrk         W = Y Y^T in the pass's precision
 //   k_chol         W = L L^T in place, one CTA per sequence (shift on pass 1)
-//   k_trsm         Q = L^-1 Y, a thread per column of Y
+//   k_trsm         Q = L^-1 Y in fp32, eight lanes per column of Y
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -306,23 +306,27 @@ k_gemm_xg(const float* __restrict__ X, const float* __restrict__ G, float* __res
 }
 
 // ------------------------------------------------------ shifted CholeskyQR
-// W[seq] = Y Y^T (r x r) accumulated in S; tiles of 32 x 32 above the
-// diagonal, mirrored.
+constexpr int kSyrkSplit = 4;   // slices of D: W = sum of kSyrkSplit partial Gram matrices
+
+// Wp[slice][seq] = Y_slice Y_slice^T (r x r) accumulated in S over the
+// slice's D / kSyrkSplit columns; tiles of 32 x 32 above the diagonal,
+// mirrored.  The Cholesky kernel sums the slices in a fixed order.
 template <typename S>
 __global__ void __launch_bounds__(256)
-k_syrk(const float* __restrict__ Y, S* __restrict__ W, int r, int D) {
+k_syrk(const float* __restrict__ Y, S* __restrict__ Wp, int r, int D, int b) {
   const int bi = blockIdx.y, bj = blockIdx.x;
   if (bi > bj) return;
   __shared__ S Ys[2][32][33];
-  const int seq = blockIdx.z;
+  const int seq = blockIdx.z % b, slice = blockIdx.z / b;
+  const int dper = D / kSyrkSplit, d0 = slice * dper;
   const float* Yb = Y + static_cast<size_t>(seq) * r * D;
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   S acc[2][2] = {};
-  for (int k0 = 0; k0 < D; k0 += 32) {
+  for (int k0 = d0; k0 < d0 + dper; k0 += 32) {
     for (int e = tid; e < 2 * 32 * 32; e += 256) {
       const int w = e >> 10, rr = (e >> 5) & 31, kk = e & 31;
       const int row = (w ? bj : bi) * 32 + rr;
-      Ys[w][rr][kk] = (row < r && k0 + kk < D) ? static_cast<S>(Yb[static_cast<size_t>(row) * D + k0 + kk]) : S(0);
+      Ys[w][rr][kk] = (row < r) ? static_cast<S>(Yb[static_cast<size_t>(row) * D + k0 + kk]) : S(0);
     }
     __syncthreads();
 #pragma unroll 8
@@ -333,7 +337,7 @@ k_syrk(const float* __restrict__ Y, S* __restrict__ W, int r, int D) {
         for (int v = 0; v < 2; ++v) acc[u][v] += Ys[0][ty * 2 + u][kk] * Ys[1][tx * 2 + v][kk];
     __syncthreads();
   }
-  S* Wb = W + static_cast<size_t>(seq) * r * r;
+  S* Wb = Wp + (static_cast<size_t>(slice) * b + seq) * r * r;
 #pragma unroll
   for (int u = 0; u < 2; ++u)
 #pragma unroll
@@ -346,110 +350,155 @@ k_syrk(const float* __restrict__ Y, S* __restrict__ W, int r, int D) {
     }
 }
 
-// In-place Cholesky W = L L^T (lower triangle), one CTA per sequence, on a
-// shared-memory copy of the packed lower triangle when it fits (else in
-// place in global memory).  With `shift`, the diagonal first gets
-// 11 (D r + r (r + 1)) u tr(W) added (u the unit roundoff of S), the shift of
-// shifted CholeskyQR.  A zero W (zero keys) becomes the identity; any other
-// non-positive pivot is reported.
+// Cholesky W = L L^T of W = sum of the kSyrkSplit partials Wp[slice][seq],
+// one CTA (1024 threads) per sequence, on a shared-memory copy of the packed
+// lower triangle when it fits (else in place in the first partial); L is left
+// in the lower triangle of the first partial.  With `shift`, the diagonal
+// first gets 11 (D r + r (r + 1)) u tr(W) added (u the unit roundoff of S),
+// the shift of shifted CholeskyQR.  Per column: the scaled column into a
+// vector, then the trailing update, during which the thread that finishes
+// the next pivot also takes its square root (two barriers per column).  A
+// zero W (zero keys) becomes the identity; any other non-positive pivot is
+// reported.
 __host__ __device__ constexpr size_t chol_tri(int r) { return static_cast<size_t>(r) * (r + 1) / 2; }
+constexpr int kCholThreads = 1024;
 
 template <typename S>
-__global__ void __launch_bounds__(1024)
-k_chol(S* __restrict__ W, int r, int D, int shift, int in_smem, int* __restrict__ status) {
+__global__ void __launch_bounds__(kCholThreads)
+k_chol(S* __restrict__ Wp, int r, int D, int b, int shift, int in_smem, int* __restrict__ status) {
   extern __shared__ __align__(16) unsigned char csm[];
-  S* Wg = W + static_cast<size_t>(blockIdx.x) * r * r;
-  S* T = reinterpret_cast<S*>(csm);     // packed lower triangle: (i, k) at i (i + 1) / 2 + k
-  __shared__ S red[32];
+  const int seq = blockIdx.x;
+  const size_t rr = static_cast<size_t>(r) * r;
+  S* Wg = Wp + static_cast<size_t>(seq) * rr;                 // slice 0: holds W, then L
+  S* T = reinterpret_cast<S*>(csm);                           // packed lower triangle, row i at i (i + 1) / 2
+  S* col = T + (in_smem ? chol_tri(r) : 0);                   // scaled column j
+  __shared__ S red[kCholThreads / 32];
   __shared__ S s_inv;
   __shared__ int s_bad;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int NW = kCholThreads / 32;
   auto at = [&](int i, int k) -> S& {
     return in_smem ? T[static_cast<size_t>(i) * (i + 1) / 2 + k] : Wg[static_cast<size_t>(i) * r + k];
   };
+  // W = sum of the slices (fixed order), lower triangle
+  for (int i = warp; i < r; i += NW)
+    for (int k = lane; k <= i; k += 32) {
+      S w = Wg[static_cast<size_t>(i) * r + k];
+      for (int sl = 1; sl < kSyrkSplit; ++sl) w += Wp[(static_cast<size_t>(sl) * b + seq) * rr + static_cast<size_t>(i) * r + k];
+      if (in_smem) T[static_cast<size_t>(i) * (i + 1) / 2 + k] = w;
+      else Wg[static_cast<size_t>(i) * r + k] = w;
+    }
+  __syncthreads();
   S tr = 0;
-  for (int i = tid; i < r; i += blockDim.x) tr += Wg[static_cast<size_t>(i) * r + i];
+  for (int i = tid; i < r; i += kCholThreads) tr += at(i, i);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) tr += __shfl_xor_sync(0xffffffffu, tr, o);
   if (lane == 0) red[warp] = tr;
   if (tid == 0) s_bad = 0;
   __syncthreads();
-  if (tid == 0) {
-    S t = 0;
-    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) t += red[w];
-    red[0] = t;
-  }
-  __syncthreads();
-  const S trace = red[0];
+  S trace = 0;
+  for (int w = 0; w < NW; ++w) trace += red[w];
   if (trace == S(0)) {
-    for (int e = tid; e < r * r; e += blockDim.x) Wg[e] = (e / r == e % r) ? S(1) : S(0);
+    for (int e = tid; e < r * r; e += kCholThreads) Wg[e] = (e / r == e % r) ? S(1) : S(0);
     return;
   }
-  S sh = 0;
   if (shift) {
     const S u = sizeof(S) == 8 ? S(1.1102230246251565e-16) : S(5.9604645e-08);
-    sh = S(11) * (static_cast<S>(D) * r + static_cast<S>(r) * (r + 1)) * u * trace;
-  }
-  if (in_smem) {
-    for (int i = warp; i < r; i += 32)
-      for (int k = lane; k <= i; k += 32)
-        T[static_cast<size_t>(i) * (i + 1) / 2 + k] = Wg[static_cast<size_t>(i) * r + k] + (i == k ? sh : S(0));
-  } else if (shift) {
-    for (int i = tid; i < r; i += blockDim.x) Wg[static_cast<size_t>(i) * r + i] += sh;
+    const S sh = S(11) * (static_cast<S>(D) * r + static_cast<S>(r) * (r + 1)) * u * trace;
+    for (int i = tid; i < r; i += kCholThreads) at(i, i) += sh;
   }
   __syncthreads();
+  auto pivot = [&](int j) {
+    S dj = at(j, j);
+    if (!(dj > S(0))) {
+      s_bad = 1;
+      dj = S(1);
+    }
+    const S lj = sqrt(dj);
+    at(j, j) = lj;
+    s_inv = S(1) / lj;
+  };
+  if (tid == 0) pivot(0);
+  __syncthreads();
   for (int j = 0; j < r; ++j) {
-    if (tid == 0) {
-      S dj = at(j, j);
-      if (!(dj > S(0))) {
-        s_bad = 1;
-        dj = S(1);
-      }
-      const S lj = sqrt(dj);
-      at(j, j) = lj;
-      s_inv = S(1) / lj;
+    const S inv = s_inv;
+    S* cj = in_smem ? col : nullptr;
+    for (int i = j + 1 + tid; i < r; i += kCholThreads) {
+      const S l = at(i, j) * inv;
+      at(i, j) = l;
+      if (cj) cj[i] = l;
     }
     __syncthreads();
-    const S inv = s_inv;
-    for (int i = j + 1 + tid; i < r; i += blockDim.x) at(i, j) *= inv;
-    __syncthreads();
-    // trailing update of the lower triangle, row i handled by a warp
-    for (int i = j + 1 + warp; i < r; i += 32) {
-      const S lij = at(i, j);
-      for (int k = j + 1 + lane; k <= i; k += 32) at(i, k) -= lij * at(k, j);
+    // trailing update of the lower triangle, row i handled by a warp; the
+    // lane that finishes (j + 1, j + 1) takes the next pivot
+    for (int i = j + 1 + warp; i < r; i += NW) {
+      const S lij = cj ? cj[i] : at(i, j);
+      for (int k = j + 1 + lane; k <= i; k += 32) {
+        at(i, k) -= lij * (cj ? cj[k] : at(k, j));
+        if (i == j + 1 && k == j + 1) pivot(j + 1);
+      }
     }
     __syncthreads();
   }
   if (in_smem) {
-    for (int e = tid; e < r * r; e += blockDim.x) {
-      const int i = e / r, k = e - (e / r) * r;
-      if (k <= i) Wg[e] = T[static_cast<size_t>(i) * (i + 1) / 2 + k];
-    }
+    for (int i = warp; i < r; i += NW)
+      for (int k = lane; k <= i; k += 32) Wg[static_cast<size_t>(i) * r + k] = T[static_cast<size_t>(i) * (i + 1) / 2 + k];
   }
   if (tid == 0 && s_bad) flag_error(status, DEV_NUMERIC);
 }
 
-// Q = L^-1 Y by forward substitution, a thread per column of Y (64 columns
-// per CTA), the column's partial results in shared memory.
+// Q = L^-1 Y by forward substitution in fp32: eight lanes per column of Y
+// (32 columns per 256-thread CTA), each summing every eighth term of a row's
+// inner product, combined by shuffles; L's packed lower triangle (rounded to
+// fp32) and the columns' results in shared memory.  After the shifted first
+// pass cond(L) is a few thousand at most, so fp32 substitution leaves Q
+// orthogonal to ~1e-3 or better, which the two plain passes that follow
+// remove.
+constexpr int kTrCols = 32;
 template <typename S>
-__global__ void __launch_bounds__(64) k_trsm(const S* __restrict__ L, const float* __restrict__ Y,
-                                              float* __restrict__ Q, int r, int D) {
+__global__ void __launch_bounds__(256) k_trsm(const S* __restrict__ L, const float* __restrict__ Y,
+                                               float* __restrict__ Q, int r, int D) {
   extern __shared__ __align__(16) unsigned char tsm[];
-  S* q = reinterpret_cast<S*>(tsm);      // [r][64]
-  const int seq = blockIdx.y, c = blockIdx.x * 64 + threadIdx.x;
+  float* Lp = reinterpret_cast<float*>(tsm);             // packed lower triangle, row i at i (i + 1) / 2
+  float* q = Lp + (chol_tri(r) + 3) / 4 * 4;             // [r][kTrCols]
+  const int seq = blockIdx.y, tid = threadIdx.x;
+  const int lc = tid >> 3, part = tid & 7;               // column within the CTA, lane within the column
+  const int c = blockIdx.x * kTrCols + lc;
   const S* Lb = L + static_cast<size_t>(seq) * r * r;
+  for (int e = tid; e < r * r; e += 256) {
+    const int i = e / r, k = e - (e / r) * r;
+    if (k <= i) Lp[static_cast<size_t>(i) * (i + 1) / 2 + k] = static_cast<float>(Lb[e]);
+  }
+  __syncthreads();
+  const bool live = c < D;
   const float* Yb = Y + static_cast<size_t>(seq) * r * D;
   float* Qb = Q + static_cast<size_t>(seq) * r * D;
-  if (c >= D) return;
+  // the CTA's columns of Y, loaded once; row i's entry is replaced by the
+  // solution once it is known (it is read only for the rows after it)
+  const int c0 = blockIdx.x * kTrCols;
+  for (int e = tid; e < r * kTrCols; e += 256) {
+    const int i = e / kTrCols, cc = e - (e / kTrCols) * kTrCols;
+    q[e] = c0 + cc < D ? Yb[static_cast<size_t>(i) * D + c0 + cc] : 0.f;
+  }
+  __syncthreads();
   for (int i = 0; i < r; ++i) {
-    S acc = static_cast<S>(Yb[static_cast<size_t>(i) * D + c]);
-    const S* Li = Lb + static_cast<size_t>(i) * r;
-    for (int k = 0; k < i; ++k) acc -= Li[k] * q[k * 64 + threadIdx.x];
-    acc /= Li[i];
-    q[i * 64 + threadIdx.x] = acc;
-    Qb[static_cast<size_t>(i) * D + c] = static_cast<float>(acc);
+    const float* Li = Lp + static_cast<size_t>(i) * (i + 1) / 2;
+    float a = 0.f;
+    for (int k = part; k < i; k += 8) a = fmaf(Li[k], q[k * kTrCols + lc], a);
+    a += __shfl_xor_sync(0xffffffffu, a, 1);
+    a += __shfl_xor_sync(0xffffffffu, a, 2);
+    a += __shfl_xor_sync(0xffffffffu, a, 4);
+    const float x = (q[i * kTrCols + lc] - a) / Li[i];
+    __syncwarp();
+    if (part == 0) {
+      q[i * kTrCols + lc] = x;
+      if (live) Qb[static_cast<size_t>(i) * D + c] = x;
+    }
+    __syncwarp();
   }
 }
+
+static size_t trsm_smem(int r) { return ((chol_tri(r) + 3) / 4 * 4 + static_cast<size_t>(r) * kTrCols) * sizeof(float); }
 
 // ------------------------------------------------------- A = M X^T (tcgen05)
 // Unit = 128 tokens of one sequence.  Per 64-dimension block of M (one KV
@@ -666,7 +715,7 @@ size_t svd_tc_workspace_bytes(const shadowkv_params& p, int nsm) {
   const size_t ntile = D / kGmTile, npairs = ntile * (ntile + 1) / 2;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   return up(b * D * s * 2) + up(b * nz * npairs * kGmTile * kGmTile * 4) + up(b * D * D * 4) +
-         up(b * r * D * 4) + up(b * r * r * 8) + 2 * up(b * r * D * 2);
+         up(b * r * D * 4) + up(kSyrkSplit * b * r * r * 8) + 2 * up(b * r * D * 2);
 }
 
 #define SVD_TRY(...)                    \
@@ -680,28 +729,27 @@ size_t svd_tc_workspace_bytes(const shadowkv_params& p, int nsm) {
 static cudaError_t orth_rows(Ctx& c, float* Y, float* X, void* W, cudaStream_t st) {
   const int b = c.p.b, r = c.p.r, D = c.p.h_kv * c.p.d;
   const int nt = (r + 31) / 32;
-  const dim3 gs(nt, nt, b);
-  const dim3 gt((D + 63) / 64, b);
+  const dim3 gs(nt, nt, b * kSyrkSplit);
+  const dim3 gt((D + kTrCols - 1) / kTrCols, b);
+  SVD_TRY(set_smem_once(reinterpret_cast<const void*>(k_trsm<double>), static_cast<int>(trsm_smem(r))));
+  SVD_TRY(set_smem_once(reinterpret_cast<const void*>(k_trsm<float>), static_cast<int>(trsm_smem(r))));
   for (int pass = 0; pass < 3; ++pass) {
-    const float* in = pass == 0 ? Y : X;
+    const float* in = pass == 1 ? X : Y;
     float* out = pass == 1 ? Y : X;   // Y -> X -> Y -> X
-    if (pass == 2) in = Y;
     kbegin(c, K_ORTH, st);
     if (pass == 0) {
-      const size_t cs = chol_tri(r) * 8;
+      const size_t cs = (chol_tri(r) + r) * 8;
       const int sm = cs <= 200 * 1024;
       if (sm) SVD_TRY(set_smem_once(reinterpret_cast<const void*>(k_chol<double>), static_cast<int>(cs)));
-      k_syrk<double><<<gs, 256, 0, st>>>(in, static_cast<double*>(W), r, D);
-      k_chol<double><<<b, 1024, sm ? cs : 0, st>>>(static_cast<double*>(W), r, D, 1, sm, c.status);
-      SVD_TRY(set_smem_once(reinterpret_cast<const void*>(k_trsm<double>), r * 64 * 8));
-      k_trsm<double><<<gt, 64, r * 64 * 8, st>>>(static_cast<const double*>(W), in, out, r, D);
+      k_syrk<double><<<gs, 256, 0, st>>>(in, static_cast<double*>(W), r, D, b);
+      k_chol<double><<<b, kCholThreads, sm ? cs : 0, st>>>(static_cast<double*>(W), r, D, b, 1, sm, c.status);
+      k_trsm<double><<<gt, 256, trsm_smem(r), st>>>(static_cast<const double*>(W), in, out, r, D);
     } else {
-      const size_t cs = chol_tri(r) * 4;
+      const size_t cs = (chol_tri(r) + r) * 4;
       SVD_TRY(set_smem_once(reinterpret_cast<const void*>(k_chol<float>), static_cast<int>(cs)));
-      k_syrk<float><<<gs, 256, 0, st>>>(in, static_cast<float*>(W), r, D);
-      k_chol<float><<<b, 1024, cs, st>>>(static_cast<float*>(W), r, D, 0, 1, c.status);
-      SVD_TRY(set_smem_once(reinterpret_cast<const void*>(k_trsm<float>), r * 64 * 4));
-      k_trsm<float><<<gt, 64, r * 64 * 4, st>>>(static_cast<const float*>(W), in, out, r, D);
+      k_syrk<float><<<gs, 256, 0, st>>>(in, static_cast<float*>(W), r, D, b);
+      k_chol<float><<<b, kCholThreads, cs, st>>>(static_cast<float*>(W), r, D, b, 0, 1, c.status);
+      k_trsm<float><<<gt, 256, trsm_smem(r), st>>>(static_cast<const float*>(W), in, out, r, D);
     }
     kend(c, K_ORTH, st);
     SVD_TRY(cudaGetLastError());
@@ -761,7 +809,7 @@ cudaError_t svd_tc_basis(Ctx& c, const void* Kv, void* ws, cudaStream_t st) {
   kend(c, K_MISC, st);
   SVD_TRY(cudaGetLastError());
 
-  bf16* Xh = reinterpret_cast<bf16*>(cur + (static_cast<size_t>(b) * r * r * 8 + 255) / 256 * 256);
+  bf16* Xh = reinterpret_cast<bf16*>(cur + (static_cast<size_t>(kSyrkSplit) * b * r * r * 8 + 255) / 256 * 256);
   bf16* Xl = Xh + (static_cast<size_t>(b) * r * D * 2 + 255) / 256 * 128;
 
   // subspace iteration on G from a seeded Gaussian start
