@@ -30,6 +30,7 @@ from __future__ import annotations
 
 import argparse
 import ctypes
+import gc
 import hashlib
 import json
 import os
@@ -362,10 +363,21 @@ def run_ours(args, cfg):
             import torch.distributed as dist
             dist.barrier()
 
-    def steps(t0, t1):
+    # every step's C-ABI call with its arguments marshalled in advance, so the
+    # timed loops allocate no Python objects (and no collection can run)
+    calls = [[ctx.prepared_step(q[t], kn[t], vn[t], out, stream) for ctx in ctxs] for t in range(W + K)]
+    host_gap = [0.0]
+
+    def steps(t0, t1, watch=False):
+        last = time.perf_counter()
         for t in range(t0, t1):
-            for ctx in ctxs:
-                ctx.decode_step(q[t], kn[t], vn[t], out, stream)
+            for call in calls[t]:
+                call()
+            if watch:
+                now = time.perf_counter()
+                if now - last > host_gap[0]:
+                    host_gap[0] = now - last
+                last = now
 
     def decode_pass(timing: bool, cache: bool = True):
         for ctx in ctxs:
@@ -379,10 +391,13 @@ def run_ours(args, cfg):
         barrier()
         torch.cuda.synchronize()
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        gc.collect()
+        gc.disable()
         ev0.record(stream)
-        steps(W, W + K)
+        steps(W, W + K, watch=not timing)
         ev1.record(stream)
         torch.cuda.synchronize()
+        gc.enable()
         barrier()
         st1 = [ctx.stats() for ctx in ctxs]
         ms = ev0.elapsed_time(ev1)
@@ -424,15 +439,21 @@ def run_ours(args, cfg):
     qd, knd, vnd = blk[:nq].view_as(q[0]), blk[nq:nq + nk].view_as(kn[0]), blk[nq + nk:].view_as(vn[0])
     outh = torch.empty(out.shape, dtype=dt).pin_memory()
     steps(0, W)
+    e2e_calls = [ctx.prepared_step(qd, knd, vnd, outh if li == L - 1 else out, stream)
+                 for li, ctx in enumerate(ctxs)]
+    rows = [host[t] for t in range(W + K)]
     torch.cuda.synchronize()
     barrier()
+    gc.collect()
+    gc.disable()
     t0 = time.perf_counter()
     for t in range(W, W + K):
-        blk.copy_(host[t], non_blocking=True)
-        for li, ctx in enumerate(ctxs):
-            ctx.decode_step(qd, knd, vnd, outh if li == L - 1 else out, stream)
+        blk.copy_(rows[t], non_blocking=True)
+        for call in e2e_calls:
+            call()
         stream.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, dev)
+    gc.enable()
     barrier()
     h2d = per * E
     d2h = out.numel() * E
@@ -506,6 +527,7 @@ def run_ours(args, cfg):
             "e2e": {"value": job_tokens_per_s(ws, cfg.b, e2e_s * 1e3 / K / L), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches,
+            "host_max_step_gap_us": host_gap[0] * 1e6,
             "clocks": clk.summary(),
         }
         if svd is not None:

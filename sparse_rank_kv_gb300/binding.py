@@ -187,6 +187,19 @@ class Context:
         _check(lib().shadowkv_decode_step(self._h, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out),
                                           _stream(stream)))
 
+    def prepared_step(self, q, k_new, v_new, out, stream=None):
+        """A callable that makes the decode_step call on these fixed buffers,
+        with the arguments marshalled once (a decode loop that reuses its
+        buffers saves that work on every step)."""
+        fn = lib().shadowkv_decode_step
+        args = (self._h, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out), _stream(stream))
+
+        def step():
+            rc = fn(*args)
+            if rc:
+                _check(rc)
+        return step
+
     def rewind(self, stream=None):
         _check(lib().shadowkv_rewind(self._h, _stream(stream)))
 
