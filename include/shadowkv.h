@@ -167,6 +167,20 @@ skv_status shadowkv_load_state(const shadowkv_params* p, const shadowkv_state_in
 skv_status shadowkv_decode_step(shadowkv_ctx* ctx, const void* q, const void* k_new,
                                 const void* v_new, void* out, void* stream);
 
+/* The same step with the token's inputs and output in host memory (the call
+ * a caller makes whose decode loop lives on the CPU side):
+ *   q     : host, b x h_q x d (copied into a library-owned device buffer)
+ *   k_new, v_new : host, b x h_kv x d, or NULL; read in place through their
+ *           device mapping when they are pinned host memory, else copied
+ *   out   : host, b x h_q x d; written in place by the attention when it is
+ *           pinned host memory, else copied back after the step
+ * Pinned (page-locked) buffers make every copy asynchronous on `stream`;
+ * the result is in `out` once `stream` has passed the call.  Pageable
+ * buffers work too, with the copies the CUDA runtime makes for them.  The
+ * pinned-or-not answer is cached per address (the last 8 addresses). */
+skv_status shadowkv_decode_step_host(shadowkv_ctx* ctx, const void* q, const void* k_new,
+                                     const void* v_new, void* out, void* stream);
+
 /* Returns the context to its state right after prefill / load_state: the
  * appended tokens are dropped (the local window holds the w prompt tokens
  * again) and the chunk cache is emptied.  Stream-ordered on `stream` after

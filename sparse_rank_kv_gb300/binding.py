@@ -87,6 +87,7 @@ def lib() -> ctypes.CDLL:
             "shadowkv_prefill": (I, [P(Params), V, V, I, V, P(V)]),
             "shadowkv_load_state": (I, [P(Params), P(StateIn), V, P(V)]),
             "shadowkv_decode_step": (I, [V, V, V, V, V, V]),
+            "shadowkv_decode_step_host": (I, [V, V, V, V, V, V]),
             "shadowkv_free": (None, [V]),
             "shadowkv_rewind": (I, [V, V]),
             "shadowkv_last_error": (ctypes.c_char_p, []),
@@ -187,11 +188,16 @@ class Context:
         _check(lib().shadowkv_decode_step(self._h, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out),
                                           _stream(stream)))
 
-    def prepared_step(self, q, k_new, v_new, out, stream=None):
-        """A callable that makes the decode_step call on these fixed buffers,
-        with the arguments marshalled once (a decode loop that reuses its
-        buffers saves that work on every step)."""
-        fn = lib().shadowkv_decode_step
+    def decode_step_host(self, q, k_new, v_new, out, stream=None):
+        """decode_step on host tensors (pinned for asynchronous copies)."""
+        _check(lib().shadowkv_decode_step_host(self._h, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out),
+                                               _stream(stream)))
+
+    def prepared_step(self, q, k_new, v_new, out, stream=None, host=False):
+        """A callable that makes the decode_step call (decode_step_host with
+        host=True) on these fixed buffers, with the arguments marshalled once
+        (a decode loop that reuses its buffers saves that work on every step)."""
+        fn = lib().shadowkv_decode_step_host if host else lib().shadowkv_decode_step
         args = (self._h, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out), _stream(stream))
 
         def step():

@@ -77,12 +77,13 @@ struct Sizes {
   size_t min_cos, logits, score_part, attn_part, basis, rope_tab;
   size_t out_ids, out_mask, sel, sel_slot, slot_chunk, miss_chunk, miss_slot;
   size_t miss_count, miss_base, att_slot, at_ctr, hits, attn_count, counters, status;
+  size_t q_stage, kv_stage, out_stage;
   size_t total() const {
     const size_t v[] = {A, Bt, L, K_out, V_out, K_loc, V_loc, slot_V, K_sparse, KV_out, KV_loc, KV_slot,
                         min_cos, logits,
                         score_part, attn_part, basis, rope_tab, out_ids, out_mask, sel, sel_slot,
                         slot_chunk, miss_chunk, miss_slot, miss_count, miss_base, att_slot, at_ctr, hits, attn_count, counters,
-                        status};
+                        status, q_stage, kv_stage, out_stage};
     size_t t = 0;
     for (size_t x : v) t += up(x);
     return t;
@@ -132,6 +133,9 @@ Sizes sizes_of(const shadowkv_params& p) {
   z.miss_count = 2 * 4;   // compact miss-list length per step parity
   z.counters = 2 * 8;
   z.status = 4;
+  // staging buffers of shadowkv_decode_step_host: q, (k_new, v_new), out
+  z.q_stage = z.out_stage = b * hq * d * E;
+  z.kv_stage = 2 * b * h * d * E;
   return z;
 }
 
@@ -292,6 +296,9 @@ skv_status create(const shadowkv_params* p, cudaStream_t st, shadowkv_ctx** out)
   c.attn_count = static_cast<int32_t*>(take(z.attn_count));
   c.counters = static_cast<unsigned long long*>(take(z.counters));
   c.status = static_cast<int*>(take(z.status));
+  c.q_stage = take(z.q_stage);
+  c.kv_stage = take(z.kv_stage);
+  c.out_stage = take(z.out_stage);
 
   // small state: zeroed; the cache starts empty
   const size_t small0 = static_cast<size_t>(reinterpret_cast<char*>(c.out_ids) - c.arena);
@@ -354,6 +361,56 @@ struct DeviceGuard {
     if (prev >= 0 && cudaGetDevice(&now) == cudaSuccess && now != prev) cudaSetDevice(prev);
   }
 };
+
+// The decode step's launches (arguments already checked).
+skv_status enqueue_step(skv::Ctx& c, const void* q, const void* k_new, const void* v_new, void* out,
+                        cudaStream_t st) {
+  const int loc_row = c.p.w + c.n_app;
+  const int n_loc = loc_row + (k_new ? 1 : 0);
+  CK(skv::launch_score(c, q, st));
+  CK(skv::launch_select(c, k_new, v_new, loc_row, st));
+  // the value fetch overlaps the key rebuild: CTAs of the rebuild's own
+  // launch, or a kernel on the side stream
+  const bool fused = skv::rebuild_fetches(c);
+  if (!fused) {
+    CK(cudaEventRecord(c.ev_fork, st));
+    CK(cudaStreamWaitEvent(c.side, c.ev_fork, 0));
+    CK(skv::launch_fetch(c, c.side));
+    CK(cudaEventRecord(c.ev_join, c.side));
+  }
+  CK(skv::launch_rebuild(c, st));
+  if (!fused) CK(cudaStreamWaitEvent(st, c.ev_join, 0));
+  CK(skv::launch_attn(c, q, out, n_loc, st));
+  if (k_new) ++c.n_app;
+  ++c.t;
+  return SKV_OK;
+}
+
+// *dev = the device address of host pointer p when p is pinned host memory
+// mapped into the device's address space (else nullptr).  The last few
+// answers are cached by address.
+cudaError_t mapped_view(skv::Ctx& c, const void* p, const void** dev) {
+  *dev = nullptr;
+  if (!p) return cudaSuccess;
+  for (size_t i = 0; i < c.map_cache.size(); ++i)
+    if (c.map_cache[i].first == p) {
+      *dev = c.map_cache[i].second;
+      // most recently used last, so a buffer used every step stays cached
+      std::rotate(c.map_cache.begin() + i, c.map_cache.begin() + i + 1, c.map_cache.end());
+      return cudaSuccess;
+    }
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();   // pageable memory on older drivers: not mapped
+    a.type = cudaMemoryTypeUnregistered;
+  }
+  const void* d = (a.type == cudaMemoryTypeHost && a.devicePointer) ? a.devicePointer : nullptr;
+  if (c.map_cache.size() >= 8) c.map_cache.erase(c.map_cache.begin());
+  c.map_cache.emplace_back(p, d);
+  *dev = d;
+  return cudaSuccess;
+}
 
 }  // namespace
 
@@ -530,25 +587,43 @@ skv_status shadowkv_decode_step(shadowkv_ctx* h, const void* q, const void* k_ne
   if (k_new && c.n_app >= c.p.max_new)
     return fail(SKV_ERR_STATE, "local window full: %d tokens appended (max_new)", c.n_app);
   DeviceGuard g(c.device);
+  return enqueue_step(c, q, k_new, v_new, out, static_cast<cudaStream_t>(stream));
+}
+
+skv_status shadowkv_decode_step_host(shadowkv_ctx* h, const void* q, const void* k_new, const void* v_new,
+                                     void* out, void* stream) {
+  if (!h) return fail(SKV_ERR_INVALID_ARG, "ctx is NULL");
+  if (!q || !out) return fail(SKV_ERR_INVALID_ARG, "q and out must be non-NULL");
+  if ((k_new == nullptr) != (v_new == nullptr)) return fail(SKV_ERR_INVALID_ARG, "k_new and v_new must both be given or both NULL");
+  skv::Ctx& c = h->c;
+  if (k_new && c.n_app >= c.p.max_new)
+    return fail(SKV_ERR_STATE, "local window full: %d tokens appended (max_new)", c.n_app);
+  DeviceGuard g(c.device);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int loc_row = c.p.w + c.n_app;
-  const int n_loc = loc_row + (k_new ? 1 : 0);
-  CK(skv::launch_score(c, q, st));
-  CK(skv::launch_select(c, k_new, v_new, loc_row, st));
-  // the value fetch overlaps the key rebuild: CTAs of the rebuild's own
-  // launch, or a kernel on the side stream
-  const bool fused = skv::rebuild_fetches(c);
-  if (!fused) {
-    CK(cudaEventRecord(c.ev_fork, st));
-    CK(cudaStreamWaitEvent(c.side, c.ev_fork, 0));
-    CK(skv::launch_fetch(c, c.side));
-    CK(cudaEventRecord(c.ev_join, c.side));
+  const size_t qb = static_cast<size_t>(c.p.b) * c.p.h_q * c.p.d * c.E;
+  const size_t kb = static_cast<size_t>(c.p.b) * c.p.h_kv * c.p.d * c.E;
+  // q goes to the staging buffer (the tensor maps stay cached on its address);
+  // k_new, v_new and out are used through their device mapping when they
+  // are pinned host memory, else staged
+  const void* kd = nullptr;
+  const void* vd = nullptr;
+  const void* oview = nullptr;
+  CK(mapped_view(c, k_new, &kd));
+  CK(mapped_view(c, v_new, &vd));
+  CK(mapped_view(c, out, &oview));
+  void* od = const_cast<void*>(oview);
+  CK(cudaMemcpyAsync(c.q_stage, q, qb, cudaMemcpyHostToDevice, st));
+  if (k_new && !kd) {
+    CK(cudaMemcpyAsync(c.kv_stage, k_new, kb, cudaMemcpyHostToDevice, st));
+    kd = c.kv_stage;
   }
-  CK(skv::launch_rebuild(c, st));
-  if (!fused) CK(cudaStreamWaitEvent(st, c.ev_join, 0));
-  CK(skv::launch_attn(c, q, out, n_loc, st));
-  if (k_new) ++c.n_app;
-  ++c.t;
+  if (v_new && !vd) {
+    CK(cudaMemcpyAsync(static_cast<char*>(c.kv_stage) + kb, v_new, kb, cudaMemcpyHostToDevice, st));
+    vd = static_cast<char*>(c.kv_stage) + kb;
+  }
+  skv_status s = enqueue_step(c, c.q_stage, kd, vd, od ? od : c.out_stage, st);
+  if (s != SKV_OK) return s;
+  if (!od) CK(cudaMemcpyAsync(out, c.out_stage, qb, cudaMemcpyDeviceToHost, st));
   return SKV_OK;
 }
 

@@ -79,6 +79,10 @@ struct Ctx {
   uint32_t* out_mask = nullptr;
   unsigned long long* counters = nullptr;  // [0] hits, [1] misses
   int* status = nullptr;
+  // staging of shadowkv_decode_step_host, and the host pointers it has seen
+  // (address -> device address when pinned and mapped, else nullptr)
+  void *q_stage = nullptr, *kv_stage = nullptr, *out_stage = nullptr;
+  std::vector<std::pair<const void*, const void*>> map_cache;
 
   // pinned host copy of V (mapped)
   void* v_cpu = nullptr;

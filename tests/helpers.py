@@ -121,5 +121,7 @@ def ey_bound(cfg, lam):
         return 1.01
     lam = np.sort(np.asarray(lam, np.float64))
     opt = lam[: lam.size - cfg.r].sum()
+    if opt <= 0.0:
+        return 1.01          # r covers every direction: exact up to roundoff
     noise = lam[: lam.size - cfg.rank_true]
     return (noise.sum() - m * noise.mean()) / opt * (1.0 + 1e-6)

@@ -88,6 +88,7 @@ def test_null_arguments_are_rejected_without_gpu(lib):
     p = binding.make_params(CONFIGS["tiny_f32_s1k"])
     assert lib.shadowkv_prefill(ctypes.byref(p), None, None, 0, None, ctypes.byref(out)) == 1
     assert lib.shadowkv_decode_step(None, None, None, None, None, None) == 1
+    assert lib.shadowkv_decode_step_host(None, None, None, None, None, None) == 1
     assert lib.shadowkv_set_option(None, 0, 1) == 1
     lib.shadowkv_free(None)   # NULL-safe
 

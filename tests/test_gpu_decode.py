@@ -323,3 +323,28 @@ def test_misaligned_queries_are_rejected_before_any_work():
     assert after.hits == before.hits and after.misses == before.misses and after.launches == before.launches
     ctx.decode_step(q, st["k_new"][0], st["v_new"][0], out)
     ctx.check()
+
+
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+def test_host_buffer_step_equals_device_step(pinned):
+    """shadowkv_decode_step_host (inputs and output in host memory) runs the
+    same step as shadowkv_decode_step on device buffers: identical selections
+    and hits, bit-identical outputs, over steps with a warm cache."""
+    cfg = SMALL.with_(steps=5, seed=64)
+    st = synth.make_state(cfg, device="cuda")
+    p = binding.make_params(cfg)
+    dev_ctx, host_ctx = binding.load_state(p, st), binding.load_state(p, st)
+    dt = synth.torch_dtype(cfg.dtype)
+    host = lambda t: t.cpu().pin_memory() if pinned else t.cpu()
+    out_h = host(torch.empty(cfg.b, cfg.h_q, cfg.d, dtype=dt))
+    stream = torch.cuda.current_stream()
+    for t in range(cfg.steps):
+        out_d = torch.empty(cfg.b, cfg.h_q, cfg.d, dtype=dt, device="cuda")
+        dev_ctx.decode_step(st["q"][t], st["k_new"][t], st["v_new"][t], out_d)
+        host_ctx.decode_step_host(host(st["q"][t]), host(st["k_new"][t]), host(st["v_new"][t]), out_h, stream)
+        torch.cuda.synchronize()
+        for f in ("SEL", "HITS"):
+            assert torch.equal(dev_ctx.export(f), host_ctx.export(f)), f"step {t}: {f}"
+        assert torch.equal(out_d.cpu(), out_h), f"step {t}: outputs differ"
+    dev_ctx.check()
+    host_ctx.check()

@@ -71,6 +71,14 @@ def decode_against_oracle(cfg, ctx, inp, steps, bsel=None, rows=False, report_ex
         if rows:
             ks = np64(ctx.export("K_SPARSE").view(b, h, k * c, d)[sl])
             assert np.abs(ks - res.K_sparse).max() <= 8e-3 * np.abs(res.K_sparse).max(), f"step {t}: rebuilt keys"
+            lg = ctx.export("LOGITS").view(b, hq, -1).numpy()[sl].astype(np.float64)
+            m = ~np.isnan(res.P)
+            lerr = np.abs(lg[m] - res.P[m]).max() / np.abs(res.P[m]).max()
+            if report_exact:
+                print(f"step {t}: logits error {lerr:.2e} of the largest logit")
+            # 128 exact bf16 products summed in fp32 in the tensor cores' order:
+            # worst case d * 2^-24 = 7.6e-6 of sum |q_i L_i|; 1.5-2.3e-7 measured.
+            assert lerr <= 1e-5, f"step {t}: logits {lerr:.3g}"
     ctx.check()
     return worst, (float(np.mean(alpha)) if alpha else None)
 

@@ -201,3 +201,21 @@ def test_full_size_32k_prefill_eckart_young_and_stats():
     check_selection(ctx.export("OUTLIER_IDS").view(b, h, cfg.o).numpy(), -mref, cfg.o,
                     what="outliers")
     check_factors(cfg, ctx, inp)
+
+
+@pytest.mark.parametrize("shape", [
+    dict(r=256, rank_true=200, seed=57),            # r = h_kv d: Cholesky of the fp64 pass in global memory, 2-stage factor
+    dict(d=64, theta=1e4, r=48, seed=58),           # 64-dim heads: one 64-column block per head in the transpose and factor
+    dict(r=16, rank_true=12, seed=59),              # the smallest rank the tensor-core path takes
+], ids=["r256", "d64", "r16"])
+def test_tensor_core_svd_shapes(shape):
+    """Shapes at the edges of the tensor-core SVD: landmarks and outliers
+    against the oracle, the factors against the Eckart-Young bars."""
+    cfg = SMALL.with_(**shape)
+    inp = synth.make_inputs(cfg, device="cuda")
+    ctx = gpu_prefill(cfg, inp)
+    assert ctx.layout()["tc_rebuild"] == (cfg.r % 16 == 0)
+    ost = O.prefill(np64(inp["k_pre"]), np64(inp["v"]), cfg.c, cfg.r, cfg.o, cfg.w, cfg.theta)
+    check_stats_and_gathers(cfg, ctx, inp, ost)
+    check_factors(cfg, ctx, inp)
+    ctx.check()
