@@ -475,17 +475,24 @@ def run_ours(args, cfg):
         hbm = hbm_bytes_per_step(cfg, E, n_loc_avg)
         hbm_rec = hbm_bytes_per_step(cfg, E, n_loc_avg, alpha, records=True) if layout["kv_records"] else None
         link = misses / K / L * cfg.c * cfg.d * E
-        fetch_kid = "rebuild" if layout["fetch_in_rebuild"] else "fetch"
-        fetch_in = "rebuild launch (fetch CTAs inside it)" if layout["fetch_in_rebuild"] else "fetch launch"
+        if layout["fetch_in_attention"]:
+            fetch_kid, fetch_in = "attention", "attention launch (fetch warps inside it)"
+        elif layout["fetch_in_rebuild"]:
+            fetch_kid, fetch_in = "rebuild", "rebuild launch (fetch CTAs inside it)"
+        else:
+            fetch_kid, fetch_in = "fetch", "fetch launch"
 
         def rate(kts, nmiss):
             ms_, n_ = kts[fetch_kid]
             byts = nmiss / K / L * cfg.c * cfg.d * E
             return byts / (ms_ / max(1, n_) * 1e-3) / 1e9 if ms_ > 0 else 0.0
 
-        fetch_gbs = rate(kt, misses)
+        # with the fetch inside the attention's launch, only the cache-off pass
+        # (every selected chunk fetched, the launch's time set by the link)
+        # measures the host link through it
+        fetch_gbs = None if layout["fetch_in_attention"] else rate(kt, misses)
         fetch_off_gbs = rate(kt_off, miss_off)
-        link_gbs = max(max(bulk.values()), fetch_gbs, fetch_off_gbs)
+        link_gbs = max(max(bulk.values()), fetch_off_gbs, fetch_gbs or 0.0)
         t_roof = hbm / (hbm_gbs * 1e9) + link / (link_gbs * 1e9)
         score_ms, score_n = kt["score"]
         land, extra = score_bytes(cfg, E)

@@ -225,6 +225,9 @@ typedef struct shadowkv_layout {
   int tc_rebuild;       /* key rebuild on the tensor cores */
   int tc_attention;     /* attention on the tensor cores over K/V records */
   int fetch_in_rebuild; /* value fetch runs as CTAs of the rebuild launch (one stream) */
+  int fetch_in_attention; /* value fetch runs as warps of the tensor-core attention's
+                           launch; each missed chunk is attended as soon as its
+                           values are in its cache slot */
 } shadowkv_layout;
 skv_status shadowkv_get_layout(const shadowkv_ctx* ctx, shadowkv_layout* out);
 

@@ -59,7 +59,7 @@ class StateIn(ctypes.Structure):
 class Layout(ctypes.Structure):
     _fields_ = [("kv_records", ctypes.c_int), ("a_tiled", ctypes.c_int), ("tc_score", ctypes.c_int),
                 ("tc_rebuild", ctypes.c_int), ("tc_attention", ctypes.c_int),
-                ("fetch_in_rebuild", ctypes.c_int)]
+                ("fetch_in_rebuild", ctypes.c_int), ("fetch_in_attention", ctypes.c_int)]
 
 
 class Stats(ctypes.Structure):

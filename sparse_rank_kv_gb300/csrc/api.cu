@@ -76,13 +76,14 @@ struct Sizes {
   size_t A, Bt, L, K_out, V_out, K_loc, V_loc, slot_V, K_sparse, KV_out, KV_loc, KV_slot;
   size_t min_cos, logits, score_part, attn_part, basis, rope_tab;
   size_t out_ids, out_mask, sel, sel_slot, slot_chunk, miss_chunk, miss_slot;
-  size_t miss_count, miss_base, att_slot, at_ctr, hits, attn_count, counters, status;
+  size_t miss_count, miss_base, att_slot, at_ctr, item_done, hits, attn_count, counters, status;
   size_t q_stage, kv_stage, out_stage;
   size_t total() const {
     const size_t v[] = {A, Bt, L, K_out, V_out, K_loc, V_loc, slot_V, K_sparse, KV_out, KV_loc, KV_slot,
                         min_cos, logits,
                         score_part, attn_part, basis, rope_tab, out_ids, out_mask, sel, sel_slot,
-                        slot_chunk, miss_chunk, miss_slot, miss_count, miss_base, att_slot, at_ctr, hits, attn_count, counters,
+                        slot_chunk, miss_chunk, miss_slot, miss_count, miss_base, att_slot, at_ctr, item_done, hits, attn_count,
+                        counters,
                         status, q_stage, kv_stage, out_stage};
     size_t t = 0;
     for (size_t x : v) t += up(x);
@@ -130,6 +131,7 @@ Sizes sizes_of(const shadowkv_params& p) {
   z.hits = z.attn_count = z.miss_base = b * h * 4;
   z.att_slot = rec ? b * h * k * 4 : 0;
   z.at_ctr = rec ? 8 * 4 : 0;
+  z.item_done = rec ? b * h * k * 4 : 0;   // at most k phase-1 attention items per head
   z.miss_count = 2 * 4;   // compact miss-list length per step parity
   z.counters = 2 * 8;
   z.status = 4;
@@ -292,6 +294,7 @@ skv_status create(const shadowkv_params* p, cudaStream_t st, shadowkv_ctx** out)
   c.miss_base = static_cast<int32_t*>(take(z.miss_base));
   c.att_slot = c.kv_rec ? static_cast<int32_t*>(take(z.att_slot)) : nullptr;
   c.at_ctr = c.kv_rec ? static_cast<int32_t*>(take(z.at_ctr)) : nullptr;
+  c.item_done = c.kv_rec ? static_cast<int32_t*>(take(z.item_done)) : nullptr;
   c.hits = static_cast<int32_t*>(take(z.hits));
   c.attn_count = static_cast<int32_t*>(take(z.attn_count));
   c.counters = static_cast<unsigned long long*>(take(z.counters));
@@ -369,9 +372,9 @@ skv_status enqueue_step(skv::Ctx& c, const void* q, const void* k_new, const voi
   const int n_loc = loc_row + (k_new ? 1 : 0);
   CK(skv::launch_score(c, q, st));
   CK(skv::launch_select(c, k_new, v_new, loc_row, st));
-  // the value fetch overlaps the key rebuild: CTAs of the rebuild's own
-  // launch, or a kernel on the side stream
-  const bool fused = skv::rebuild_fetches(c);
+  // the value fetch overlaps the key rebuild: warps of the attention's
+  // launch, CTAs of the rebuild's own launch, or a kernel on the side stream
+  const bool fused = skv::attn_fetches(c) || skv::rebuild_fetches(c);
   if (!fused) {
     CK(cudaEventRecord(c.ev_fork, st));
     CK(cudaStreamWaitEvent(c.side, c.ev_fork, 0));
@@ -635,6 +638,8 @@ skv_status shadowkv_rewind(shadowkv_ctx* h, void* stream) {
   CK(cudaStreamWaitEvent(st, c.ev_join, 0));   // the last fetch on the side stream
   CK(skv::launch_fill_i32(c, c.slot_chunk, -1, static_cast<size_t>(c.p.b) * c.p.h_kv * c.p.k, st));
   if (c.at_ctr) CK(cudaMemsetAsync(c.at_ctr, 0, 8 * sizeof(int32_t), st));
+  if (c.item_done)
+    CK(cudaMemsetAsync(c.item_done, 0, static_cast<size_t>(c.p.b) * c.p.h_kv * c.p.k * sizeof(int32_t), st));
   c.n_app = 0;
   return SKV_OK;
 }
@@ -695,6 +700,7 @@ skv_status shadowkv_get_layout(const shadowkv_ctx* h, shadowkv_layout* out) {
   out->tc_rebuild = c.tc_rebuild && !c.force_simt ? 1 : 0;
   out->tc_attention = c.kv_rec && !c.force_simt && !c.split_set ? 1 : 0;
   out->fetch_in_rebuild = skv::rebuild_fetches(c) ? 1 : 0;
+  out->fetch_in_attention = skv::attn_fetches(c) ? 1 : 0;
   return SKV_OK;
 }
 

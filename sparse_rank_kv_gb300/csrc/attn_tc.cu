@@ -6,10 +6,11 @@
 // Work items are 128-token pieces of one (batch, KV head): its outliers, its
 // local window, its cache hits (16 chunks of 8 tokens per item), then its
 // missed chunks.  Items are taken from two step-wide counters: phase 0
-// (outliers, local window, hits) needs nothing the step's value fetch or key
-// rebuild produce, so it runs while they do (this kernel is launched with
-// programmatic dependent launch right behind them); phase 1 (the misses)
-// starts after griddepcontrol.wait.  Keys and values are stored by 8-token
+// (outliers, local window, hits) needs nothing the step's key rebuild or
+// value fetch produce, so it runs while they do (this kernel is launched with
+// programmatic dependent launch right behind the rebuild); phase 1 (the
+// misses) starts after griddepcontrol.wait, each item once its own values
+// have arrived.  Keys and values are stored by 8-token
 // group in 4 KB records laid out as the tensor core's no-swizzle K-major
 // tiles: K ([d/8][token%8][d%8], 2 KB), then V^T ([d/8][d%8][token%8], 2 KB).
 //   warp 0     : producer -- per item the keys and values by bulk copies
@@ -26,6 +27,12 @@
 //                bf16 P^T into shared memory, head sums), for O the dimension:
 //                the item's partial (max, sum, sum p v) per query head goes to
 //                the item's slot, and a ticket per head counts finished items.
+//   warps 6..9 : the step's value fetch (Algorithm 2 step 3, V from the host):
+//                8-token groups of the missed chunks, taken from a fourth
+//                counter in phase-1 item order, read from pinned host memory
+//                through its device mapping and written as the V^T half of the
+//                chunk's cache-slot record; a count per phase-1 item tells
+//                the producer when all of the item's groups are in place.
 // When both counters are exhausted a CTA takes heads from a third counter and
 // merges each head's item partials once its ticket shows all of them done.
 #include "common.cuh"
@@ -37,7 +44,8 @@ namespace skv {
 constexpr int kAtT = 128;                    // tokens per item
 constexpr int kAtD = 128;                    // head dimension handled here
 constexpr int kAtStages = 3;
-constexpr int kAtThreads = 192;
+constexpr int kAtFetchWarps = 4;
+constexpr int kAtThreads = 192 + 32 * kAtFetchWarps;
 constexpr int kAtSoft = 128;                 // softmax threads
 constexpr int kAtRec = kAtT / 8 * 4096;      // 16 group records (K tile | V^T tile)
 constexpr int kAtQBytes = 16 * kAtD * 2;     // q: 4 x [16 rows][64 B]
@@ -59,12 +67,14 @@ struct AtItem {
 template <int G>
 __global__ void __launch_bounds__(kAtThreads, 1)
 k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_out,
-          const bf16* __restrict__ KV_slot, const int32_t* __restrict__ att_slot,
+          bf16* KV_slot, const int32_t* __restrict__ att_slot,
           const int32_t* __restrict__ hits_in, const bf16* __restrict__ KV_loc,
           bf16* __restrict__ out, float* __restrict__ part, int32_t* __restrict__ ticket,
           int32_t* __restrict__ ctr, int32_t* __restrict__ ctr_next, int n_out, int n_loc,
           int loc_cap, int c, int k, int npairs, int max_splits, float scale_log2,
-          int* __restrict__ status) {
+          const bf16* __restrict__ vcpu, const int32_t* __restrict__ miss_chunk,
+          const int32_t* __restrict__ miss_slot, const int32_t* __restrict__ miss_base,
+          int32_t* __restrict__ item_done, int s, int n_chunks, int* __restrict__ status) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -113,7 +123,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
     *s_end = -1;
     *s_ndone = 0;
     // the next step's counters start at zero
-    if (blockIdx.x == 0) ctr_next[0] = ctr_next[1] = ctr_next[2] = 0;
+    if (blockIdx.x == 0) ctr_next[0] = ctr_next[1] = ctr_next[2] = ctr_next[3] = 0;
   }
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, 64);
@@ -214,8 +224,9 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
     int lastA[kAtStages];
 #pragma unroll
     for (int i = 0; i < kAtStages; ++i) lastA[i] = -1;
-    // item numbers are requested two items ahead, so the atomics' round
-    // trips overlap the copies
+    // phase-0 item numbers are requested two items ahead, so the atomics'
+    // round trips overlap the copies; phase 1 (a few items per CTA) runs one
+    // number ahead, which spreads its items over more CTAs
     int phase = 0, x = 0, x1 = 0;
     if (lane == 0) {
       x = atomicAdd(&ctr[0], 1);
@@ -228,10 +239,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
         // (the number requested ahead is past T0 as well)
         phase = 1;
         tc::grid_dep_wait();
-        if (lane == 0) {
-          x = atomicAdd(&ctr[1], 1);
-          x1 = atomicAdd(&ctr[1], 1);
-        }
+        if (lane == 0) x = atomicAdd(&ctr[1], 1);
         x = __shfl_sync(0xffffffffu, x, 0);
       }
       const int st = it % kAtStages, use = it / kAtStages;
@@ -240,7 +248,8 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
       // cache slots of the item's chunks (lane = chunk), loaded before the wait
       const int nch = t.seg >= 2 ? t.cnt / c : 0;
       const int slot = lane < nch ? att_slot[static_cast<size_t>(t.pair) * k + t.t0 + lane] : 0;
-      // the number after the next one, requested before this item's copies
+      // the number after the next one (phase 1: the next one), requested
+      // before this item's copies
       int xn = 0;
       if (lane == 0 && !done) xn = atomicAdd(&ctr[phase], 1);
       bool ok = true;
@@ -272,6 +281,31 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
         tc::fence_proxy_async_smem();
         __syncwarp();
       }
+      if (t.seg == 3 && vcpu != nullptr) {
+        // the item's values come from this launch's fetch warps: wait for
+        // all of its groups, then zero the count for the next step
+        bool got = true;
+        if (lane == 0) {
+          const uint64_t w0 = tc::globaltimer_ns();
+          for (;;) {
+            int v;
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(item_done + x) : "memory");
+            if (v >= groups) break;
+            if (*s_abort || tc::globaltimer_ns() - w0 > kWaitLimit) {
+              got = false;
+              break;
+            }
+          }
+          if (got) {
+            item_done[x] = 0;
+            tc::fence_proxy_async_global();
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, got, 0)) {
+          if (lane == 0) abort_now();
+          break;
+        }
+      }
       if (lane == 0) {
         inf[0] = t.pair;
         inf[1] = t.cnt;
@@ -295,8 +329,12 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
         }
       }
       lastA[st] = use;
-      x = x1;
-      x1 = xn;
+      if (phase == 1) {
+        x = xn;
+      } else {
+        x = x1;
+        x1 = xn;
+      }
     }
     // no copy may still be landing in this CTA's shared memory at exit
     if (lane == 0)
@@ -369,7 +407,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
       if (no > 0) tc::mbar_wait(&ofull[(no - 1) & 1], ((no - 1) >> 1) & 1, kWaitLimit);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 6) {
     // ------------------------------------------------------------ softmax
     const int ct = tid - 64, quarter = warp & 3;
     const int row = quarter * 32 + lane;          // TMEM lane: token row for S, dimension for O
@@ -574,6 +612,69 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
       if (ct == 0) ticket[pair] = 0;
       tc::named_sync(1, kAtSoft);
     }
+  } else if (vcpu != nullptr) {
+    // ------------------------------------------------------------ value fetch
+    // units: 16 groups of 8 tokens per phase-1 item (a full item holds 128
+    // tokens), numbered item-major so that items complete in the order the
+    // producers take them; a half-warp moves one group (2 KB), two per round
+    // with both read before either is written; a warp takes 4 units at a time
+    const int half = lane >> 4, q = lane & 15;
+    const int gpc = c >> 3;   // groups per chunk
+    const int units = T1 * (kAtT / 8);
+    for (;;) {
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&ctr[3], 4);
+      base = __shfl_sync(0xffffffffu, base, 0);
+      if (base >= units) break;
+      uint4 in[2][8];
+      uint4* dst[2] = {nullptr, nullptr};
+      int xs[2] = {-1, -1};
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int U = base + 2 * half + u;
+        if (U >= units) continue;
+        const int x = U / (kAtT / 8), gi = U - x * (kAtT / 8);
+        const int p = head_of(s_p1, x), j = x - s_p1[p];
+        const int nch = min(cpi, k - s_hits[p] - j * cpi);
+        if (gi >= nch * gpc) continue;
+        // counted even when its entry is bad, so that no producer waits for it
+        xs[u] = x;
+        const int l = gi / gpc, gs = gi - l * gpc;
+        const int m = miss_base[p] + j * cpi + l;
+        int chunk = -1, slot = -1;
+        if (m >= 0 && m < npairs * k) {
+          chunk = miss_chunk[m] - p * n_chunks;
+          slot = miss_slot[m] - p * k;
+        }
+        if (chunk < 0 || chunk >= n_chunks || slot < 0 || slot >= k) {
+          if (q == 0) flag_error(status, DEV_BAD_SLOT);
+          continue;
+        }
+        const uint4* src = reinterpret_cast<const uint4*>(
+            vcpu + (static_cast<size_t>(p) * s + static_cast<size_t>(chunk) * c + gs * 8) * kAtD);
+        dst[u] = reinterpret_cast<uint4*>(KV_slot + ((static_cast<size_t>(p) * k + slot) * c + gs * 8) * 2 * kAtD +
+                                          kAtD * 8);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) in[u][t] = src[t * 16 + q];
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        if (dst[u] == nullptr) continue;
+        uint4 outv[8];
+        transpose8x8(in[u], outv);
+#pragma unroll
+        for (int r = 0; r < 8; ++r) dst[u][q * 8 + r] = outv[r];
+      }
+      // the groups' values are visible at device scope (and ordered before
+      // the consuming CTA's bulk copies) before their items' counts move
+      tc::fence_proxy_async_global();
+      __threadfence();
+      __syncwarp();
+      if (q == 0)
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+          if (xs[u] >= 0) atomicAdd(&item_done[xs[u]], 1);
+    }
   }
   tc::fence_before();
   __syncthreads();
@@ -647,13 +748,22 @@ static cudaError_t attn_tc_t(Ctx& c, const CUtensorMap& mq, void* out, int n_loc
     if (e != cudaSuccess) return e;
   }
   c.at_last = c.t;
-  // launched behind the value fetch and key rebuild: phase 0 overlaps them
+  // launched behind the key rebuild: phase 0 overlaps it and this launch's
+  // own value fetch
+  const bool fetch = attn_fetches(c);
   return launch_pdl(kern, dim3(c.nsm), dim3(kAtThreads), static_cast<size_t>(smem), st, mq,
-                    static_cast<const bf16*>(c.KV_out), static_cast<const bf16*>(c.KV_slot),
+                    static_cast<const bf16*>(c.KV_out), static_cast<bf16*>(c.KV_slot),
                     static_cast<const int32_t*>(c.att_slot), static_cast<const int32_t*>(c.hits),
                     static_cast<const bf16*>(c.KV_loc), static_cast<bf16*>(out), c.attn_part, c.attn_count,
                     c.at_ctr + 4 * par, c.at_ctr + 4 * (par ^ 1), c.p.o * c.p.c, n_loc, c.loc_cap, c.p.c,
-                    c.p.k, npairs, c.max_splits, scale_log2, c.status);
+                    c.p.k, npairs, c.max_splits, scale_log2,
+                    static_cast<const bf16*>(fetch ? c.v_cpu_dev : nullptr),
+                    static_cast<const int32_t*>(c.miss_chunk), static_cast<const int32_t*>(c.miss_slot),
+                    static_cast<const int32_t*>(c.miss_base), c.item_done, c.p.s, c.n, c.status);
+}
+
+bool attn_fetches(const Ctx& c) {
+  return c.kv_rec && !c.force_simt && !c.split_set && c.v_cpu_dev != nullptr && c.item_done != nullptr;
 }
 
 cudaError_t launch_attn_tc(Ctx& c, const void* q, void* out, int n_loc, cudaStream_t st) {

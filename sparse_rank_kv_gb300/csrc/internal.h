@@ -101,6 +101,7 @@ struct Ctx {
   int32_t* miss_base = nullptr;   // per (batch, KV head): start of its misses in the step's list
   int32_t* att_slot = nullptr;    // per head: slots of its hits, then of its misses (attention order)
   int32_t* at_ctr = nullptr;      // attention work counters, 4 per step parity
+  int32_t* item_done = nullptr;   // per phase-1 attention item: its value groups fetched this step
   long long at_last = -2;         // step of the last tensor-core attention launch
   // tensor map of the caller's query buffer (16-row boxes), encoded again
   // only when the buffer's address changes
@@ -189,7 +190,8 @@ cudaError_t launch_build_mask(Ctx& c, cudaStream_t st);
 // rebuild.cu
 cudaError_t launch_rebuild(Ctx& c, cudaStream_t st);
 // true when launch_rebuild also moves the step's value misses (records with
-// the tensor-core rebuild): no separate fetch launch then
+// the tensor-core rebuild and the classic attention): no separate fetch
+// launch then
 bool rebuild_fetches(const Ctx& c);
 bool tc_rebuild_supported(const shadowkv_params& p);
 cudaError_t make_rebuild_maps(Ctx& c);   // encodes mapBt
@@ -197,6 +199,9 @@ cudaError_t launch_tile_a(Ctx& c, int to_tiled, cudaStream_t st);   // no-op unl
 cudaError_t launch_pack_kv(Ctx& c, cudaStream_t st);                // records of outliers and local window (kv_rec)
 bool attn_tc_supported(const shadowkv_params& p);
 cudaError_t launch_attn_tc(Ctx& c, const void* q, void* out, int n_loc, cudaStream_t st);
+// true when the tensor-core attention moves the step's value misses itself
+// (warps of its own launch): no separate fetch launch then
+bool attn_fetches(const Ctx& c);
 cudaError_t encode_q_map(const Ctx& c, const void* q, CUtensorMap* map);
 // the query map for buffer q: the context's cached one, encoded when q differs
 cudaError_t q_map_for(Ctx& c, const void* q, CUtensorMap* map);

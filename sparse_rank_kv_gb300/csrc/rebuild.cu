@@ -667,9 +667,10 @@ static cudaError_t rebuild_tc(Ctx& c, cudaStream_t st) {
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), ps.smem);
   if (e != cudaSuccess) return e;
   const int tiles = (c.p.k * c.p.c + kTcRows - 1) / kTcRows * npairs;
-  // records: the value fetch runs in the same launch, on its own CTAs;
-  // otherwise it runs on a side stream and the rebuild leaves it its SMs
-  const int nfetch = REC ? std::min(c.fetch_sms, c.nsm / 2) : 0;
+  // records: the value fetch runs in the attention's launch, or in this one
+  // on its own CTAs; otherwise it runs on a side stream and the rebuild
+  // leaves it its SMs
+  const int nfetch = REC && rebuild_fetches(c) ? std::min(c.fetch_sms, c.nsm / 2) : 0;
   const int sms = REC ? std::min(kRebuildSMsRec, c.nsm - nfetch)
                       : c.nsm > 2 * c.fetch_sms ? c.nsm - c.fetch_sms : c.nsm;
   const int grid = nfetch + std::min(sms, tiles);
@@ -683,7 +684,9 @@ static cudaError_t rebuild_tc(Ctx& c, cudaStream_t st) {
                     static_cast<const int32_t*>(c.miss_count), static_cast<int>(c.t & 1), nfetch, c.status);
 }
 
-bool rebuild_fetches(const Ctx& c) { return c.tc_rebuild && !c.force_simt && c.kv_rec && c.a_tiled; }
+bool rebuild_fetches(const Ctx& c) {
+  return c.tc_rebuild && !c.force_simt && c.kv_rec && c.a_tiled && !attn_fetches(c);
+}
 
 template <typename T, int D>
 static cudaError_t rebuild_simt(Ctx& c, cudaStream_t st) {

@@ -235,6 +235,11 @@ __device__ __forceinline__ void cp_async_wait() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Orders this thread's generic-proxy view of global memory with its
+// async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 
 // ------------------------------------------------------------ grid dependencies
 // Programmatic dependent launch: a kernel launched with programmatic stream
