@@ -76,15 +76,14 @@ struct Sizes {
   size_t A, Bt, L, K_out, V_out, K_loc, V_loc, slot_V, K_sparse, KV_out, KV_loc, KV_slot;
   size_t min_cos, logits, score_part, attn_part, basis, rope_tab;
   size_t out_ids, out_mask, sel, sel_slot, slot_chunk, miss_chunk, miss_slot;
-  size_t miss_count, miss_base, att_slot, at_ctr, item_done, hits, attn_count, counters, status;
+  size_t miss_count, miss_base, att_slot, at_ctr, item_done, sc_ctr, hits, attn_count, counters, status;
   size_t q_stage, kv_stage, out_stage;
   size_t total() const {
     const size_t v[] = {A, Bt, L, K_out, V_out, K_loc, V_loc, slot_V, K_sparse, KV_out, KV_loc, KV_slot,
-                        min_cos, logits,
-                        score_part, attn_part, basis, rope_tab, out_ids, out_mask, sel, sel_slot,
-                        slot_chunk, miss_chunk, miss_slot, miss_count, miss_base, att_slot, at_ctr, item_done, hits, attn_count,
-                        counters,
-                        status, q_stage, kv_stage, out_stage};
+                        min_cos, logits, score_part, attn_part, basis, rope_tab, out_ids, out_mask, sel,
+                        sel_slot, slot_chunk, miss_chunk, miss_slot, miss_count, miss_base, att_slot,
+                        at_ctr, item_done, sc_ctr, hits, attn_count, counters, status, q_stage, kv_stage,
+                        out_stage};
     size_t t = 0;
     for (size_t x : v) t += up(x);
     return t;
@@ -132,6 +131,7 @@ Sizes sizes_of(const shadowkv_params& p) {
   z.att_slot = rec ? b * h * k * 4 : 0;
   z.at_ctr = rec ? 8 * 4 : 0;
   z.item_done = rec ? b * h * k * 4 : 0;   // at most k phase-1 attention items per head
+  z.sc_ctr = 2 * 4;
   z.miss_count = 2 * 4;   // compact miss-list length per step parity
   z.counters = 2 * 8;
   z.status = 4;
@@ -295,6 +295,7 @@ skv_status create(const shadowkv_params* p, cudaStream_t st, shadowkv_ctx** out)
   c.att_slot = c.kv_rec ? static_cast<int32_t*>(take(z.att_slot)) : nullptr;
   c.at_ctr = c.kv_rec ? static_cast<int32_t*>(take(z.at_ctr)) : nullptr;
   c.item_done = c.kv_rec ? static_cast<int32_t*>(take(z.item_done)) : nullptr;
+  c.sc_ctr = static_cast<int32_t*>(take(z.sc_ctr));
   c.hits = static_cast<int32_t*>(take(z.hits));
   c.attn_count = static_cast<int32_t*>(take(z.attn_count));
   c.counters = static_cast<unsigned long long*>(take(z.counters));
@@ -640,6 +641,7 @@ skv_status shadowkv_rewind(shadowkv_ctx* h, void* stream) {
   if (c.at_ctr) CK(cudaMemsetAsync(c.at_ctr, 0, 8 * sizeof(int32_t), st));
   if (c.item_done)
     CK(cudaMemsetAsync(c.item_done, 0, static_cast<size_t>(c.p.b) * c.p.h_kv * c.p.k * sizeof(int32_t), st));
+  CK(cudaMemsetAsync(c.sc_ctr, 0, 2 * sizeof(int32_t), st));
   c.n_app = 0;
   return SKV_OK;
 }

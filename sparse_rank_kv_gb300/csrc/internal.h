@@ -103,6 +103,8 @@ struct Ctx {
   int32_t* at_ctr = nullptr;      // attention work counters, 4 per step parity
   int32_t* item_done = nullptr;   // per phase-1 attention item: its value groups fetched this step
   long long at_last = -2;         // step of the last tensor-core attention launch
+  int32_t* sc_ctr = nullptr;      // landmark-score tail tile counters, one per step parity
+  long long sc_last = -2;         // step of the last tensor-core score launch
   // tensor map of the caller's query buffer (16-row boxes), encoded again
   // only when the buffer's address changes
   const void* q_enc = nullptr;

@@ -5,8 +5,13 @@
 // read of a decode step, so this kernel is built to keep HBM busy:
 //
 //   persistent: one CTA per SM, each owning a contiguous range of 128-row
-//               landmark tiles (a tile never spans two KV heads)
-//   warp 0    : TMA producer -- per tile, d/64 boxes of 128 landmark rows x
+//               landmark tiles (a tile never spans two KV heads) for about
+//               85% of the work; the remaining tiles go one at a time, from a
+//               step-wide counter, to whichever CTAs finish first (SMs do not
+//               all read HBM at the same rate)
+//   warp 0    : TMA producer -- per tile (its number goes to a ring in shared
+//               memory that the MMA warp passes on to the epilogue through a
+//               per-accumulator barrier), d/64 boxes of 128 landmark rows x
 //               64 columns and d/64 boxes of the head's q (16 rows; rows past
 //               G are zero-filled by TMA) into a 5-stage shared-memory ring,
 //               K-major with the 128-byte swizzle; lanes 0..2d/64-1 issue one
@@ -34,6 +39,8 @@ constexpr int kScStages = 5;
 constexpr int kScGroups = 4;     // epilogue warpgroups
 constexpr int kScThreads = 64 + kScGroups * 128;
 constexpr int kScAcc = 8;        // TMEM accumulators of 16 columns
+constexpr int kScRing = 32;      // tile numbers in flight (producer <= 13 ahead of the epilogue, plus 4 end marks)
+constexpr int kScStaticPct = 85; // share of the tiles assigned as contiguous ranges
 
 __host__ __device__ constexpr int sc_stage_bytes(int D) { return (D / 32) * (kScTile + 16) * 64; }
 __host__ __device__ constexpr int sc_smem_bytes(int D) {
@@ -44,7 +51,8 @@ template <int D, int G>
 __global__ void __launch_bounds__(kScThreads, 1)
 k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUtensorMap mapQ,
            const uint32_t* __restrict__ mask, float* __restrict__ P, float2* __restrict__ part, int n,
-           int ntile, int total_tiles, float scale, int* __restrict__ status) {
+           int ntile, int total_tiles, int per_cta, int* __restrict__ tail, int* __restrict__ tail_next,
+           float scale, int* __restrict__ status) {
   constexpr int KA = D / 64;                  // landmark and q boxes of 64 dims (128-byte swizzle)
   constexpr int A_BYTES = KA * kScTile * 128;
   constexpr int STAGE = sc_stage_bytes(D);
@@ -55,12 +63,14 @@ k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUt
   uint64_t* empty = full + kScStages;
   uint64_t* tfull = empty + kScStages;
   uint64_t* tempty = tfull + kScAcc;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + kScAcc);
+  uint64_t* tinfo = tempty + kScAcc;                        // [kScAcc]: the accumulator's tile number is set
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tinfo + kScAcc);
+  int* ring = reinterpret_cast<int*>(smem + 512);          // [kScRing] tile numbers (-1: no more)
   unsigned char* stages = smem + 1024;
 
-  const int t_begin = static_cast<int>(static_cast<long long>(total_tiles) * blockIdx.x / gridDim.x);
-  const int t_end = static_cast<int>(static_cast<long long>(total_tiles) * (blockIdx.x + 1) / gridDim.x);
-  const int ntl = t_end - t_begin;
+  // this CTA's contiguous range, then the shared tail [tail0, total_tiles)
+  const int t_begin = per_cta * static_cast<int>(blockIdx.x);
+  const int tail0 = per_cta * static_cast<int>(gridDim.x);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   tc::grid_dep_launch();
 
@@ -74,8 +84,11 @@ k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUt
     for (int a = 0; a < kScAcc; ++a) {
       tc::mbar_init(&tfull[a], 1);
       tc::mbar_init(&tempty[a], 128);
+      tc::mbar_init(&tinfo[a], 1);
     }
     tc::fence_mbar_init();
+    // the next step's tail counter starts at zero
+    if (blockIdx.x == 0) *tail_next = 0;
   }
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, 16 * kScAcc);
@@ -92,18 +105,41 @@ k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUt
   if (warp == 0) {
     // lane 0 waits for the stage and arms its barrier; lanes 0..2KB-1 then
     // issue one box each (landmark boxes, then q boxes), so the copies of a
-    // stage are not serialised behind one thread's issue
-    for (int i = 0; i < ntl; ++i) {
+    // stage are not serialised behind one thread's issue.  Tail tiles are
+    // requested one ahead, so the atomic's round trip overlaps a stage.
+    int next = -1;
+    if (lane == 0 && per_cta == 0) next = tail0 + atomicAdd(tail, 1);
+    for (int i = 0;; ++i) {
       const int s = i % kScStages;
       const uint32_t ph = (i / kScStages) & 1;
+      int tile = -1;
+      if (lane == 0) {
+        if (i < per_cta) {
+          tile = t_begin + i;
+          if (i + 1 == per_cta) next = tail0 + atomicAdd(tail, 1);
+        } else {
+          tile = next;
+          if (tile < total_tiles) next = tail0 + atomicAdd(tail, 1);
+        }
+        if (tile >= total_tiles) tile = -1;
+      }
+      tile = __shfl_sync(0xffffffffu, tile, 0);
       bool ok = true;
       if (lane == 0) {
         ok = tc::mbar_wait(&empty[s], ph ^ 1, kWaitLimit);
-        if (!ok) flag_error(status, DEV_TIMEOUT);
-        else tc::mbar_expect_tx(&full[s], STAGE);
+        if (!ok) {
+          flag_error(status, DEV_TIMEOUT);
+        } else if (tile < 0) {
+          // no more tiles: an end mark for the MMA warp and for each of the
+          // four epilogue warpgroups' next tile
+          for (int u = 0; u < kScGroups; ++u) ring[(i + u) % kScRing] = -1;
+          tc::mbar_arrive(&full[s]);
+        } else {
+          ring[i % kScRing] = tile;
+          tc::mbar_expect_tx(&full[s], STAGE);
+        }
       }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      const int tile = t_begin + i;
+      if (!__shfl_sync(0xffffffffu, ok, 0) || tile < 0) break;
       const int pair = tile / ntile, ti = tile - pair * ntile;
       unsigned char* st = stages + s * STAGE;
       if (lane < KA)
@@ -114,13 +150,26 @@ k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUt
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(kScTile, 16);
-      for (int i = 0; i < ntl; ++i) {
+      for (int i = 0;; ++i) {
         const int s = i % kScStages;
         const uint32_t ph = (i / kScStages) & 1;
         const int a = i % kScAcc;
         const uint32_t tph = (i / kScAcc) & 1;
         if (!tc::mbar_wait(&full[s], ph, kWaitLimit) || !tc::mbar_wait(&tempty[a], tph ^ 1, kWaitLimit)) {
           flag_error(status, DEV_TIMEOUT);
+          break;
+        }
+        if (ring[i % kScRing] < 0) {
+          // the end: pass the mark to the epilogue warpgroups' next tiles,
+          // each once its accumulator is free (keeps the barriers' phases)
+          for (int u = 0; u < kScGroups; ++u) {
+            const int au = (i + u) % kScAcc;
+            if (u > 0 && !tc::mbar_wait(&tempty[au], (((i + u) / kScAcc) & 1) ^ 1, kWaitLimit)) {
+              flag_error(status, DEV_TIMEOUT);
+              break;
+            }
+            tc::mbar_arrive(&tinfo[au]);
+          }
           break;
         }
         tc::fence_after();
@@ -134,6 +183,7 @@ k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUt
                        tc::desc_k_sw128(b0 + (kk >> 2) * (16 * 128) + (kk & 3) * 32, 1024), idesc, kk != 0);
         tc::mma_commit(&empty[s]);
         tc::mma_commit(&tfull[a]);
+        tc::mbar_arrive(&tinfo[a]);
       }
     }
   } else {
@@ -141,18 +191,20 @@ k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUt
     const int eg = (warp - 2) >> 2;        // epilogue warpgroup: tiles eg, eg + kScGroups, ...
     const int row = q4 * 32 + lane;
     const int nw = (n + 31) >> 5;
-    auto mask_word = [&](int i) -> uint32_t {
-      if (i >= ntl) return 0u;
-      const int tile = t_begin + i;
-      const int pair = tile / ntile, ti = tile - pair * ntile;
-      const int w = ti * (kScTile / 32) + q4;
-      return w < nw ? __ldg(&mask[static_cast<size_t>(pair) * nw + w]) : 0u;
-    };
-    uint32_t mword = mask_word(eg);
-    for (int i = eg; i < ntl; i += kScGroups) {
-      const uint32_t mnext = mask_word(i + kScGroups);
+    for (int i = eg;; i += kScGroups) {
       const int a = i % kScAcc;
       const uint32_t tph = (i / kScAcc) & 1;
+      // the tile number (published by the MMA warp after the producer's),
+      // then the outlier-mask word, loaded while the MMA runs
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&tinfo[a], tph, kWaitLimit))) {
+        if (lane == 0) flag_error(status, DEV_TIMEOUT);
+        break;
+      }
+      const int tile = ring[i % kScRing];
+      if (tile < 0) break;
+      const int pair = tile / ntile, ti = tile - pair * ntile;
+      const int w = ti * (kScTile / 32) + q4;
+      const uint32_t mword = w < nw ? __ldg(&mask[static_cast<size_t>(pair) * nw + w]) : 0u;
       const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(&tfull[a], tph, kWaitLimit));
       if (!ok) {
         if (lane == 0) flag_error(status, DEV_TIMEOUT);
@@ -165,8 +217,6 @@ k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUt
       else tc::tmem_ld8(taddr, acc);
       tc::fence_before();
       tc::mbar_arrive(&tempty[a]);
-      const int tile = t_begin + i;
-      const int pair = tile / ntile, ti = tile - pair * ntile;
       const int j = ti * kScTile + row;
       const bool valid = j < n && !((mword >> lane) & 1u);
 #pragma unroll
@@ -177,7 +227,6 @@ k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUt
         const float e = warp_sum(valid ? __expf(x - m) : 0.f);
         if (lane == 0) part[((static_cast<size_t>(pair) * G + g) * ntile + ti) * 4 + q4] = make_float2(m, e);
       }
-      mword = mnext;
     }
   }
   tc::fence_before();
@@ -258,10 +307,20 @@ static cudaError_t score_tc_t(Ctx& c, const CUtensorMap& mq, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const int total = c.p.b * c.p.h_kv * c.ntile;
   const int grid = total < c.nsm ? total : c.nsm;
+  const int per_cta = static_cast<int>(static_cast<long long>(total) * kScStaticPct / 100 / grid);
+  const int par = static_cast<int>(c.t & 1);
+  // each launch clears the other parity's tail counter for the next step;
+  // after a step on the CUDA-core kernel this parity's is cleared here
+  if (c.sc_last != c.t - 1) {
+    e = cudaMemsetAsync(c.sc_ctr + par, 0, sizeof(int32_t), st);
+    if (e != cudaSuccess) return e;
+  }
+  c.sc_last = c.t;
   // the prologue overlaps the tail of the stream's previous kernel
   return launch_pdl(kern, dim3(grid), dim3(kScThreads), static_cast<size_t>(smem), st, c.mapL, mq,
                     static_cast<const uint32_t*>(c.out_mask), c.logits, c.score_part, c.n, c.ntile, total,
-                    1.0f / sqrtf(static_cast<float>(D)), c.status);
+                    per_cta, c.sc_ctr + par, c.sc_ctr + (par ^ 1), 1.0f / sqrtf(static_cast<float>(D)),
+                    c.status);
 }
 
 template <int D>
