@@ -74,13 +74,13 @@ size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 // Byte sizes of every device buffer of a context, in allocation order.
 struct Sizes {
   size_t A, Bt, L, K_out, V_out, K_loc, V_loc, slot_V, K_sparse, KV_out, KV_loc, KV_slot;
-  size_t min_cos, logits, score_part, attn_part, basis, rope_tab;
+  size_t min_cos, logits, score_part, score_m8, attn_part, basis, rope_tab;
   size_t out_ids, out_mask, sel, sel_slot, slot_chunk, miss_chunk, miss_slot;
   size_t miss_count, miss_base, att_slot, at_ctr, item_done, sc_ctr, hits, attn_count, counters, status;
   size_t q_stage, kv_stage, out_stage;
   size_t total() const {
     const size_t v[] = {A, Bt, L, K_out, V_out, K_loc, V_loc, slot_V, K_sparse, KV_out, KV_loc, KV_slot,
-                        min_cos, logits, score_part, attn_part, basis, rope_tab, out_ids, out_mask, sel,
+                        min_cos, logits, score_part, score_m8, attn_part, basis, rope_tab, out_ids, out_mask, sel,
                         sel_slot, slot_chunk, miss_chunk, miss_slot, miss_count, miss_base, att_slot,
                         at_ctr, item_done, sc_ctr, hits, attn_count, counters, status, q_stage, kv_stage,
                         out_stage};
@@ -121,6 +121,7 @@ Sizes sizes_of(const shadowkv_params& p) {
   z.min_cos = b * h * n * 4;
   z.logits = b * hq * n * 4;
   z.score_part = b * hq * ntile * 4 * 8;   // 4 softmax partials per 128-landmark tile
+  z.score_m8 = b * hq * ((n + 7) / 8) * 4;
   z.attn_part = b * hq * static_cast<size_t>(max_splits_of(p)) * (d + 2) * 4;
   z.basis = b * r * h * d * 4;
   z.rope_tab = d / 2 * 8;
@@ -280,6 +281,7 @@ skv_status create(const shadowkv_params* p, cudaStream_t st, shadowkv_ctx** out)
   c.min_cos = static_cast<float*>(take(z.min_cos));
   c.logits = static_cast<float*>(take(z.logits));
   c.score_part = static_cast<float2*>(take(z.score_part));
+  c.score_m8 = static_cast<float*>(take(z.score_m8));
   c.attn_part = static_cast<float*>(take(z.attn_part));
   c.basis = static_cast<float*>(take(z.basis));
   c.rope_tab = static_cast<float2*>(take(z.rope_tab));

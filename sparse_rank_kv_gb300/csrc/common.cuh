@@ -556,6 +556,30 @@ __device__ __forceinline__ void block_kth_256(const uint32_t* v, int cnt, int kt
 // more than 4 blockDim.x survivors) the radix select over all keys decides
 // instead.  All threads of the block must call it.
 constexpr int kTopkSample = 1024;
+
+// The indices set in bits[0..nw) in ascending order into out[], and wpref[w]
+// = the number of them below 32 w (all in shared memory; tmp holds >= 33
+// ints).  All threads of the block must call it.
+__device__ __forceinline__ void bitmap_list(const uint32_t* bits, int nw, int* out, int* wpref, int* tmp) {
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int per = (nw + nthr - 1) / nthr;
+  const int w0 = tid * per, w1 = min(nw, w0 + per);
+  int cnt = 0;
+  for (int w = w0; w < w1; ++w) cnt += __popc(bits[w]);
+  int tot;
+  int ex = block_exclusive_scan(cnt, tmp, &tot);
+  for (int w = w0; w < w1; ++w) {
+    wpref[w] = ex;
+    uint32_t b = bits[w];
+    while (b) {
+      const int bit = __ffs(b) - 1;
+      out[ex++] = w * 32 + bit;
+      b &= b - 1;
+    }
+  }
+  __syncthreads();
+}
+
 __device__ __forceinline__ void block_topk(const uint32_t* keys, int n, int k, int* out, int* scratch,
                                            uint32_t* bits, int* wpref) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthr = blockDim.x;
@@ -696,25 +720,7 @@ __device__ __forceinline__ void block_topk(const uint32_t* keys, int n, int k, i
     for (int i = tid; i < k; i += nthr) atomicOr(&bits[out[i] >> 5], 1u << (out[i] & 31));
   }
   __syncthreads();
-  // prefix popcounts per word, then the ascending list from the bitmap
-  {
-    const int per = (nw + nthr - 1) / nthr;
-    const int w0 = tid * per, w1 = min(nw, w0 + per);
-    int cnt = 0;
-    for (int w = w0; w < w1; ++w) cnt += __popc(bits[w]);
-    int tot;
-    int ex = block_exclusive_scan(cnt, tmp, &tot);
-    for (int w = w0; w < w1; ++w) {
-      wpref[w] = ex;
-      uint32_t b = bits[w];
-      while (b) {
-        const int bit = __ffs(b) - 1;
-        out[ex++] = w * 32 + bit;
-        b &= b - 1;
-      }
-    }
-  }
-  __syncthreads();
+  bitmap_list(bits, nw, out, wpref, tmp);
 }
 
 // The step's value misses, for bf16 records with d = 128: thread h of nh

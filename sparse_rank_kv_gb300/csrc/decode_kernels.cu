@@ -74,7 +74,7 @@ k_score(const T* __restrict__ L, const T* __restrict__ q, const uint32_t* __rest
 // bookkeeping arrays.
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kSelectThreads)
-k_select(const float* __restrict__ P, const float2* __restrict__ part,
+k_select(const float* __restrict__ P, const float2* __restrict__ part, const float* __restrict__ m8,
          const uint32_t* __restrict__ mask, int n, int ntile, int k, int group_reduce,
          int cache_on, int32_t* __restrict__ sel, int32_t* __restrict__ sel_slot,
          int32_t* __restrict__ slot_chunk, int32_t* __restrict__ miss_chunk,
@@ -135,13 +135,154 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part,
     if (lane == 0) lse[g] = m + __logf(z);
   }
   __syncthreads();
-  // selection keys: S2 per chunk, 0 for outliers
   const uint32_t* mk = mask + static_cast<size_t>(pair) * nw;
+  // With the max reading of S2 and the score kernel's maxima of each 8
+  // consecutive chunks, the top k is taken among few chunks: the bound of a
+  // group, max over heads of (its max logit - lse), is the largest S2 of the
+  // group; the k-th largest bound B is at most the k-th largest S2, so every
+  // chunk of the top k lies in a group with bound >= B and has S2 >= B.  Only
+  // those groups' chunks get keys; the top k of the ones with key >= B
+  // (survivors), ties toward the lower index, is the answer.  Too many
+  // candidates (massive ties) take the general path below.
+  const int n8 = (n + 7) >> 3;
+  bool topk_done = false;
+  if (m8 != nullptr && group_reduce == 0 && 2 * n8 <= n && n8 <= 4 * nthr) {
+    const int cap = 4 * nthr;
+    uint32_t* bkey = keys;                                   // [n8] group bounds (0: no valid chunk)
+    int* cand = reinterpret_cast<int*>(keys + n8);           // [n8] candidate groups
+    uint32_t* vals = reinterpret_cast<uint32_t*>(scratch);  // survivors' keys
+    int* vidx = scratch + cap;                               // their chunks
+    int* ks = vidx + cap;                                    // block_kth scratch
+    int* stmp = ks + (nthr / 32) * 256 + 256 + 8;            // scans, then counters at +36..+39
+    int* cnt_slot = stmp + 36;
+    int* eq_slot = stmp + 37;
+    int* nnz_slot = stmp + 38;
+    int* ncand_slot = stmp + 39;
+    if (tid == 0) *cnt_slot = *eq_slot = *nnz_slot = *ncand_slot = 0;
+    __syncthreads();
+    int nz = 0;
+    for (int w = tid; w < n8; w += nthr) {
+      float bnd = -INFINITY;
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+        bnd = fmaxf(bnd, __ldcg(m8 + (static_cast<size_t>(pair) * G + g) * n8 + w) - lse[g]);
+      const uint32_t kb = bnd == -INFINITY ? 0u : order_key(bnd);
+      bkey[w] = kb;
+      nz += kb != 0u;
+    }
+    nz = __reduce_add_sync(0xffffffffu, nz);
+    if (lane == 0 && nz) atomicAdd(nnz_slot, nz);
+    __syncthreads();
+    uint32_t B = 1u;    // fewer than k groups with a valid chunk: all of them are candidates
+    if (*nnz_slot >= k) {
+      int unused;
+      block_kth(bkey, n8, k, ks, &B, &unused);
+    }
+    // candidate groups, compacted by warps of 32 groups
+    for (int w0 = warp * 32; w0 < n8; w0 += nthr) {
+      const int w = w0 + lane;
+      const bool isc = w < n8 && bkey[w] != 0u && bkey[w] >= B;
+      const unsigned m = __ballot_sync(0xffffffffu, isc);
+      int base = 0;
+      if (lane == 0 && m) base = atomicAdd(ncand_slot, __popc(m));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      if (isc) cand[base + __popc(m & ((1u << lane) - 1u))] = w;
+    }
+    __syncthreads();
+    const int ne = *ncand_slot * 8;
+    if (ne <= cap) {
+      // the candidates' chunks: all loads of a thread (<= 4 chunks) issued
+      // before any key is formed; survivors appended by warp ballots
+      float pv[4][G];
+      int jj[4];
+      uint32_t mw[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = u * nthr + tid;
+        jj[u] = -1;
+        mw[u] = 0u;
+        if (e < ne) {
+          const int j = cand[e >> 3] * 8 + (e & 7);
+          if (j < n) {
+            jj[u] = j;
+            mw[u] = mk[j >> 5];
+#pragma unroll
+            for (int g = 0; g < G; ++g) pv[u][g] = __ldcg(P + (static_cast<size_t>(pair) * G + g) * n + j);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (u * nthr >= ne) break;
+        uint32_t key = 0u;
+        if (jj[u] >= 0 && !((mw[u] >> (jj[u] & 31)) & 1u)) {
+          float sm = -INFINITY;
+#pragma unroll
+          for (int g = 0; g < G; ++g) sm = fmaxf(sm, pv[u][g] - lse[g]);
+          key = order_key(sm);
+        }
+        const bool keep = key != 0u && key >= B;
+        const unsigned m = __ballot_sync(0xffffffffu, keep);
+        int base = 0;
+        if (lane == 0 && m) base = atomicAdd(cnt_slot, __popc(m));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        if (keep) {
+          const int pos = base + __popc(m & ((1u << lane) - 1u));
+          vals[pos] = key;
+          vidx[pos] = jj[u];
+        }
+      }
+      __syncthreads();
+      const int nsurv = *cnt_slot;
+      if (nsurv >= k) {
+        // Tk = the k-th largest survivor; `need` of the survivors equal to
+        // Tk are taken (every chunk equal to Tk is a survivor)
+        uint32_t Tk;
+        int need;
+        if (nsurv <= 1024) {
+          block_kth_256(vals, nsurv, k, ks);
+          __syncthreads();
+          Tk = static_cast<uint32_t>(ks[kKth8T]);
+          need = ks[kKth8Need];
+        } else {
+          block_kth(vals, nsurv, k, ks, &Tk, &need);
+        }
+        for (int w = tid; w < nw; w += nthr) words[w] = 0u;
+        int eq = 0;
+        for (int i = tid; i < nsurv; i += nthr) eq += vals[i] == Tk;
+        eq = __reduce_add_sync(0xffffffffu, eq);
+        if (lane == 0 && eq) atomicAdd(eq_slot, eq);
+        __syncthreads();
+        if (*eq_slot == need) {
+          for (int i = tid; i < nsurv; i += nthr)
+            if (vals[i] >= Tk) atomicOr(&words[vidx[i] >> 5], 1u << (vidx[i] & 31));
+        } else {
+          // the survivors above Tk, then the `need` lowest chunks equal to Tk:
+          // the need-th largest of n - chunk among those
+          for (int i = tid; i < nsurv; i += nthr)
+            if (vals[i] > Tk) atomicOr(&words[vidx[i] >> 5], 1u << (vidx[i] & 31));
+          __syncthreads();
+          for (int i = tid; i < nsurv; i += nthr) vals[i] = vals[i] == Tk ? static_cast<uint32_t>(n - vidx[i]) : 0u;
+          __syncthreads();
+          uint32_t R;
+          int unused;
+          block_kth(vals, nsurv, need, ks, &R, &unused);
+          for (int i = tid; i < nsurv; i += nthr)
+            if (vals[i] != 0u && vals[i] >= R) atomicOr(&words[vidx[i] >> 5], 1u << (vidx[i] & 31));
+        }
+        __syncthreads();
+        bitmap_list(words, nw, s_sel, wpref, stmp);
+        topk_done = true;
+      }
+    }
+  }
+  // selection keys: S2 per chunk, 0 for outliers
   auto key_of = [&](float sc_max, float sc_sum, bool excluded) -> uint32_t {
     if (excluded) return 0u;
     return group_reduce == 0 ? order_key(sc_max) : __float_as_uint(sc_sum) + 1u;
   };
-  if ((n & 3) == 0) {
+  if (topk_done) {
+  } else if ((n & 3) == 0) {
     // 16-byte loads of 4 consecutive chunks per head; a batch of IT x G loads
     // is issued before any key of the batch is computed
     constexpr int IT = G >= 8 ? 1 : 8 / G;
@@ -196,9 +337,11 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part,
     }
     keys[j] = key;
   }
-  __syncthreads();
   // the selection (ascending), its bitmap and per-word prefix popcounts
-  block_topk(keys, n, k, s_sel, scratch, words, wpref);
+  if (!topk_done) {
+    __syncthreads();
+    block_topk(keys, n, k, s_sel, scratch, words, wpref);
+  }
   for (int i = tid; i < k; i += nthr) s_hit[i] = 0;
   __syncthreads();
   // slots whose chunk is selected again keep it (hits)
@@ -429,7 +572,8 @@ static cudaError_t select_t(Ctx& c, const void* k_new, const void* v_new, int lo
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(c.p.b * c.p.h_kv), dim3(kSelectThreads), smem, st,
-      c.logits, c.score_part, c.out_mask, c.n, c.ntile, c.p.k, c.p.group_reduce,
+      c.logits, c.score_part, static_cast<const float*>(c.m8_step == c.t ? c.score_m8 : nullptr), c.out_mask,
+      c.n, c.ntile, c.p.k, c.p.group_reduce,
       c.cache_on ? 1 : 0, c.sel, c.sel_slot, c.slot_chunk, c.miss_chunk, c.miss_slot,
       c.miss_count, c.miss_base, c.att_slot, static_cast<int>(c.t & 1), c.hits, c.counters, static_cast<const T*>(k_new),
       static_cast<const T*>(v_new),

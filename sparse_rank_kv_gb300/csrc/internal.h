@@ -105,6 +105,8 @@ struct Ctx {
   long long at_last = -2;         // step of the last tensor-core attention launch
   int32_t* sc_ctr = nullptr;      // landmark-score tail tile counters, one per step parity
   long long sc_last = -2;         // step of the last tensor-core score launch
+  float* score_m8 = nullptr;      // per (batch, query head, 8 chunks): max logit (tensor-core score)
+  long long m8_step = -2;         // step whose score launch wrote score_m8
   // tensor map of the caller's query buffer (16-row boxes), encoded again
   // only when the buffer's address changes
   const void* q_enc = nullptr;

@@ -24,8 +24,9 @@
 //               per thread (TMEM lane), scale, store the G logits, and per
 //               32-row warp the max (one integer warp reduction of
 //               order-preserving keys) and sum of exp over the non-outlier
-//               rows (softmax partials); the outlier-mask word of the group's
-//               next tile is loaded before waiting on the current one
+//               rows (softmax partials), and per 8 rows the max logit (the
+//               selection bounds each 8-chunk group's S2 by it); the tile's
+//               outlier-mask word is loaded while its MMAs run
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -52,7 +53,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
 k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUtensorMap mapQ,
            const uint32_t* __restrict__ mask, float* __restrict__ P, float2* __restrict__ part, int n,
            int ntile, int total_tiles, int per_cta, int* __restrict__ tail, int* __restrict__ tail_next,
-           float scale, int* __restrict__ status) {
+           float* __restrict__ m8, int n8, float scale, int* __restrict__ status) {
   constexpr int KA = D / 64;                  // landmark and q boxes of 64 dims (128-byte swizzle)
   constexpr int A_BYTES = KA * kScTile * 128;
   constexpr int STAGE = sc_stage_bytes(D);
@@ -226,6 +227,12 @@ k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUt
         const float m = from_order_key(__reduce_max_sync(0xffffffffu, order_key(valid ? x : -INFINITY)));
         const float e = warp_sum(valid ? __expf(x - m) : 0.f);
         if (lane == 0) part[((static_cast<size_t>(pair) * G + g) * ntile + ti) * 4 + q4] = make_float2(m, e);
+        // the max over each 8 consecutive rows (-inf: none valid)
+        float y = valid ? x : -INFINITY;
+        y = fmaxf(y, __shfl_xor_sync(0xffffffffu, y, 1));
+        y = fmaxf(y, __shfl_xor_sync(0xffffffffu, y, 2));
+        y = fmaxf(y, __shfl_xor_sync(0xffffffffu, y, 4));
+        if ((lane & 7) == 0 && j < n) m8[(static_cast<size_t>(pair) * G + g) * n8 + (j >> 3)] = y;
       }
     }
   }
@@ -316,11 +323,12 @@ static cudaError_t score_tc_t(Ctx& c, const CUtensorMap& mq, cudaStream_t st) {
     if (e != cudaSuccess) return e;
   }
   c.sc_last = c.t;
+  c.m8_step = c.t;
   // the prologue overlaps the tail of the stream's previous kernel
   return launch_pdl(kern, dim3(grid), dim3(kScThreads), static_cast<size_t>(smem), st, c.mapL, mq,
                     static_cast<const uint32_t*>(c.out_mask), c.logits, c.score_part, c.n, c.ntile, total,
-                    per_cta, c.sc_ctr + par, c.sc_ctr + (par ^ 1), 1.0f / sqrtf(static_cast<float>(D)),
-                    c.status);
+                    per_cta, c.sc_ctr + par, c.sc_ctr + (par ^ 1), c.score_m8, (c.n + 7) / 8,
+                    1.0f / sqrtf(static_cast<float>(D)), c.status);
 }
 
 template <int D>
