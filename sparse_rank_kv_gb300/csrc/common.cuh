@@ -436,13 +436,14 @@ __device__ __forceinline__ void block_kth(const uint32_t* v, int cnt, int kth, i
   *need_out = need;
 }
 
-// block_kth for at most 1024 values, computed by the block's first 256
-// threads alone (eight warps meeting at named barrier 1, four values per
+// block_kth for at most 256 V values, computed by the block's first 256
+// threads alone (eight warps meeting at named barrier 1, V values per
 // thread): far fewer threads wait at each of the passes' barriers.  The
 // k-th largest lands in scratch[kKth8T] and the count of its equals within
 // the top kth in scratch[kKth8Need]; the caller synchronises the block before
 // reading them.  scratch holds kKth8Ints ints.
 constexpr int kKth8T = 8 * 256 + 256 + 4, kKth8Need = kKth8T + 1, kKth8Ints = 8 * 256 + 256 + 8;
+template <int V = 4>
 __device__ __forceinline__ void block_kth_256(const uint32_t* v, int cnt, int kth, int* scratch) {
   const int tid = threadIdx.x;
   if (tid >= 256) return;
@@ -451,10 +452,10 @@ __device__ __forceinline__ void block_kth_256(const uint32_t* v, int cnt, int kt
   int* hist = scratch + 8 * 256;    // [256]
   int* bc = hist + 256;             // broadcast slots
   auto bar = []() { asm volatile("bar.sync 1, 256;" ::: "memory"); };
-  uint32_t x[4];
+  uint32_t x[V];
   uint32_t lo = 0xffffffffu, hi = 0u;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < V; ++q) {
     const int i = tid + q * 256;
     x[q] = i < cnt ? v[i] : 0u;
     if (x[q]) { lo = min(lo, x[q]); hi = max(hi, x[q]); }
@@ -491,7 +492,7 @@ __device__ __forceinline__ void block_kth_256(const uint32_t* v, int cnt, int kt
     for (int i = 0; i < 8; ++i) wh[i * 32 + lane] = 0;
     __syncwarp();
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < V; ++q) {
       const uint32_t r = x[q] - vmin;
       if (x[q] && (r & pmask) == prefix) atomicAdd(&wh[(r >> shift) & dmask], 1);
     }

@@ -118,7 +118,25 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
       }
     }
   }
+  // this head's cache slots (written by the previous step's selection)
+  int32_t* sc_row = slot_chunk + static_cast<size_t>(pair) * k;
+  const int my_slot_chunk = cache_on && tid < k ? sc_row[tid] : -1;
   tc::grid_dep_wait();   // the logits and partials of the score kernel
+  const int n8 = (n + 7) >> 3;
+  const bool bounded = m8 != nullptr && group_reduce == 0 && 2 * n8 <= n && n8 <= 4 * nthr;
+  // with at most 2 groups per thread, their maxima are loaded before the
+  // log-sum-exp, so that the two round trips overlap
+  const bool pre = bounded && n8 <= 2 * nthr;
+  float gm[2][G];
+  if (pre) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int w = tid + u * nthr;
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+        gm[u][g] = w < n8 ? __ldcg(m8 + (static_cast<size_t>(pair) * G + g) * n8 + w) : -INFINITY;
+    }
+  }
   // log-sum-exp of each query head over the candidate chunks (4 partials
   // of 32 landmarks per 128-landmark score tile): a warp per head
   for (int g = warp; g < G; g += nthr / 32) {
@@ -144,9 +162,8 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
   // those groups' chunks get keys; the top k of the ones with key >= B
   // (survivors), ties toward the lower index, is the answer.  Too many
   // candidates (massive ties) take the general path below.
-  const int n8 = (n + 7) >> 3;
   bool topk_done = false;
-  if (m8 != nullptr && group_reduce == 0 && 2 * n8 <= n && n8 <= 4 * nthr) {
+  if (bounded) {
     const int cap = 4 * nthr;
     uint32_t* bkey = keys;                                   // [n8] group bounds (0: no valid chunk)
     int* cand = reinterpret_cast<int*>(keys + n8);           // [n8] candidate groups
@@ -161,22 +178,43 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
     if (tid == 0) *cnt_slot = *eq_slot = *nnz_slot = *ncand_slot = 0;
     __syncthreads();
     int nz = 0;
-    for (int w = tid; w < n8; w += nthr) {
-      float bnd = -INFINITY;
-#pragma unroll
-      for (int g = 0; g < G; ++g)
-        bnd = fmaxf(bnd, __ldcg(m8 + (static_cast<size_t>(pair) * G + g) * n8 + w) - lse[g]);
+    auto put_bound = [&](int w, float bnd) {
       const uint32_t kb = bnd == -INFINITY ? 0u : order_key(bnd);
       bkey[w] = kb;
       nz += kb != 0u;
+    };
+    if (pre) {
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int w = tid + u * nthr;
+        if (w >= n8) continue;
+        float bnd = -INFINITY;
+#pragma unroll
+        for (int g = 0; g < G; ++g) bnd = fmaxf(bnd, gm[u][g] - lse[g]);
+        put_bound(w, bnd);
+      }
+    } else {
+      for (int w = tid; w < n8; w += nthr) {
+        float bnd = -INFINITY;
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+          bnd = fmaxf(bnd, __ldcg(m8 + (static_cast<size_t>(pair) * G + g) * n8 + w) - lse[g]);
+        put_bound(w, bnd);
+      }
     }
     nz = __reduce_add_sync(0xffffffffu, nz);
     if (lane == 0 && nz) atomicAdd(nnz_slot, nz);
     __syncthreads();
     uint32_t B = 1u;    // fewer than k groups with a valid chunk: all of them are candidates
     if (*nnz_slot >= k) {
-      int unused;
-      block_kth(bkey, n8, k, ks, &B, &unused);
+      if (n8 <= 2048) {
+        block_kth_256<8>(bkey, n8, k, ks);
+        __syncthreads();
+        B = static_cast<uint32_t>(ks[kKth8T]);
+      } else {
+        int unused;
+        block_kth(bkey, n8, k, ks, &B, &unused);
+      }
     }
     // candidate groups, compacted by warps of 32 groups
     for (int w0 = warp * 32; w0 < n8; w0 += nthr) {
@@ -239,8 +277,9 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
         // Tk are taken (every chunk equal to Tk is a survivor)
         uint32_t Tk;
         int need;
-        if (nsurv <= 1024) {
-          block_kth_256(vals, nsurv, k, ks);
+        if (nsurv <= 2048) {
+          if (nsurv <= 1024) block_kth_256<4>(vals, nsurv, k, ks);
+          else block_kth_256<8>(vals, nsurv, k, ks);
           __syncthreads();
           Tk = static_cast<uint32_t>(ks[kKth8T]);
           need = ks[kKth8Need];
@@ -344,10 +383,9 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
   }
   for (int i = tid; i < k; i += nthr) s_hit[i] = 0;
   __syncthreads();
-  // slots whose chunk is selected again keep it (hits)
-  int32_t* sc_row = slot_chunk + static_cast<size_t>(pair) * k;
+  // slots whose chunk is selected again keep it (hits); k <= blockDim.x
   for (int i = tid; i < k; i += nthr) {
-    int ch = cache_on ? sc_row[i] : -1;
+    int ch = my_slot_chunk;
     if (ch >= n) { flag_error(status, DEV_BAD_CHUNK); ch = -1; }
     int keep = 0;
     if (ch >= 0 && ((words[ch >> 5] >> (ch & 31)) & 1u)) {
@@ -362,9 +400,11 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
   // the m-th missing chunk (ascending) takes the m-th freed slot (ascending)
   const int is_miss = tid < k ? !s_hit[tid] : 0;
   const int is_free = tid < k ? !s_keep[tid] : 0;
-  int nmiss, nfree;
-  const int mrank = block_exclusive_scan(is_miss, tmp, &nmiss);
-  const int frank = block_exclusive_scan(is_free, tmp, &nfree);
+  // both ranks from one scan (counts < 2^16)
+  int both;
+  const int ranks = block_exclusive_scan(is_miss | (is_free << 16), tmp, &both);
+  const int mrank = ranks & 0xffff, frank = ranks >> 16;
+  const int nmiss = both & 0xffff, nfree = both >> 16;
   if (is_free) s_free[frank] = tid;
   // the attention's order of the selected chunks' slots: hits first (each
   // after the hits before it), then misses
