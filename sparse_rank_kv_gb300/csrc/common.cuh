@@ -441,10 +441,14 @@ __device__ __forceinline__ void block_kth(const uint32_t* v, int cnt, int kth, i
 // thread): far fewer threads wait at each of the passes' barriers.  The
 // k-th largest lands in scratch[kKth8T] and the count of its equals within
 // the top kth in scratch[kKth8Need]; the caller synchronises the block before
-// reading them.  scratch holds kKth8Ints ints.
+// reading them.  scratch holds kKth8Ints ints.  With max_passes < 4 the
+// select may stop before the last digit: scratch[kKth8T] is then the lower
+// edge of the digit range that holds the k-th largest (a lower bound of it)
+// and scratch[kKth8Need] is not meaningful.
 constexpr int kKth8T = 8 * 256 + 256 + 4, kKth8Need = kKth8T + 1, kKth8Ints = 8 * 256 + 256 + 8;
 template <int V = 4>
-__device__ __forceinline__ void block_kth_256(const uint32_t* v, int cnt, int kth, int* scratch) {
+__device__ __forceinline__ void block_kth_256(const uint32_t* v, int cnt, int kth, int* scratch,
+                                              int max_passes = 4) {
   const int tid = threadIdx.x;
   if (tid >= 256) return;
   const int lane = tid & 31, warp = tid >> 5;
@@ -483,7 +487,7 @@ __device__ __forceinline__ void block_kth_256(const uint32_t* v, int cnt, int kt
   int hb = span ? 32 - __clz(span) : 1;
   uint32_t prefix = 0, pmask = 0;
   int need = kth;
-  while (hb > 0) {
+  for (int pass = 0; hb > 0 && pass < max_passes; ++pass) {
     const int width = hb < 8 ? hb : 8;
     const int shift = hb - width;
     const uint32_t dmask = (1u << width) - 1u;

@@ -208,7 +208,9 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
     uint32_t B = 1u;    // fewer than k groups with a valid chunk: all of them are candidates
     if (*nnz_slot >= k) {
       if (n8 <= 2048) {
-        block_kth_256<8>(bkey, n8, k, ks);
+        // two 8-bit digits: B is the lower edge of the range that holds the
+        // k-th largest bound, still a lower bound of the k-th largest S2
+        block_kth_256<8>(bkey, n8, k, ks, 2);
         __syncthreads();
         B = static_cast<uint32_t>(ks[kKth8T]);
       } else {
