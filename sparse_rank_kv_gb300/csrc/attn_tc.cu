@@ -94,7 +94,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
   int* s_task = reinterpret_cast<int*>(misc + 204);
   int* s_ndone = reinterpret_cast<int*>(misc + 208);
   int* s_done = reinterpret_cast<int*>(misc + 328);       // [kAtDone] heads of finished items
-  int* info = reinterpret_cast<int*>(misc + 256);         // [kAtStages][6]: head (-1: no more), tokens, partial slot
+  int* info = reinterpret_cast<int*>(misc + 256);         // [kAtStages][6]: head (-1: no more), tokens, partial slot, kind
   float* red = reinterpret_cast<float*>(misc + 512);      // [2][4][8] maxima, then sums at +32
   int* s_p0 = reinterpret_cast<int*>(misc + kAtMisc);     // [npairs + 1] phase-0 item prefix
   int* s_p1 = s_p0 + npairs + 1;                          // [npairs + 1] phase-1 item prefix
@@ -225,8 +225,10 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
 #pragma unroll
     for (int i = 0; i < kAtStages; ++i) lastA[i] = -1;
     // phase-0 item numbers are requested two items ahead, so the atomics'
-    // round trips overlap the copies; phase 1 (a few items per CTA) runs one
-    // number ahead, which spreads its items over more CTAs
+    // round trips overlap the copies; in phase 1 (about one item per CTA)
+    // the next number is requested only once the current item's copies are
+    // issued, so that every CTA has taken its first item before any takes a
+    // second
     int phase = 0, x = 0, x1 = 0;
     if (lane == 0) {
       x = atomicAdd(&ctr[0], 1);
@@ -248,10 +250,9 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
       // cache slots of the item's chunks (lane = chunk), loaded before the wait
       const int nch = t.seg >= 2 ? t.cnt / c : 0;
       const int slot = lane < nch ? att_slot[static_cast<size_t>(t.pair) * k + t.t0 + lane] : 0;
-      // the number after the next one (phase 1: the next one), requested
-      // before this item's copies
+      // the number after the next one, requested before this item's copies
       int xn = 0;
-      if (lane == 0 && !done) xn = atomicAdd(&ctr[phase], 1);
+      if (lane == 0 && !done && phase == 0) xn = atomicAdd(&ctr[0], 1);
       bool ok = true;
       if (lane == 0) ok = !*s_abort && tc::mbar_wait(&empty[st], (use & 1) ^ 1, kWaitLimit);
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -310,6 +311,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
         inf[0] = t.pair;
         inf[1] = t.cnt;
         inf[2] = t.li;
+        inf[3] = t.seg;
         tc::mbar_expect_tx(&full[st], static_cast<uint32_t>(groups * 4096 + kAtQBytes));
         tc::tma_load_4d(sR + kAtRec, &mapQ, &full[st], 0, 0, 0, t.pair);
         if (t.seg == 0)
@@ -330,6 +332,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
       }
       lastA[st] = use;
       if (phase == 1) {
+        if (lane == 0) xn = atomicAdd(&ctr[1], 1);
         x = xn;
       } else {
         x = x1;
@@ -477,7 +480,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
       if (dead || *s_end == it) break;
       // the item's description (its stage is complete and not yet reused)
       if (!tc::mbar_wait(&full[st], (it / kAtStages) & 1, kWaitLimit) && lane == 0) abort_now();
-      const int pair = info[st * 6], cnt = info[st * 6 + 1], li = info[st * 6 + 2];
+      const int pair = info[st * 6], cnt = info[st * 6 + 1], li = info[st * 6 + 2], seg = info[st * 6 + 3];
       float s[8];
       tc::fence_after();
       load_cols(tmem + tlane + sb * 16, s);
@@ -524,6 +527,13 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
       for (int g = 0; g < G; ++g) {
         pm[g] = mi[g];
         pl[g] = li_sum[g];
+      }
+      if (seg == 3) {
+        // a missed-chunk item (the step's tail): its partial and its head's
+        // ticket at once, without waiting for the next item
+        finish();
+        pj = -1;
+        publish();
       }
     }
     if (pj >= 0 && !dead) {
