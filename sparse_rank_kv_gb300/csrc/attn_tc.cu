@@ -461,7 +461,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
     auto publish = [&]() {
       tc::named_sync(1, kAtSoft);
       if (ct == 0 && *s_ndone > 0) {
-        __threadfence();
+        tc::fence_acq_rel_gpu();
         for (int i = 0; i < *s_ndone; ++i) atomicAdd(&ticket[s_done[i]], 1);
         *s_ndone = 0;
       }
@@ -678,7 +678,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
       // the groups' values are visible at device scope (and ordered before
       // the consuming CTA's bulk copies) before their items' counts move
       tc::fence_proxy_async_global();
-      __threadfence();
+      tc::fence_acq_rel_gpu();
       __syncwarp();
       if (q == 0)
 #pragma unroll

@@ -235,6 +235,11 @@ __device__ __forceinline__ void cp_async_wait() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Release/acquire fence at device scope: the writes before it (and, through
+// a preceding CTA barrier, the CTA's) are visible to a thread that acquires
+// a flag written after it.  Lighter than the sequentially consistent fence of
+// __threadfence(), which release/acquire hand-offs do not need.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 // Orders this thread's generic-proxy view of global memory with its
 // async-proxy (bulk copy) accesses.
 __device__ __forceinline__ void fence_proxy_async_global() {
