@@ -158,7 +158,7 @@ skv_status shadowkv_load_state(const shadowkv_params* p, const shadowkv_state_in
  * selects the top-k chunks per KV head (ties to the lower index), rebuilds
  * their keys as RoPE(Gather(A, I) B) at their token positions, takes their
  * values from the GPU chunk cache (hits of the previous step) or from pinned
- * host memory (misses, fetched while the keys are rebuilt), and writes
+ * host memory (misses, fetched while the rest is attended), and writes
  * softmax(q K^T / sqrt(d)) V over [outliers; rebuilt chunks; local window].
  * The kernels read q in place through tensor maps: q must be 16-byte aligned
  * (else SKV_ERR_INVALID_ARG before any work is enqueued) and must not change
@@ -276,8 +276,9 @@ int shadowkv_num_kernels(void);
 const char* shadowkv_kernel_name(int id);
 /* With SKV_OPT_TIMING on: total milliseconds and launch count per kernel id
  * since the last reset (arrays of n entries).  Synchronizes.  With K/V
- * records (bf16, d = 128) the value fetch runs inside the "rebuild" launch,
- * and "fetch" counts no launches.  The events recorded between launches
+ * records (bf16, d = 128) the value fetch runs inside the "attention" launch
+ * (or, with SKV_OPT_SPLIT_TOKENS set, inside the "rebuild" launch), and
+ * "fetch" counts no launches.  The events recorded between launches
  * remove the overlap between consecutive kernels, so the per-kernel times sum
  * to more than a step takes with timing off. */
 skv_status shadowkv_kernel_times(shadowkv_ctx* ctx, double* ms, long long* launches, int n);

@@ -18,8 +18,8 @@ enum KernelId {
   K_SCORE = 0,      // landmark scores P = q L^T / sqrt(d) and per-tile softmax stats
   K_SELECT,         // S2, top-k, cache set difference, local-window append
   K_FETCH,          // value misses from pinned host memory into cache slots (side stream)
-  K_REBUILD,        // RoPE(Gather(A, I) B); with K/V records also the value fetch
-  K_ATTN,           // attention over [outliers; rebuilt chunks; local window] and its merge
+  K_REBUILD,        // RoPE(Gather(A, I) B); with K/V records and the classic attention also the value fetch
+  K_ATTN,           // attention over [outliers; rebuilt chunks; local window] and its merge; tensor-core path also the value fetch
   K_CHUNKSTATS,     // prefill: RoPE, chunk means, min cosine
   K_OUTLIERS,       // prefill: ArgTopK(-min cos, o) + mask
   K_GATHER,         // prefill: outlier / local-window rows
@@ -38,7 +38,8 @@ struct Timed {
 
 // SMs reserved for the host-memory value fetch, which runs next to the key
 // rebuild: on a side stream, the rebuild's grid leaving it these SMs, or
-// (records) as the first CTAs of the rebuild's own launch.  When only the
+// (records with the classic attention) as the first CTAs of the rebuild's own
+// launch; the tensor-core attention moves the values with its own warps.  When only the
 // missed chunks are rebuilt (records) the rebuild is small and the fetch gets
 // more SMs.
 constexpr int kFetchSMs = 16;
