@@ -287,16 +287,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
         // all of its groups, then zero the count for the next step
         bool got = true;
         if (lane == 0) {
-          const uint64_t w0 = tc::globaltimer_ns();
-          for (;;) {
-            int v;
-            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(item_done + x) : "memory");
-            if (v >= groups) break;
-            if (*s_abort || tc::globaltimer_ns() - w0 > kWaitLimit) {
-              got = false;
-              break;
-            }
-          }
+          got = tc::wait_count(item_done + x, groups, kWaitLimit, s_abort);
           if (got) {
             item_done[x] = 0;
             tc::fence_proxy_async_global();
@@ -558,14 +549,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
       if (pair >= npairs) break;
       const int ntot = s_p0[pair + 1] - s_p0[pair] + s_p1[pair + 1] - s_p1[pair];
       if (ct == 0) {
-        bool ok = ntot <= wcap;
-        const uint64_t t0 = tc::globaltimer_ns();
-        while (ok) {
-          int v;
-          asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ticket + pair) : "memory");
-          if (v >= ntot) break;
-          if (tc::globaltimer_ns() - t0 > kWaitLimit) ok = false;
-        }
+        const bool ok = ntot <= wcap && tc::wait_count(ticket + pair, ntot, kWaitLimit, s_abort);
         if (!ok) abort_now();
       }
       tc::named_sync(1, kAtSoft);

@@ -235,6 +235,22 @@ __device__ __forceinline__ void cp_async_wait() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Waits until the int at p reaches at least `target`, polling with relaxed
+// loads and a short sleep between them (acquire loads in a tight loop keep
+// invalidating the SM's L1 and flood the counter's L2 line), then issues one
+// acquire fence.  False once `limit_ns` has passed or *abort is set.
+__device__ __forceinline__ bool wait_count(const int* p, int target, uint64_t limit_ns, volatile int* abort) {
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v >= target) break;
+    if ((abort && *abort) || globaltimer_ns() - t0 > limit_ns) return false;
+    __nanosleep(64);
+  }
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+  return true;
+}
 // Release/acquire fence at device scope: the writes before it (and, through
 // a preceding CTA barrier, the CTA's) are visible to a thread that acquires
 // a flag written after it.  Lighter than the sequentially consistent fence of
