@@ -207,16 +207,12 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
     __syncthreads();
     uint32_t B = 1u;    // fewer than k groups with a valid chunk: all of them are candidates
     if (*nnz_slot >= k) {
-      if (n8 <= 2048) {
-        // two 8-bit digits: B is the lower edge of the range that holds the
-        // k-th largest bound, still a lower bound of the k-th largest S2
-        block_kth_256<8>(bkey, n8, k, ks, 2);
-        __syncthreads();
-        B = static_cast<uint32_t>(ks[kKth8T]);
-      } else {
-        int unused;
-        block_kth(bkey, n8, k, ks, &B, &unused);
-      }
+      // two 8-bit digits: B is the lower edge of the range that holds the
+      // k-th largest bound, still a lower bound of the k-th largest S2
+      if (n8 <= 2048) block_kth_256<8>(bkey, n8, k, ks, 2);
+      else block_kth_256<16>(bkey, n8, k, ks, 2);
+      __syncthreads();
+      B = static_cast<uint32_t>(ks[kKth8T]);
     }
     // candidate groups, compacted by warps of 32 groups
     for (int w0 = warp * 32; w0 < n8; w0 += nthr) {
@@ -230,15 +226,17 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
     }
     __syncthreads();
     const int ne = *ncand_slot * 8;
-    if (ne <= cap) {
-      // the candidates' chunks: all loads of a thread (<= 4 chunks) issued
-      // before any key is formed; survivors appended by warp ballots
+    if (ne <= 2 * cap) {
+      // the candidates' chunks, in rounds of 4 per thread: all loads of a
+      // round issued before any key is formed; survivors appended by warp
+      // ballots (at most cap of them are kept)
+      for (int h0 = 0; h0 < ne; h0 += 4 * nthr) {
       float pv[4][G];
       int jj[4];
       uint32_t mw[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int e = u * nthr + tid;
+        const int e = h0 + u * nthr + tid;
         jj[u] = -1;
         mw[u] = 0u;
         if (e < ne) {
@@ -253,7 +251,7 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        if (u * nthr >= ne) break;
+        if (h0 + u * nthr >= ne) break;
         uint32_t key = 0u;
         if (jj[u] >= 0 && !((mw[u] >> (jj[u] & 31)) & 1u)) {
           float sm = -INFINITY;
@@ -266,28 +264,26 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
         int base = 0;
         if (lane == 0 && m) base = atomicAdd(cnt_slot, __popc(m));
         base = __shfl_sync(0xffffffffu, base, 0);
-        if (keep) {
-          const int pos = base + __popc(m & ((1u << lane) - 1u));
+        const int pos = base + __popc(m & ((1u << lane) - 1u));
+        if (keep && pos < cap) {
           vals[pos] = key;
           vidx[pos] = jj[u];
         }
       }
+      }
       __syncthreads();
       const int nsurv = *cnt_slot;
-      if (nsurv >= k) {
+      if (nsurv >= k && nsurv <= cap) {
         // Tk = the k-th largest survivor; `need` of the survivors equal to
         // Tk are taken (every chunk equal to Tk is a survivor)
         uint32_t Tk;
         int need;
-        if (nsurv <= 2048) {
-          if (nsurv <= 1024) block_kth_256<4>(vals, nsurv, k, ks);
-          else block_kth_256<8>(vals, nsurv, k, ks);
-          __syncthreads();
-          Tk = static_cast<uint32_t>(ks[kKth8T]);
-          need = ks[kKth8Need];
-        } else {
-          block_kth(vals, nsurv, k, ks, &Tk, &need);
-        }
+        if (nsurv <= 1024) block_kth_256<4>(vals, nsurv, k, ks);
+        else if (nsurv <= 2048) block_kth_256<8>(vals, nsurv, k, ks);
+        else block_kth_256<16>(vals, nsurv, k, ks);
+        __syncthreads();
+        Tk = static_cast<uint32_t>(ks[kKth8T]);
+        need = ks[kKth8Need];
         for (int w = tid; w < nw; w += nthr) words[w] = 0u;
         int eq = 0;
         for (int i = tid; i < nsurv; i += nthr) eq += vals[i] == Tk;
