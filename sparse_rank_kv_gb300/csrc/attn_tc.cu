@@ -22,12 +22,14 @@
 //                one of two TMEM S buffers; after the softmax warps publish
 //                P, O = V^T P^T (M = d, N = 16, K = 16-token steps) into one
 //                of two TMEM O buffers, polling both queues.
-//   warps 2..5 : softmax, thread = TMEM lane: for S the token row (scale,
-//                mask, head maxima by integer warp reductions, p = 2^(s - m),
+//   warps 2..9 : softmax, two groups of four taking alternate items (each
+//                with its own S, O and P^T buffers); thread = TMEM lane: for S
+//                the token row (scale, mask, head maxima by integer warp
+//                reductions, p = 2^(s - m),
 //                bf16 P^T into shared memory, head sums), for O the dimension:
 //                the item's partial (max, sum, sum p v) per query head goes to
 //                the item's slot, and a ticket per head counts finished items.
-//   warps 6..9 : the step's value fetch (Algorithm 2 step 3, V from the host):
+//   warps 10..13: the step's value fetch (Algorithm 2 step 3, V from the host):
 //                8-token groups of the missed chunks, taken from a fourth
 //                counter in phase-1 item order, read from pinned host memory
 //                through its device mapping and written as the V^T half of the
@@ -45,13 +47,14 @@ constexpr int kAtT = 128;                    // tokens per item
 constexpr int kAtD = 128;                    // head dimension handled here
 constexpr int kAtStages = 3;
 constexpr int kAtFetchWarps = 4;
-constexpr int kAtThreads = 192 + 32 * kAtFetchWarps;
+constexpr int kAtSoftGroups = 2;            // softmax warpgroups, taking alternate items
+constexpr int kAtThreads = 64 + 128 * kAtSoftGroups + 32 * kAtFetchWarps;
 constexpr int kAtSoft = 128;                 // softmax threads
 constexpr int kAtRec = kAtT / 8 * 4096;      // 16 group records (K tile | V^T tile)
 constexpr int kAtQBytes = 16 * kAtD * 2;     // q: 4 x [16 rows][64 B]
 constexpr int kAtStage = kAtRec + kAtQBytes;
 constexpr int kAtPBytes = 16 * kAtT * 2;     // P^T: 16 x 128 bf16
-constexpr int kAtMisc = 1024;                // barriers, item descriptions, reductions
+constexpr int kAtMisc = 1280;                // barriers, item descriptions, reductions, the second group's lists
 constexpr int kAtDone = 44;                  // finished items whose tickets are not yet counted
 __host__ __device__ constexpr int at_smem_bytes(int npairs) {
   return 1024 /* alignment slack */ + kAtStages * kAtStage + 2 * kAtPBytes + kAtMisc + (3 * npairs + 2) * 4;
@@ -91,9 +94,11 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 192);
   volatile int* s_abort = reinterpret_cast<volatile int*>(misc + 196);
   volatile int* s_end = reinterpret_cast<volatile int*>(misc + 200);    // items of this CTA, once known
-  int* s_task = reinterpret_cast<int*>(misc + 204);
-  int* s_ndone = reinterpret_cast<int*>(misc + 208);
-  int* s_done = reinterpret_cast<int*>(misc + 328);       // [kAtDone] heads of finished items
+  // per softmax group: its current merge head, its count and list of
+  // finished items whose tickets are not yet counted
+  int* s_task_g[2] = {reinterpret_cast<int*>(misc + 204), reinterpret_cast<int*>(misc + 1216)};
+  int* s_ndone_g[2] = {reinterpret_cast<int*>(misc + 208), reinterpret_cast<int*>(misc + 1220)};
+  int* s_done_g[2] = {reinterpret_cast<int*>(misc + 328), reinterpret_cast<int*>(misc + 1024)};   // [kAtDone]
   int* info = reinterpret_cast<int*>(misc + 256);         // [kAtStages][6]: head (-1: no more), tokens, partial slot, kind
   float* red = reinterpret_cast<float*>(misc + 512);      // [2][4][8] maxima, then sums at +32
   int* s_p0 = reinterpret_cast<int*>(misc + kAtMisc);     // [npairs + 1] phase-0 item prefix
@@ -121,7 +126,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
     tc::fence_mbar_init();
     *s_abort = 0;
     *s_end = -1;
-    *s_ndone = 0;
+    *s_ndone_g[0] = *s_ndone_g[1] = 0;
     // the next step's counters start at zero
     if (blockIdx.x == 0) ctr_next[0] = ctr_next[1] = ctr_next[2] = ctr_next[3] = 0;
   }
@@ -348,10 +353,16 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
               tc::mbar_test(&sempty[sb], ((ns >> 1) & 1) ^ 1)) {
             tc::fence_after();
             if (info[st * 6] < 0) {
-              // the producer has no more items: tell the softmax warps
+              // the producer has no more items: tell the softmax group of
+              // index ns, then the group of index ns + 1, once it has read
+              // the other buffer's S of index ns - 1 (the same condition as
+              // for issuing S of index ns + 1; an earlier arrival would end
+              // that phase twice)
               nit = ns;
               *s_end = ns;
               tc::mbar_arrive(&sfull[sb]);
+              if (tc::mbar_wait(&sempty[sb ^ 1], (((ns + 1) >> 1) & 1) ^ 1, kWaitLimit)) tc::mbar_arrive(&sfull[sb ^ 1]);
+              else abort_now();
             } else {
               const uint32_t a0 = tc::smem_u32(stages + st * kAtStage);
               const uint32_t b0 = a0 + kAtRec;
@@ -393,7 +404,8 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
         } else if (*s_abort || tc::globaltimer_ns() - t_last > kWaitLimit) {
           abort_now();
           *s_end = ns;
-          tc::mbar_arrive(&sfull[ns & 1]);
+          tc::mbar_arrive(&sfull[0]);
+          tc::mbar_arrive(&sfull[1]);
           break;
         }
       }
@@ -401,9 +413,15 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
       if (no > 0) tc::mbar_wait(&ofull[(no - 1) & 1], ((no - 1) >> 1) & 1, kWaitLimit);
     }
     __syncwarp();
-  } else if (warp < 6) {
+  } else if (warp < 2 + 4 * kAtSoftGroups) {
     // ------------------------------------------------------------ softmax
-    const int ct = tid - 64, quarter = warp & 3;
+    // group gs takes the items of its parity: their S and O buffers, P^T
+    // buffer and reduction scratch are its own; it meets at named barrier bar
+    const int gs = (warp - 2) >> 2, bar = gs ? 3 : 1;
+    int* s_done = s_done_g[gs];
+    int* s_ndone = s_ndone_g[gs];
+    int* s_task = s_task_g[gs];
+    const int ct = tid - 64 - 128 * gs, quarter = warp & 3;
     const int row = quarter * 32 + lane;          // TMEM lane: token row for S, dimension for O
     const uint32_t tlane = static_cast<uint32_t>(quarter * 32) << 16;
     auto load_cols = [&](uint32_t taddr, float* v) {
@@ -450,15 +468,15 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
       if (ct == 0) s_done[(*s_ndone)++] = ppair;
     };
     auto publish = [&]() {
-      tc::named_sync(1, kAtSoft);
+      tc::named_sync(bar, kAtSoft);
       if (ct == 0 && *s_ndone > 0) {
         tc::fence_acq_rel_gpu();
         for (int i = 0; i < *s_ndone; ++i) atomicAdd(&ticket[s_done[i]], 1);
         *s_ndone = 0;
       }
-      tc::named_sync(1, kAtSoft);
+      tc::named_sync(bar, kAtSoft);
     };
-    for (int it = 0;; ++it) {
+    for (int it = gs;; it += kAtSoftGroups) {
       const int sb = it & 1, st = it % kAtStages;
       if (!dead) {
         bool ok = !*s_abort && tc::mbar_wait(&sfull[sb], (it >> 1) & 1, kWaitLimit);
@@ -468,7 +486,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
           dead = true;
         }
       }
-      if (dead || *s_end == it) break;
+      if (dead || (*s_end >= 0 && it >= *s_end)) break;
       // the item's description (its stage is complete and not yet reused)
       if (!tc::mbar_wait(&full[st], (it / kAtStages) & 1, kWaitLimit) && lane == 0) abort_now();
       const int pair = info[st * 6], cnt = info[st * 6 + 1], li = info[st * 6 + 2], seg = info[st * 6 + 3];
@@ -486,7 +504,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
         const uint32_t m = __reduce_max_sync(0xffffffffu, order_key(s[g]));
         if (lane == 0) rmax[quarter * 8 + g] = from_order_key(m);
       }
-      tc::named_sync(1, kAtSoft);
+      tc::named_sync(bar, kAtSoft);
       unsigned char* P = pbuf + sb * kAtPBytes;
       float mi[G];
 #pragma unroll
@@ -502,7 +520,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
         if (lane == 0) rmax[32 + quarter * 8 + g] = z;
       }
       tc::fence_proxy_async_smem();
-      tc::named_sync(1, kAtSoft);
+      tc::named_sync(bar, kAtSoft);
       if (ct == 0) tc::mbar_arrive(&pfull[sb]);
       float li_sum[G];
 #pragma unroll
@@ -538,21 +556,21 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
     // its items' partials, then merges them (weights 2^(m - M) / sum)
     // [G][wcap] maxima, turned into weights, then [G][wcap] sums (P^T is no
     // longer used)
-    float* w = reinterpret_cast<float*>(pbuf);
-    const int wcap = kAtPBytes / 4 / G;
+    float* w = reinterpret_cast<float*>(pbuf + gs * kAtPBytes);
+    const int wcap = kAtPBytes / 8 / G;
     float* lsum = w + G * wcap;
     while (!dead) {
       if (ct == 0) *s_task = atomicAdd(&ctr[2], 1);
-      tc::named_sync(1, kAtSoft);
+      tc::named_sync(bar, kAtSoft);
       const int pair = *s_task;
-      tc::named_sync(1, kAtSoft);
+      tc::named_sync(bar, kAtSoft);
       if (pair >= npairs) break;
       const int ntot = s_p0[pair + 1] - s_p0[pair] + s_p1[pair + 1] - s_p1[pair];
       if (ct == 0) {
         const bool ok = ntot <= wcap && tc::wait_count(ticket + pair, ntot, kWaitLimit, s_abort);
         if (!ok) abort_now();
       }
-      tc::named_sync(1, kAtSoft);
+      tc::named_sync(bar, kAtSoft);
       if (*s_abort) break;
       const size_t pb = static_cast<size_t>(pair) * G * max_splits;
       // every item's (max, sum) per query head, one round trip
@@ -562,10 +580,10 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
         w[g * wcap + i] = __ldcg(pp);
         lsum[g * wcap + i] = __ldcg(pp + 1);
       }
-      tc::named_sync(1, kAtSoft);
-      if (warp - 2 < G) {
+      tc::named_sync(bar, kAtSoft);
+      if (((warp - 2) & 3) < G) {
         // warp g: M, the sum of 2^(m - M) l, then the weights 2^(m - M) / sum
-        for (int gg = warp - 2; gg < G; gg += 4) {
+        for (int gg = (warp - 2) & 3; gg < G; gg += 4) {
           float M = -INFINITY;
           for (int i = lane; i < ntot; i += 32) M = fmaxf(M, w[gg * wcap + i]);
           M = warp_max(M);
@@ -576,7 +594,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
           for (int i = lane; i < ntot; i += 32) w[gg * wcap + i] = exp2f(w[gg * wcap + i] - M) * inv;
         }
       }
-      tc::named_sync(1, kAtSoft);
+      tc::named_sync(bar, kAtSoft);
       // sum over items of weight x partial: items outermost, so that the
       // loads of all heads for 8 items are in flight together
       float num[G];
@@ -604,7 +622,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
       for (int g = 0; g < G; ++g)
         out[(static_cast<size_t>(pair) * G + g) * kAtD + row] = __float2bfloat16_rn(num[g]);
       if (ct == 0) ticket[pair] = 0;
-      tc::named_sync(1, kAtSoft);
+      tc::named_sync(bar, kAtSoft);
     }
   } else if (vcpu != nullptr) {
     // ------------------------------------------------------------ value fetch
@@ -723,7 +741,7 @@ bool attn_tc_supported(const shadowkv_params& p) {
   const int items = at_items_max(p, p.w + p.max_new);
   return p.dtype == SKV_DTYPE_BF16 && p.d == kAtD && p.c % 8 == 0 && kAtT % p.c == 0 &&
          static_cast<long long>(p.b) * p.h_kv <= npairs_max && at_smem_bytes(npairs_max) <= 227 * 1024 &&
-         G >= 1 && items * G <= kAtPBytes / 4;
+         G >= 1 && items * G <= kAtPBytes / 8;
 }
 
 template <int G>
