@@ -573,7 +573,19 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
       tc::named_sync(bar, kAtSoft);
       if (*s_abort) break;
       const size_t pb = static_cast<size_t>(pair) * G * max_splits;
-      // every item's (max, sum) per query head, one round trip
+      const float* pr = part + pb * (kAtD + 2) + row;
+      // R items' partial rows per round; the first round is loaded together
+      // with every item's (max, sum), before the weights are known
+      constexpr int R = 64 / G;
+      float v[R][G];
+      auto load_round = [&](int i0) {
+#pragma unroll
+        for (int u = 0; u < R; ++u)
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+            v[u][g] = i0 + u < ntot ? __ldcg(pr + (static_cast<size_t>(g) * max_splits + i0 + u) * (kAtD + 2)) : 0.f;
+      };
+      load_round(0);
       for (int e = ct; e < G * ntot; e += kAtSoft) {
         const int g = e / ntot, i = e - g * ntot;
         const float* pp = part + (pb + static_cast<size_t>(g) * max_splits + i) * (kAtD + 2) + kAtD;
@@ -595,29 +607,18 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
         }
       }
       tc::named_sync(bar, kAtSoft);
-      // sum over items of weight x partial: items outermost, so that the
-      // loads of all heads for 8 items are in flight together
+      // sum over items of weight x partial row
       float num[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) num[g] = 0.f;
-      const float* pr = part + pb * (kAtD + 2) + row;
-      int i = 0;
-      for (; i + 8 <= ntot; i += 8) {
-        float v[8][G];
+      for (int i0 = 0; i0 < ntot; i0 += R) {
+        if (i0 > 0) load_round(i0);
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
+        for (int u = 0; u < R; ++u)
 #pragma unroll
           for (int g = 0; g < G; ++g)
-            v[u][g] = __ldcg(pr + (static_cast<size_t>(g) * max_splits + i + u) * (kAtD + 2));
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-#pragma unroll
-          for (int g = 0; g < G; ++g) num[g] = fmaf(w[g * wcap + i + u], v[u][g], num[g]);
+            if (i0 + u < ntot) num[g] = fmaf(w[g * wcap + i0 + u], v[u][g], num[g]);
       }
-      for (; i < ntot; ++i)
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-          num[g] = fmaf(w[g * wcap + i], __ldcg(pr + (static_cast<size_t>(g) * max_splits + i) * (kAtD + 2)), num[g]);
 #pragma unroll
       for (int g = 0; g < G; ++g)
         out[(static_cast<size_t>(pair) * G + g) * kAtD + row] = __float2bfloat16_rn(num[g]);
