@@ -118,6 +118,7 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
       }
     }
   }
+  for (int i = tid; i < k; i += nthr) s_hit[i] = 0;
   // this head's cache slots (written by the previous step's selection)
   int32_t* sc_row = slot_chunk + static_cast<size_t>(pair) * k;
   const int my_slot_chunk = cache_on && tid < k ? sc_row[tid] : -1;
@@ -379,8 +380,6 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
     __syncthreads();
     block_topk(keys, n, k, s_sel, scratch, words, wpref);
   }
-  for (int i = tid; i < k; i += nthr) s_hit[i] = 0;
-  __syncthreads();
   // slots whose chunk is selected again keep it (hits); k <= blockDim.x
   for (int i = tid; i < k; i += nthr) {
     int ch = my_slot_chunk;
@@ -419,18 +418,18 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
     if (pair == 0) miss_total[par ^ 1] = 0;
   }
   __syncthreads();
-  if (is_miss && mrank < nfree) {
-    const int slot = s_free[mrank];
-    s_slot[tid] = slot;
-    sc_row[slot] = s_sel[tid];
-    miss_chunk[s_base + mrank] = pair * n + s_sel[tid];
-    miss_slot[s_base + mrank] = pair * k + slot;
-    if (att_slot != nullptr) att_slot[static_cast<size_t>(pair) * k + (k - nmiss) + mrank] = slot;
-  }
-  __syncthreads();
-  for (int i = tid; i < k; i += nthr) {
-    sel[static_cast<size_t>(pair) * k + i] = s_sel[i];
-    sel_slot[static_cast<size_t>(pair) * k + i] = s_slot[i];
+  // (k <= blockDim.x: thread i writes selection entry i, its slot included)
+  if (tid < k) {
+    int slot = s_slot[tid];
+    if (is_miss && mrank < nfree) {
+      slot = s_free[mrank];
+      sc_row[slot] = s_sel[tid];
+      miss_chunk[s_base + mrank] = pair * n + s_sel[tid];
+      miss_slot[s_base + mrank] = pair * k + slot;
+      if (att_slot != nullptr) att_slot[static_cast<size_t>(pair) * k + (k - nmiss) + mrank] = slot;
+    }
+    sel[static_cast<size_t>(pair) * k + tid] = s_sel[tid];
+    sel_slot[static_cast<size_t>(pair) * k + tid] = slot;
   }
   if (tid == 0) {
     hits[pair] = k - nmiss;
