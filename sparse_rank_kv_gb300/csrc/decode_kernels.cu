@@ -381,6 +381,7 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
     block_topk(keys, n, k, s_sel, scratch, words, wpref);
   }
   // slots whose chunk is selected again keep it (hits); k <= blockDim.x
+  int my_keep = 0;
   for (int i = tid; i < k; i += nthr) {
     int ch = my_slot_chunk;
     if (ch >= n) { flag_error(status, DEV_BAD_CHUNK); ch = -1; }
@@ -392,8 +393,18 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
       keep = 1;
     }
     s_keep[i] = keep;
+    my_keep = keep;
   }
-  __syncthreads();
+  // the head's misses (each kept slot is one hit): its range of the step's
+  // compact miss list is reserved now, the atomic's round trip overlapping
+  // the scan below; the block of head 0 also clears the other step
+  // parity's counter for the next step
+  const int nres = k - __syncthreads_count(my_keep);
+  int base_r = 0;
+  if (tid == 0) {
+    base_r = atomicAdd(&miss_total[par], nres);
+    if (pair == 0) miss_total[par ^ 1] = 0;
+  }
   // the m-th missing chunk (ascending) takes the m-th freed slot (ascending)
   const int is_miss = tid < k ? !s_hit[tid] : 0;
   const int is_free = tid < k ? !s_keep[tid] : 0;
@@ -408,20 +419,17 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
   if (att_slot != nullptr && tid < k && !is_miss)
     att_slot[static_cast<size_t>(pair) * k + tid - mrank] = s_slot[tid];
   __syncthreads();
-  if (nmiss != nfree) flag_error(status, DEV_BAD_COUNT);
-  // reserve this head's range of the step's compact miss list; the block of
-  // head 0 also clears the other step parity's counter for the next step
+  if (nmiss != nfree || nmiss != nres) flag_error(status, DEV_BAD_COUNT);
   __shared__ int s_base;
   if (tid == 0) {
-    s_base = atomicAdd(&miss_total[par], min(nmiss, nfree));
-    miss_base[pair] = s_base;
-    if (pair == 0) miss_total[par ^ 1] = 0;
+    s_base = base_r;
+    miss_base[pair] = base_r;
   }
   __syncthreads();
   // (k <= blockDim.x: thread i writes selection entry i, its slot included)
   if (tid < k) {
     int slot = s_slot[tid];
-    if (is_miss && mrank < nfree) {
+    if (is_miss && mrank < nfree && mrank < nres) {
       slot = s_free[mrank];
       sc_row[slot] = s_sel[tid];
       miss_chunk[s_base + mrank] = pair * n + s_sel[tid];
