@@ -7,6 +7,8 @@
 //             zero-copy from pinned host memory on the side stream (row-major
 //             contexts; with K/V records the rebuild's launch does the fetch)
 // (the attention kernels are in attn*.cu, the key rebuild in rebuild.cu)
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
@@ -72,8 +74,8 @@ k_score(const T* __restrict__ L, const T* __restrict__ q, const uint32_t* __rest
 // ----------------------------------------------------------------- select
 // One block per (batch, KV head).  Shared memory: keys[n], then the cache
 // bookkeeping arrays.
-template <typename T, int D, int G>
-__global__ void __launch_bounds__(kSelectThreads)
+template <typename T, int D, int G, int NT>
+__global__ void __launch_bounds__(NT, 1024 / NT)
 k_select(const float* __restrict__ P, const float2* __restrict__ part, const float* __restrict__ m8,
          const uint32_t* __restrict__ mask, int n, int ntile, int k, int group_reduce,
          int cache_on, int32_t* __restrict__ sel, int32_t* __restrict__ sel_slot,
@@ -94,8 +96,8 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
   int* s_hit = s_slot + k;
   int* s_keep = s_hit + k;
   int* s_free = s_keep + k;
-  int* scratch = align16(s_free + k);   // topk_scratch_ints(kSelectThreads) ints, 16-byte aligned
-  float* lse = reinterpret_cast<float*>(scratch + topk_scratch_ints(kSelectThreads));  // G floats
+  int* scratch = align16(s_free + k);   // topk_scratch_ints(NT) ints, 16-byte aligned
+  float* lse = reinterpret_cast<float*>(scratch + topk_scratch_ints(NT));  // G floats
   int* tmp = scratch;          // block scans after the top-k
 
   const int pair = blockIdx.x;
@@ -603,20 +605,25 @@ cudaError_t launch_score(Ctx& c, const void* q, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-size_t select_smem_bytes(int n, int k, int G) {
+size_t select_smem_bytes(int n, int k, int G, int nthreads) {
   const int nw = (n + 31) / 32;
   return sizeof(uint32_t) * (static_cast<size_t>(n) + 2 * nw) +
-         sizeof(int) * (5 * static_cast<size_t>(k) + topk_scratch_ints(kSelectThreads)) + sizeof(float) * G + 16;
+         sizeof(int) * (5 * static_cast<size_t>(k) + topk_scratch_ints(nthreads)) + sizeof(float) * G + 16;
 }
 
 template <typename T, int D, int G>
 static cudaError_t select_t(Ctx& c, const void* k_new, const void* v_new, int loc_row,
                             cudaStream_t st) {
-  const size_t smem = select_smem_bytes(c.n, c.p.k, c.G);
-  auto kern = k_select<T, D, G>;
+  // more heads than SMs: 512-thread CTAs, two per SM (each thread keeps one
+  // cache slot, so k <= 512); else one 1024-thread CTA per head
+  constexpr bool kHalf = std::is_same<T, bf16>::value && D == 128;
+  const bool half = kHalf && c.p.b * c.p.h_kv > c.nsm && c.p.k <= kSelectThreads / 2;
+  const int nt = half ? kSelectThreads / 2 : kSelectThreads;
+  const size_t smem = select_smem_bytes(c.n, c.p.k, c.G, nt);
+  auto kern = half ? k_select<T, D, G, (kHalf ? kSelectThreads / 2 : kSelectThreads)> : k_select<T, D, G, kSelectThreads>;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(c.p.b * c.p.h_kv), dim3(kSelectThreads), smem, st,
+  return launch_pdl(kern, dim3(c.p.b * c.p.h_kv), dim3(nt), smem, st,
       c.logits, c.score_part, static_cast<const float*>(c.m8_step == c.t ? c.score_m8 : nullptr), c.out_mask,
       c.n, c.ntile, c.p.k, c.p.group_reduce,
       c.cache_on ? 1 : 0, c.sel, c.sel_slot, c.slot_chunk, c.miss_chunk, c.miss_slot,

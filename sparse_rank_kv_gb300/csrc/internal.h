@@ -136,7 +136,7 @@ struct Ctx {
   long long kcount[K_NUM] = {};
 };
 
-size_t select_smem_bytes(int n, int k, int G);
+size_t select_smem_bytes(int n, int k, int G, int nthreads = 1024);
 size_t attn_smem_bytes(int E, int G, int D, int S, int max_splits);
 
 // Records the text of a failure for shadowkv_last_error (api.cu).
