@@ -341,6 +341,8 @@ def run_ours(args, cfg):
         ctx = binding.prefill(p, inp["k_pre"], inp["v"], stream)
         torch.cuda.synchronize()
         prefill_ms.append((time.perf_counter() - t0) * 1e3)
+        if args.rebuild_in_attention:
+            ctx.set_option(binding.OPT_REBUILD_IN_ATTENTION, 1)
         if layer == 0:
             kt = ctx.kernel_times()
             prefill_kernels = {k_: {"ms": v[0], "launches": v[1]} for k_, v in kt.items()
@@ -601,6 +603,8 @@ def main():
     ap.add_argument("--budget", type=float, default=None, help="sparse budget k*c/s in percent")
     ap.add_argument("--q-sigma", type=float, default=None)
     ap.add_argument("--layers", type=int, default=1)
+    ap.add_argument("--rebuild-in-attention", action="store_true",
+                    help="rebuild the missed keys inside the attention's launch (three launches per step)")
     ap.add_argument("--svd-report", action="store_true",
                     help="SVD error and subspace similarity (on by default for the 256K workload)")
     ap.add_argument("--prefill-only", action="store_true",

@@ -203,11 +203,19 @@ enum {
                                with d = 128 and c a multiple of 8 dividing 128 use the
                                tensor-core attention over K/V records; other bf16 contexts
                                use the pipelined (TMA-fed, 64-token items) kernel */
-  SKV_OPT_CUDA_CORES = 3    /* 1: compute the landmark scores and rebuild the keys with the
+  SKV_OPT_CUDA_CORES = 3,   /* 1: compute the landmark scores and rebuild the keys with the
                                CUDA-core kernels even where the tensor-core (tcgen05) kernels
                                apply (bf16; for the rebuild also c a multiple of 8 dividing 128
                                and r a multiple of 16), and run the classic split-KV attention
                                instead of the pipelined one; for cross-checking the paths */
+  SKV_OPT_REBUILD_IN_ATTENTION = 4 /* 1: where the tensor-core attention moves the values itself
+                               (shadowkv_layout.fetch_in_attention) and the rebuild runs on the
+                               tensor cores over tiled A, the missed chunks' keys are rebuilt
+                               inside the attention's launch: its first CTAs rebuild them
+                               (Algorithm 2 step 3, key branch) into the cache slots before
+                               they take attention items, and each missed chunk's item waits
+                               for its own keys and values.  Three launches per step instead
+                               of four.  0 (default): a rebuild launch of its own */
 };
 skv_status shadowkv_set_option(shadowkv_ctx* ctx, int option, long long value);
 
@@ -228,6 +236,9 @@ typedef struct shadowkv_layout {
   int fetch_in_attention; /* value fetch runs as warps of the tensor-core attention's
                            launch; each missed chunk is attended as soon as its
                            values are in its cache slot */
+  int rebuild_in_attention; /* SKV_OPT_REBUILD_IN_ATTENTION is on and applies: the missed
+                           chunks' keys are rebuilt by the first CTAs of the attention's
+                           launch (three launches per step) */
 } shadowkv_layout;
 skv_status shadowkv_get_layout(const shadowkv_ctx* ctx, shadowkv_layout* out);
 

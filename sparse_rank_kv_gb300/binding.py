@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libshadowkv.so")
 
 DTYPE_F32, DTYPE_BF16 = 0, 1
 GROUP_MAX, GROUP_SUM = 0, 1
-OPT_CACHE, OPT_TIMING, OPT_SPLIT_TOKENS, OPT_CUDA_CORES = 0, 1, 2, 3
+OPT_CACHE, OPT_TIMING, OPT_SPLIT_TOKENS, OPT_CUDA_CORES, OPT_REBUILD_IN_ATTENTION = 0, 1, 2, 3, 4
 
 FIELDS = {
     "A": 0, "BT": 1, "L": 2, "MIN_COS": 3, "OUTLIER_IDS": 4, "K_OUT": 5, "V_OUT": 6,
@@ -59,7 +59,8 @@ class StateIn(ctypes.Structure):
 class Layout(ctypes.Structure):
     _fields_ = [("kv_records", ctypes.c_int), ("a_tiled", ctypes.c_int), ("tc_score", ctypes.c_int),
                 ("tc_rebuild", ctypes.c_int), ("tc_attention", ctypes.c_int),
-                ("fetch_in_rebuild", ctypes.c_int), ("fetch_in_attention", ctypes.c_int)]
+                ("fetch_in_rebuild", ctypes.c_int), ("fetch_in_attention", ctypes.c_int),
+                ("rebuild_in_attention", ctypes.c_int)]
 
 
 class Stats(ctypes.Structure):

@@ -384,7 +384,7 @@ skv_status enqueue_step(skv::Ctx& c, const void* q, const void* k_new, const voi
     CK(skv::launch_fetch(c, c.side));
     CK(cudaEventRecord(c.ev_join, c.side));
   }
-  CK(skv::launch_rebuild(c, st));
+  if (!skv::attn_rebuilds(c)) CK(skv::launch_rebuild(c, st));
   if (!fused) CK(cudaStreamWaitEvent(st, c.ev_join, 0));
   CK(skv::launch_attn(c, q, out, n_loc, st));
   if (k_new) ++c.n_app;
@@ -675,6 +675,10 @@ skv_status shadowkv_set_option(shadowkv_ctx* h, int option, long long value) {
       if (value != 0 && value != 1) return fail(SKV_ERR_INVALID_ARG, "option must be 0 or 1");
       c.force_simt = value == 1;
       return SKV_OK;
+    case SKV_OPT_REBUILD_IN_ATTENTION:
+      if (value != 0 && value != 1) return fail(SKV_ERR_INVALID_ARG, "option must be 0 or 1");
+      c.rebuild_in_attn = value == 1;
+      return SKV_OK;
     default:
       return fail(SKV_ERR_INVALID_ARG, "unknown option %d", option);
   }
@@ -705,6 +709,7 @@ skv_status shadowkv_get_layout(const shadowkv_ctx* h, shadowkv_layout* out) {
   out->tc_attention = c.kv_rec && !c.force_simt && !c.split_set ? 1 : 0;
   out->fetch_in_rebuild = skv::rebuild_fetches(c) ? 1 : 0;
   out->fetch_in_attention = skv::attn_fetches(c) ? 1 : 0;
+  out->rebuild_in_attention = skv::attn_rebuilds(c) ? 1 : 0;
   return SKV_OK;
 }
 

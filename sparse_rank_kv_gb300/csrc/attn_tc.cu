@@ -40,6 +40,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
+#include "rebuild_pipe.cuh"
 
 namespace skv {
 
@@ -77,8 +78,20 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
           int loc_cap, int c, int k, int npairs, int max_splits, float scale_log2,
           const bf16* __restrict__ vcpu, const int32_t* __restrict__ miss_chunk,
           const int32_t* __restrict__ miss_slot, const int32_t* __restrict__ miss_base,
-          int32_t* __restrict__ item_done, int s, int n_chunks, int* __restrict__ status) {
+          int32_t* __restrict__ item_done, int s, int n_chunks, const bf16* __restrict__ A,
+          const __grid_constant__ CUtensorMap mapBt, const float2* __restrict__ rope_tab, int r, int h_kv,
+          int nreb, int rbS, int rbNB, int* __restrict__ status) {
   extern __shared__ unsigned char smem_raw[];
+  if (static_cast<int>(blockIdx.x) < nreb) {
+    // the first nreb CTAs first rebuild the missed chunks' keys, every
+    // nreb-th tile from their own, each tile counted on its phase-1 item (a
+    // tile is that item's 128 rows); then they take attention items like
+    // the others, so every CTA a phase-1 item waits for is resident (one
+    // CTA per SM)
+    rebuild_pipe_body<kAtD, true, 8>(smem_raw, static_cast<int>(blockIdx.x), nreb, true, item_done, A, mapBt,
+                                     mapBt, nullptr, rope_tab, miss_chunk, miss_slot, miss_base, hits_in,
+                                     KV_slot, n_chunks, npairs, h_kv, s, r, c, k, rbS, rbNB, 0, status);
+  }
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   unsigned char* stages = smem;                           // [kAtStages][records | q]
@@ -130,6 +143,9 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
     // the next step's counters start at zero
     if (blockIdx.x == 0) ctr_next[0] = ctr_next[1] = ctr_next[2] = ctr_next[3] = 0;
   }
+  // with the rebuild in this launch (launched right behind the selection),
+  // the selection's results are read only after its grid has completed
+  if (nreb > 0) tc::grid_dep_wait();
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, 64);
     tc::tmem_relinquish();
@@ -288,11 +304,13 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
         __syncwarp();
       }
       if (t.seg == 3 && vcpu != nullptr) {
-        // the item's values come from this launch's fetch warps: wait for
-        // all of its groups, then zero the count for the next step
+        // the item's values come from this launch's fetch warps (and, with
+        // the rebuild in this launch, its keys from a rebuild CTA): wait for
+        // all of its groups (and its tile), then zero the count for the next
+        // step
         bool got = true;
         if (lane == 0) {
-          got = tc::wait_count(item_done + x, groups, kWaitLimit, s_abort);
+          got = tc::wait_count(item_done + x, groups + (nreb > 0 ? 1 : 0), kWaitLimit, s_abort);
           if (got) {
             item_done[x] = 0;
             tc::fence_proxy_async_global();
@@ -764,6 +782,8 @@ static cudaError_t attn_tc_t(Ctx& c, const CUtensorMap& mq, void* out, int n_loc
   // launched behind the key rebuild: phase 0 overlaps it and this launch's
   // own value fetch
   const bool fetch = attn_fetches(c);
+  int rbS = 0, rbNB = 0;
+  const int nreb = attn_rebuilds(c, &rbS, &rbNB) ? std::min(kRebuildSMsRec, c.nsm / 4) : 0;
   return launch_pdl(kern, dim3(c.nsm), dim3(kAtThreads), static_cast<size_t>(smem), st, mq,
                     static_cast<const bf16*>(c.KV_out), static_cast<bf16*>(c.KV_slot),
                     static_cast<const int32_t*>(c.att_slot), static_cast<const int32_t*>(c.hits),
@@ -772,11 +792,29 @@ static cudaError_t attn_tc_t(Ctx& c, const CUtensorMap& mq, void* out, int n_loc
                     c.p.k, npairs, c.max_splits, scale_log2,
                     static_cast<const bf16*>(fetch ? c.v_cpu_dev : nullptr),
                     static_cast<const int32_t*>(c.miss_chunk), static_cast<const int32_t*>(c.miss_slot),
-                    static_cast<const int32_t*>(c.miss_base), c.item_done, c.p.s, c.n, c.status);
+                    static_cast<const int32_t*>(c.miss_base), c.item_done, c.p.s, c.n,
+                    static_cast<const bf16*>(c.A), c.mapBt, static_cast<const float2*>(c.rope_tab), c.p.r,
+                    c.p.h_kv, nreb, rbS, rbNB, c.status);
 }
 
 bool attn_fetches(const Ctx& c) {
   return c.kv_rec && !c.force_simt && !c.split_set && c.v_cpu_dev != nullptr && c.item_done != nullptr;
+}
+
+bool attn_rebuilds(const Ctx& c, int* S, int* NB) {
+  if (!c.rebuild_in_attn || !attn_fetches(c) || !c.tc_rebuild || !c.a_tiled || c.p.d != kAtD) return false;
+  // the rebuild's pipeline (A stages, B slots, the head tables) in the
+  // attention's shared memory
+  const int npairs = c.p.b * c.p.h_kv;
+  const int room = at_smem_bytes(npairs) - (3 * npairs + 1) * 4;
+  const int cand[4][2] = {{2, 2}, {2, 1}, {1, 2}, {1, 1}};
+  for (auto& x : cand)
+    if (pipe_smem(c.p.r, kAtD, x[0], x[1], 0) <= room) {
+      if (S) *S = x[0];
+      if (NB) *NB = x[1];
+      return true;
+    }
+  return false;
 }
 
 cudaError_t launch_attn_tc(Ctx& c, const void* q, void* out, int n_loc, cudaStream_t st) {

@@ -121,6 +121,7 @@ struct Ctx {
   CUtensorMap mapL{};           // landmarks (b*h_kv*n x d) for the tensor-core score kernel
   bool tc_rebuild = false;      // shapes and dtype allow the tcgen05 rebuild
   bool tc_score = false;        // ... and the tcgen05 landmark scores
+  bool rebuild_in_attn = false; // the attention's launch also rebuilds the missed keys
   bool force_simt = false;      // test hook: use the CUDA-core kernels anyway
   bool attn_pipe = false;       // bf16 shapes the pipelined attention handles
   CUtensorMap mapKo{}, mapKs{}, mapKl{};   // K_out, K_sparse, K_loc (64-row boxes)
@@ -207,6 +208,10 @@ cudaError_t launch_attn_tc(Ctx& c, const void* q, void* out, int n_loc, cudaStre
 // true when the tensor-core attention moves the step's value misses itself
 // (warps of its own launch): no separate fetch launch then
 bool attn_fetches(const Ctx& c);
+// true when the tensor-core attention's launch also rebuilds the missed
+// chunks' keys (its first CTAs): no separate rebuild launch then; *S, *NB
+// get the rebuild pipeline's A stages and B slots
+bool attn_rebuilds(const Ctx& c, int* S = nullptr, int* NB = nullptr);
 cudaError_t encode_q_map(const Ctx& c, const void* q, CUtensorMap* map);
 // the query map for buffer q: the context's cached one, encoded when q differs
 cudaError_t q_map_for(Ctx& c, const void* q, CUtensorMap* map);

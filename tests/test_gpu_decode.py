@@ -34,9 +34,10 @@ SMALL = CONFIGS["llama_b1_s32k"].with_(
 
 
 def run_parity(cfg, steps=None, group="max", cache=True, bsel=None, rows=True, append=True,
-               v_on_host=False, split=None, st=None, sels=None):
+               v_on_host=False, split=None, st=None, sels=None, opts=None):
     """Decode `steps` steps of `cfg` (state `st`, else a random one) and check
-    each against the oracle; the selections are appended to `sels` if given."""
+    each against the oracle; the selections are appended to `sels` if given;
+    `opts` maps context options to values."""
     if st is None:
         st = synth.make_state(cfg, device="cuda")
     if v_on_host:
@@ -47,6 +48,8 @@ def run_parity(cfg, steps=None, group="max", cache=True, bsel=None, rows=True, a
         ctx.set_option(binding.OPT_CACHE, 0)
     if split:
         ctx.set_option(binding.OPT_SPLIT_TOKENS, split)
+    for o, v in (opts or {}).items():
+        ctx.set_option(o, v)
     sl = slice(None) if bsel is None else slice(bsel, bsel + 1)
     dec = O.OracleDecoder(oracle_state(st, cfg, bsel), h_q=cfg.h_q, k=cfg.k, group_reduce=group,
                           key_dtype=cfg.dtype)
@@ -165,7 +168,8 @@ def test_values_from_host_memory():
     run_parity(SMALL.with_(seed=38), steps=3, v_on_host=True)
 
 
-def test_cache_is_lossless():
+@pytest.mark.parametrize("in_attn", [0, 1], ids=["rebuild_launch", "rebuild_in_attention"])
+def test_cache_is_lossless(in_attn):
     """The set-difference cache changes only what crosses the host link.  With
     the cache on and forced off every step attends bit-identical data: the
     same chunks, the same rebuilt keys and the same values for them.  The
@@ -178,6 +182,9 @@ def test_cache_is_lossless():
     b, h, hq, d, k, c = cfg.b, cfg.h_kv, cfg.h_q, cfg.d, cfg.k, cfg.c
     ctxs = [binding.load_state(binding.make_params(cfg), st) for _ in range(2)]
     ctxs[1].set_option(binding.OPT_CACHE, 0)
+    for ctx in ctxs:
+        ctx.set_option(binding.OPT_REBUILD_IN_ATTENTION, in_attn)
+        assert ctx.layout()["rebuild_in_attention"] == in_attn
     dt = synth.torch_dtype(cfg.dtype)
 
     def attended(ctx):
@@ -222,6 +229,29 @@ def test_full_size_sampled_sequence(name, bsel, steps):
     """The full-size workloads in the benchmark's launch configuration; the
     oracle recomputes one sequence of the batch."""
     run_parity(CONFIGS[name], steps=steps, bsel=bsel, rows=False)
+
+
+@pytest.mark.parametrize("cfg", [
+    SMALL.with_(seed=50),
+    SMALL.with_(r=48, seed=51),                       # last K block half out of range
+    SMALL.with_(c=16, k=20, seed=52),                 # 16-row chunks: 8 per item
+    SMALL.with_(b=6, h_kv=8, h_q=32, k=64, seed=53),  # 48 heads: more tiles than rebuild CTAs
+], ids=["r64", "r48", "c16", "h48"])
+def test_rebuild_inside_the_attention_launch(cfg):
+    """SKV_OPT_REBUILD_IN_ATTENTION: the first CTAs of the attention's launch
+    rebuild the missed chunks' keys into their cache slots, then take
+    attention items; each missed chunk's item waits for its own keys and
+    values.  Selections, hits, rebuilt keys and outputs against the oracle on
+    every step."""
+    _, ctx, _, _ = run_parity(cfg, opts={binding.OPT_REBUILD_IN_ATTENTION: 1})
+    assert ctx.layout()["rebuild_in_attention"] == 1
+
+
+def test_rebuild_inside_the_attention_launch_full_size():
+    """The same at batch 8, 128K (the oracle recomputes one sequence)."""
+    _, ctx, _, _ = run_parity(CONFIGS["llama_b8_s128k"], steps=4, bsel=2, rows=False,
+                              opts={binding.OPT_REBUILD_IN_ATTENTION: 1})
+    assert ctx.layout()["rebuild_in_attention"] == 1
 
 
 def test_max_new_is_enforced():
