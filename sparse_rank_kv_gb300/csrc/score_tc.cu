@@ -110,6 +110,10 @@ k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUt
     // requested one ahead, so the atomic's round trip overlaps a stage.
     int next = -1;
     if (lane == 0 && per_cta == 0) next = tail0 + atomicAdd(tail, 1);
+    // the landmarks are read once per step: evicted from L2 first, so that
+    // the logits, partials and maxima this kernel writes stay there for the
+    // selection
+    const uint64_t evict_first = tc::l2_evict_first_policy();
     for (int i = 0;; ++i) {
       const int s = i % kScStages;
       const uint32_t ph = (i / kScStages) & 1;
@@ -144,7 +148,8 @@ k_score_tc(const __grid_constant__ CUtensorMap mapL, const __grid_constant__ CUt
       const int pair = tile / ntile, ti = tile - pair * ntile;
       unsigned char* st = stages + s * STAGE;
       if (lane < KA)
-        tc::tma_load_2d(st + lane * (kScTile * 128), &mapL, &full[s], lane * 64, pair * n + ti * kScTile);
+        tc::tma_load_2d_hint(st + lane * (kScTile * 128), &mapL, &full[s], lane * 64, pair * n + ti * kScTile,
+                             evict_first);
       else if (lane < 2 * KA)
         tc::tma_load_3d(st + A_BYTES + (lane - KA) * (16 * 128), &mapQ, &full[s], (lane - KA) * 64, 0, pair);
     }
