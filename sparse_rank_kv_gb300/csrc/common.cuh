@@ -444,11 +444,15 @@ __device__ __forceinline__ void block_kth(const uint32_t* v, int cnt, int kth, i
 // reading them.  scratch holds kKth8Ints ints.  With max_passes < 4 the
 // select may stop before the last digit: scratch[kKth8T] is then the lower
 // edge of the digit range that holds the k-th largest (a lower bound of it)
-// and scratch[kKth8Need] is not meaningful.
-constexpr int kKth8T = 8 * 256 + 256 + 4, kKth8Need = kKth8T + 1, kKth8Ints = 8 * 256 + 256 + 8;
+// and scratch[kKth8Need] is not meaningful.  After a complete select
+// scratch[kKth8Eq] is the number of values equal to the k-th largest.  A
+// caller that knows a range [rlo, rhi] (rhi != 0) holding every non-zero
+// value passes it, and the select skips its min/max reduction.
+constexpr int kKth8T = 8 * 256 + 256 + 4, kKth8Need = kKth8T + 1, kKth8Eq = kKth8T + 2,
+              kKth8Ints = 8 * 256 + 256 + 8;
 template <int V = 4>
 __device__ __forceinline__ void block_kth_256(const uint32_t* v, int cnt, int kth, int* scratch,
-                                              int max_passes = 4) {
+                                              int max_passes = 4, uint32_t rlo = 0u, uint32_t rhi = 0u) {
   const int tid = threadIdx.x;
   if (tid >= 256) return;
   const int lane = tid & 31, warp = tid >> 5;
@@ -464,6 +468,7 @@ __device__ __forceinline__ void block_kth_256(const uint32_t* v, int cnt, int kt
     x[q] = i < cnt ? v[i] : 0u;
     if (x[q]) { lo = min(lo, x[q]); hi = max(hi, x[q]); }
   }
+  if (rhi == 0u) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
@@ -482,8 +487,9 @@ __device__ __forceinline__ void block_kth_256(const uint32_t* v, int cnt, int kt
     if (tid == 0) { bc[2] = static_cast<int>(m); bc[3] = static_cast<int>(M); }
   }
   bar();
-  const uint32_t vmin = static_cast<uint32_t>(bc[2]);
-  const uint32_t span = static_cast<uint32_t>(bc[3]) - vmin;
+  }
+  const uint32_t vmin = rhi != 0u ? rlo : static_cast<uint32_t>(bc[2]);
+  const uint32_t span = (rhi != 0u ? rhi : static_cast<uint32_t>(bc[3])) - vmin;
   int hb = span ? 32 - __clz(span) : 1;
   uint32_t prefix = 0, pmask = 0;
   int need = kth;
@@ -521,14 +527,19 @@ __device__ __forceinline__ void block_kth_256(const uint32_t* v, int cnt, int kt
       const unsigned hit = __ballot_sync(0xffffffffu, incl >= need);
       const int first = __ffs(hit) - 1;
       if (lane == first) {
-        int acc = incl - sum, digit = 255 - 8 * lane;
+        int acc = incl - sum, digit = 255 - 8 * lane, in_digit = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          if (acc + cnt8[i] >= need) { digit = 255 - 8 * lane - i; break; }
+          if (acc + cnt8[i] >= need) {
+            digit = 255 - 8 * lane - i;
+            in_digit = cnt8[i];
+            break;
+          }
           acc += cnt8[i];
         }
         bc[0] = digit;
         bc[1] = need - acc;
+        bc[6] = in_digit;   // after the last digit: the values equal to the result
       }
     }
     bar();

@@ -124,9 +124,32 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
   // this head's cache slots (written by the previous step's selection)
   int32_t* sc_row = slot_chunk + static_cast<size_t>(pair) * k;
   const int my_slot_chunk = cache_on && tid < k ? sc_row[tid] : -1;
-  tc::grid_dep_wait();   // the logits and partials of the score kernel
   const int n8 = (n + 7) >> 3;
   const bool bounded = m8 != nullptr && group_reduce == 0 && 2 * n8 <= n && n8 <= 4 * nthr;
+  // the bounded path's shared state (below); its counters and the bitmap of
+  // the selection are set before the wait
+  const int cap = 4 * nthr;
+  uint32_t* bkey = keys;                                   // [n8] group bounds (0: no valid chunk)
+  int* cand = reinterpret_cast<int*>(keys + n8);           // [n8] candidate groups
+  uint32_t* vals = reinterpret_cast<uint32_t*>(scratch);  // survivors' keys
+  int* vidx = scratch + cap;                               // their chunks
+  int* ks = vidx + cap;                                    // block_kth scratch
+  int* stmp = ks + (nthr / 32) * 256 + 256 + 8;            // scans; then +33..+39 below
+  unsigned* bmax_slot = reinterpret_cast<unsigned*>(stmp + 33);   // largest non-zero bound
+  unsigned* bmin_slot = reinterpret_cast<unsigned*>(stmp + 34);   // smallest non-zero bound
+  unsigned* smax_slot = reinterpret_cast<unsigned*>(stmp + 35);   // largest survivor key
+  int* cnt_slot = stmp + 36;
+  int* nnz_slot = stmp + 38;
+  int* ncand_slot = stmp + 39;
+  if (bounded) {
+    if (tid == 0) {
+      *cnt_slot = *nnz_slot = *ncand_slot = 0;
+      *bmax_slot = *smax_slot = 0u;
+      *bmin_slot = 0xffffffffu;
+    }
+    for (int w = tid; w < nw; w += nthr) words[w] = 0u;
+  }
+  tc::grid_dep_wait();   // the logits and partials of the score kernel
   // with at most 2 groups per thread, their maxima are loaded before the
   // log-sum-exp, so that the two round trips overlap
   const bool pre = bounded && n8 <= 2 * nthr;
@@ -141,19 +164,32 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
     }
   }
   // log-sum-exp of each query head over the candidate chunks (4 partials
-  // of 32 landmarks per 128-landmark score tile): a warp per head
+  // of 32 landmarks per 128-landmark score tile): a warp per head, one pass
+  // (each lane's partials in rounds of 8 loads, merged as (max, sum))
   for (int g = warp; g < G; g += nthr / 32) {
     const float2* pp = part + (static_cast<size_t>(pair) * G + g) * ntile * 4;
-    float m = -INFINITY;
-    for (int t = lane; t < 4 * ntile; t += 32) m = fmaxf(m, pp[t].x);
-    m = warp_max(m);
-    float z = 0.f;
-    for (int t = lane; t < 4 * ntile; t += 32) {
-      const float2 v = pp[t];
-      if (v.y > 0.f) z += v.y * __expf(v.x - m);
+    const int lim = 4 * ntile;
+    float m = -INFINITY, z = 0.f;
+    for (int t0 = 0; t0 < lim; t0 += 32 * 8) {
+      float2 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int t = t0 + u * 32 + lane;
+        v[u] = t < lim ? __ldcg(pp + t) : make_float2(-INFINITY, 0.f);
+      }
+      float mc = m;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mc = fmaxf(mc, v[u].x);
+      float zc = z > 0.f ? z * __expf(m - mc) : 0.f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (v[u].y > 0.f) zc += v[u].y * __expf(v[u].x - mc);
+      m = mc;
+      z = zc;
     }
-    z = warp_sum(z);
-    if (lane == 0) lse[g] = m + __logf(z);
+    const float M = warp_max(m);
+    z = warp_sum(z > 0.f ? z * __expf(m - M) : 0.f);
+    if (lane == 0) lse[g] = M + __logf(z);
   }
   __syncthreads();
   const uint32_t* mk = mask + static_cast<size_t>(pair) * nw;
@@ -167,24 +203,16 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
   // candidates (massive ties) take the general path below.
   bool topk_done = false;
   if (bounded) {
-    const int cap = 4 * nthr;
-    uint32_t* bkey = keys;                                   // [n8] group bounds (0: no valid chunk)
-    int* cand = reinterpret_cast<int*>(keys + n8);           // [n8] candidate groups
-    uint32_t* vals = reinterpret_cast<uint32_t*>(scratch);  // survivors' keys
-    int* vidx = scratch + cap;                               // their chunks
-    int* ks = vidx + cap;                                    // block_kth scratch
-    int* stmp = ks + (nthr / 32) * 256 + 256 + 8;            // scans, then counters at +36..+39
-    int* cnt_slot = stmp + 36;
-    int* eq_slot = stmp + 37;
-    int* nnz_slot = stmp + 38;
-    int* ncand_slot = stmp + 39;
-    if (tid == 0) *cnt_slot = *eq_slot = *nnz_slot = *ncand_slot = 0;
-    __syncthreads();
     int nz = 0;
+    uint32_t kmax = 0u, kmin = 0xffffffffu;
     auto put_bound = [&](int w, float bnd) {
       const uint32_t kb = bnd == -INFINITY ? 0u : order_key(bnd);
       bkey[w] = kb;
-      nz += kb != 0u;
+      if (kb != 0u) {
+        ++nz;
+        kmax = max(kmax, kb);
+        kmin = min(kmin, kb);
+      }
     };
     if (pre) {
 #pragma unroll
@@ -206,14 +234,21 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
       }
     }
     nz = __reduce_add_sync(0xffffffffu, nz);
-    if (lane == 0 && nz) atomicAdd(nnz_slot, nz);
+    kmax = __reduce_max_sync(0xffffffffu, kmax);
+    kmin = __reduce_min_sync(0xffffffffu, kmin);
+    if (lane == 0 && nz) {
+      atomicAdd(nnz_slot, nz);
+      atomicMax(bmax_slot, kmax);
+      atomicMin(bmin_slot, kmin);
+    }
     __syncthreads();
     uint32_t B = 1u;    // fewer than k groups with a valid chunk: all of them are candidates
     if (*nnz_slot >= k) {
       // two 8-bit digits: B is the lower edge of the range that holds the
-      // k-th largest bound, still a lower bound of the k-th largest S2
-      if (n8 <= 2048) block_kth_256<8>(bkey, n8, k, ks, 2);
-      else block_kth_256<16>(bkey, n8, k, ks, 2);
+      // k-th largest bound, still a lower bound of the k-th largest S2 (the
+      // bounds' range is known)
+      if (n8 <= 2048) block_kth_256<8>(bkey, n8, k, ks, 2, *bmin_slot, *bmax_slot);
+      else block_kth_256<16>(bkey, n8, k, ks, 2, *bmin_slot, *bmax_slot);
       __syncthreads();
       B = static_cast<uint32_t>(ks[kKth8T]);
     }
@@ -233,6 +268,7 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
       // the candidates' chunks, in rounds of 4 per thread: all loads of a
       // round issued before any key is formed; survivors appended by warp
       // ballots (at most cap of them are kept)
+      uint32_t kept_max = 0u;
       for (int h0 = 0; h0 < ne; h0 += 4 * nthr) {
       float pv[4][G];
       int jj[4];
@@ -263,6 +299,7 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
           key = order_key(sm);
         }
         const bool keep = key != 0u && key >= B;
+        if (keep) kept_max = max(kept_max, key);
         const unsigned m = __ballot_sync(0xffffffffu, keep);
         int base = 0;
         if (lane == 0 && m) base = atomicAdd(cnt_slot, __popc(m));
@@ -274,26 +311,22 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
         }
       }
       }
+      kept_max = __reduce_max_sync(0xffffffffu, kept_max);
+      if (lane == 0 && kept_max) atomicMax(smax_slot, kept_max);
       __syncthreads();
       const int nsurv = *cnt_slot;
       if (nsurv >= k && nsurv <= cap) {
-        // Tk = the k-th largest survivor; `need` of the survivors equal to
-        // Tk are taken (every chunk equal to Tk is a survivor)
-        uint32_t Tk;
-        int need;
-        if (nsurv <= 1024) block_kth_256<4>(vals, nsurv, k, ks);
-        else if (nsurv <= 2048) block_kth_256<8>(vals, nsurv, k, ks);
-        else block_kth_256<16>(vals, nsurv, k, ks);
+        // Tk = the k-th largest survivor (all survivors lie in [B, their
+        // largest key]); `need` of the survivors equal to Tk are taken
+        // (every chunk equal to Tk is a survivor)
+        const uint32_t shi = *smax_slot;
+        if (nsurv <= 1024) block_kth_256<4>(vals, nsurv, k, ks, 4, B, shi);
+        else if (nsurv <= 2048) block_kth_256<8>(vals, nsurv, k, ks, 4, B, shi);
+        else block_kth_256<16>(vals, nsurv, k, ks, 4, B, shi);
         __syncthreads();
-        Tk = static_cast<uint32_t>(ks[kKth8T]);
-        need = ks[kKth8Need];
-        for (int w = tid; w < nw; w += nthr) words[w] = 0u;
-        int eq = 0;
-        for (int i = tid; i < nsurv; i += nthr) eq += vals[i] == Tk;
-        eq = __reduce_add_sync(0xffffffffu, eq);
-        if (lane == 0 && eq) atomicAdd(eq_slot, eq);
-        __syncthreads();
-        if (*eq_slot == need) {
+        const uint32_t Tk = static_cast<uint32_t>(ks[kKth8T]);
+        const int need = ks[kKth8Need];
+        if (ks[kKth8Eq] == need) {
           for (int i = tid; i < nsurv; i += nthr)
             if (vals[i] >= Tk) atomicOr(&words[vidx[i] >> 5], 1u << (vidx[i] & 31));
         } else {
