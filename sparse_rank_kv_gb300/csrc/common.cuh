@@ -131,7 +131,9 @@ __device__ __forceinline__ float warp_max(float v) {
 // Block-wide exclusive scan of one int per thread.  `tmp` holds >= 33 ints of
 // shared memory.  Returns the exclusive prefix; *total gets the block sum.
 // Every thread of the block must call it.
-__device__ __forceinline__ int block_exclusive_scan(int v, int* tmp, int* total) {
+// With last_use, tmp is not written again before the block's next barrier,
+// and the scan skips its closing barrier.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* tmp, int* total, bool last_use = false) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nwarps = (blockDim.x + 31) >> 5;
   int x = v;
@@ -155,7 +157,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* tmp, int* total)
   __syncthreads();
   const int excl = (warp ? tmp[warp - 1] : 0) + x - v;
   *total = tmp[32];
-  __syncthreads();
+  if (!last_use) __syncthreads();
   return excl;
 }
 

@@ -445,7 +445,7 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
   const int is_free = tid < k ? !s_keep[tid] : 0;
   // both ranks from one scan (counts < 2^16)
   int both;
-  const int ranks = block_exclusive_scan(is_miss | (is_free << 16), tmp, &both);
+  const int ranks = block_exclusive_scan(is_miss | (is_free << 16), tmp, &both, true);
   const int mrank = ranks & 0xffff, frank = ranks >> 16;
   const int nmiss = both & 0xffff, nfree = both >> 16;
   if (is_free) s_free[frank] = tid;
@@ -453,14 +453,14 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
   // after the hits before it), then misses
   if (att_slot != nullptr && tid < k && !is_miss)
     att_slot[static_cast<size_t>(pair) * k + tid - mrank] = s_slot[tid];
-  __syncthreads();
-  if (nmiss != nfree || nmiss != nres) flag_error(status, DEV_BAD_COUNT);
+  // the reserved range's start (the atomic issued before the scan)
   __shared__ int s_base;
   if (tid == 0) {
     s_base = base_r;
     miss_base[pair] = base_r;
   }
   __syncthreads();
+  if (nmiss != nfree || nmiss != nres) flag_error(status, DEV_BAD_COUNT);
   // (k <= blockDim.x: thread i writes selection entry i, its slot included)
   if (tid < k) {
     int slot = s_slot[tid];
