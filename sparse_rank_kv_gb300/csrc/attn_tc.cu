@@ -28,7 +28,10 @@
 //                reductions, p = 2^(s - m),
 //                bf16 P^T into shared memory, head sums), for O the dimension:
 //                the item's partial (max, sum, sum p v) per query head goes to
-//                the item's slot, and a ticket per head counts finished items.
+//                the item's slot, and a ticket per head counts finished items
+//                (phase-1 items in its upper 16 bits).  Once the producer
+//                takes missed chunks, a group publishes each phase-0 item as
+//                soon as it is done rather than with later items.
 //   warps 10..13: the step's value fetch (Algorithm 2 step 3, V from the host):
 //                8-token groups of the missed chunks, taken from a fourth
 //                counter in phase-1 item order, read from pinned host memory
@@ -36,7 +39,9 @@
 //                chunk's cache-slot record; a count per phase-1 item tells
 //                the producer when all of the item's groups are in place.
 // When both counters are exhausted a CTA takes heads from a third counter and
-// merges each head's item partials once its ticket shows all of them done.
+// merges each head's item partials: the phase-0 ones as soon as its ticket
+// shows all of them, then the phase-1 ones, so that after the last missed
+// chunk only its few partials remain to be read.
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
@@ -107,6 +112,8 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 192);
   volatile int* s_abort = reinterpret_cast<volatile int*>(misc + 196);
   volatile int* s_end = reinterpret_cast<volatile int*>(misc + 200);    // items of this CTA, once known
+  volatile int* s_phase1 = reinterpret_cast<volatile int*>(misc + 212); // the producer takes missed chunks
+  int* s_dec_g[2] = {reinterpret_cast<int*>(misc + 216), reinterpret_cast<int*>(misc + 220)};
   // per softmax group: its current merge head, its count and list of
   // finished items whose tickets are not yet counted
   int* s_task_g[2] = {reinterpret_cast<int*>(misc + 204), reinterpret_cast<int*>(misc + 1216)};
@@ -139,6 +146,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
     tc::fence_mbar_init();
     *s_abort = 0;
     *s_end = -1;
+    *s_phase1 = 0;
     *s_ndone_g[0] = *s_ndone_g[1] = 0;
     // the next step's counters start at zero
     if (blockIdx.x == 0) ctr_next[0] = ctr_next[1] = ctr_next[2] = ctr_next[3] = 0;
@@ -262,7 +270,10 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
         // (the number requested ahead is past T0 as well)
         phase = 1;
         tc::grid_dep_wait();
-        if (lane == 0) x = atomicAdd(&ctr[1], 1);
+        if (lane == 0) {
+          *s_phase1 = 1;
+          x = atomicAdd(&ctr[1], 1);
+        }
         x = __shfl_sync(0xffffffffu, x, 0);
       }
       const int st = it % kAtStages, use = it / kAtStages;
@@ -439,6 +450,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
     int* s_done = s_done_g[gs];
     int* s_ndone = s_ndone_g[gs];
     int* s_task = s_task_g[gs];
+    int* s_dec = s_dec_g[gs];
     const int ct = tid - 64 - 128 * gs, quarter = warp & 3;
     const int row = quarter * 32 + lane;          // TMEM lane: token row for S, dimension for O
     const uint32_t tlane = static_cast<uint32_t>(quarter * 32) << 16;
@@ -454,7 +466,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
     };
     bool dead = false;
     // the pending item: its O buffer holds sum p v once ofull completes
-    int pj = -1, ppair = 0, pli = 0;
+    int pj = -1, ppair = 0, pli = 0, pseg = 0;
     float pm[G], pl[G];
     auto finish = [&]() {
       if (!dead) {
@@ -481,21 +493,51 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
           pp[kAtD + 1] = pl[g];
         }
       }
-      // the head's ticket counts the item once its partial is visible; the
-      // counts are published together (one fence) when the CTA's items end
-      if (ct == 0) s_done[(*s_ndone)++] = ppair;
+      // the head's ticket counts the item once its partial is visible (a
+      // phase-1 item in the upper 16 bits); the counts are published
+      // together, after one fence
+      if (ct == 0) s_done[(*s_ndone)++] = ppair | (pseg == 3 ? (1 << 30) : 0);
     };
     auto publish = [&]() {
       tc::named_sync(bar, kAtSoft);
       if (ct == 0 && *s_ndone > 0) {
         tc::fence_acq_rel_gpu();
-        for (int i = 0; i < *s_ndone; ++i) atomicAdd(&ticket[s_done[i]], 1);
+        for (int i = 0; i < *s_ndone; ++i)
+          atomicAdd(&ticket[s_done[i] & 0x3fffffff], (s_done[i] >> 30) ? (1 << 16) : 1);
         *s_ndone = 0;
       }
       tc::named_sync(bar, kAtSoft);
     };
     for (int it = gs;; it += kAtSoftGroups) {
       const int sb = it & 1, st = it % kAtStages;
+      // once the producer takes missed chunks (whose items wait for the
+      // host link), the phase-0 item this group holds is finished and
+      // published while the group waits for its next item, so that the
+      // heads' merges can fold their phase-0 partials in early (one
+      // decision for the group)
+      if (pj >= 0 && !dead) {
+        if (ct == 0) {
+          // the next item's S or the producer's move to the missed chunks,
+          // whichever comes first (a missed wait is reported below)
+          int d = 0;
+          const uint64_t t0 = tc::globaltimer_ns();
+          while (!tc::mbar_test(&sfull[sb], (it >> 1) & 1)) {
+            if (*s_phase1) {
+              d = 1;
+              break;
+            }
+            if (*s_abort || tc::globaltimer_ns() - t0 > kWaitLimit) break;
+            __nanosleep(64);   // leaves the SM's issue slots to the copy, MMA and fetch warps
+          }
+          *s_dec = d;
+        }
+        tc::named_sync(bar, kAtSoft);
+        if (*s_dec) {
+          finish();
+          pj = -1;
+          publish();
+        }
+      }
       if (!dead) {
         bool ok = !*s_abort && tc::mbar_wait(&sfull[sb], (it >> 1) & 1, kWaitLimit);
         ok = __all_sync(0xffffffffu, ok);
@@ -550,6 +592,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
       pj = it;
       ppair = pair;
       pli = li;
+      pseg = seg;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         pm[g] = mi[g];
@@ -570,76 +613,115 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
     if (!dead) publish();
 
     // ------------------------------------------------------------ combine
-    // heads from the third counter; each waits for its ticket to show all of
-    // its items' partials, then merges them (weights 2^(m - M) / sum)
-    // [G][wcap] maxima, turned into weights, then [G][wcap] sums (P^T is no
-    // longer used)
+    // heads from the third counter.  A head's ticket counts its published
+    // phase-0 items (outliers, local window, cache hits) in the low 16 bits
+    // and its phase-1 items (missed chunks) above them.  The phase-0
+    // partials are folded in once all of them are published, the phase-1
+    // partials once those are (all in one stage when the whole count is
+    // there at the first look): per query head a running max M, sum of
+    // 2^(m - M) l and, per output row, sum of 2^(m - M) pv, divided at the
+    // end.  Scratch: [G][wcap] maxima, turned into 2^(m - M), then [G][wcap]
+    // sums (P^T is no longer used); the group's reduction scratch holds M,
+    // the sum and the factor that rescales the earlier terms, per head.
     float* w = reinterpret_cast<float*>(pbuf + gs * kAtPBytes);
     const int wcap = kAtPBytes / 8 / G;
     float* lsum = w + G * wcap;
+    float* mst = red + gs * 64;
     while (!dead) {
       if (ct == 0) *s_task = atomicAdd(&ctr[2], 1);
       tc::named_sync(bar, kAtSoft);
       const int pair = *s_task;
       tc::named_sync(bar, kAtSoft);
       if (pair >= npairs) break;
-      const int ntot = s_p0[pair + 1] - s_p0[pair] + s_p1[pair + 1] - s_p1[pair];
-      if (ct == 0) {
-        const bool ok = ntot <= wcap && tc::wait_count(ticket + pair, ntot, kWaitLimit, s_abort);
-        if (!ok) abort_now();
-      }
-      tc::named_sync(bar, kAtSoft);
-      if (*s_abort) break;
+      const int n0 = s_p0[pair + 1] - s_p0[pair], n1 = s_p1[pair + 1] - s_p1[pair];
       const size_t pb = static_cast<size_t>(pair) * G * max_splits;
       const float* pr = part + pb * (kAtD + 2) + row;
-      // R items' partial rows per round; the first round is loaded together
-      // with every item's (max, sum), before the weights are known
+      if (ct < G) {
+        mst[ct] = -INFINITY;
+        mst[G + ct] = 0.f;
+      }
+      // R items' partial rows per round; a stage's first round is loaded
+      // together with its items' (max, sum), before the weights are known
       constexpr int R = 64 / G;
-      float v[R][G];
-      auto load_round = [&](int i0) {
-#pragma unroll
-        for (int u = 0; u < R; ++u)
-#pragma unroll
-          for (int g = 0; g < G; ++g)
-            v[u][g] = i0 + u < ntot ? __ldcg(pr + (static_cast<size_t>(g) * max_splits + i0 + u) * (kAtD + 2)) : 0.f;
-      };
-      load_round(0);
-      for (int e = ct; e < G * ntot; e += kAtSoft) {
-        const int g = e / ntot, i = e - g * ntot;
-        const float* pp = part + (pb + static_cast<size_t>(g) * max_splits + i) * (kAtD + 2) + kAtD;
-        w[g * wcap + i] = __ldcg(pp);
-        lsum[g * wcap + i] = __ldcg(pp + 1);
-      }
-      tc::named_sync(bar, kAtSoft);
-      if (((warp - 2) & 3) < G) {
-        // warp g: M, the sum of 2^(m - M) l, then the weights 2^(m - M) / sum
-        for (int gg = (warp - 2) & 3; gg < G; gg += 4) {
-          float M = -INFINITY;
-          for (int i = lane; i < ntot; i += 32) M = fmaxf(M, w[gg * wcap + i]);
-          M = warp_max(M);
-          float den = 0.f;
-          for (int i = lane; i < ntot; i += 32) den += exp2f(w[gg * wcap + i] - M) * lsum[gg * wcap + i];
-          den = warp_sum(den);
-          const float inv = 1.f / den;
-          for (int i = lane; i < ntot; i += 32) w[gg * wcap + i] = exp2f(w[gg * wcap + i] - M) * inv;
-        }
-      }
-      tc::named_sync(bar, kAtSoft);
-      // sum over items of weight x partial row
-      float num[G];
+      float v[R][G], num[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) num[g] = 0.f;
-      for (int i0 = 0; i0 < ntot; i0 += R) {
-        if (i0 > 0) load_round(i0);
+      bool ok = n0 + n1 <= wcap;
+      const int full = n0 + (n1 << 16);
+      int split = n0;   // items folded in the first stage
+      for (int stage = 0; stage < 2; ++stage) {
+        if (stage == 1 && split == n0 + n1) break;
+        if (ct == 0) {
+          int seen = 0;
+          ok = ok && tc::wait_count(ticket + pair, stage ? full : n0, kWaitLimit, s_abort, stage ? -1 : 0xffff,
+                                    &seen);
+          if (!ok) abort_now();
+          if (stage == 0) *s_dec = seen == full ? n0 + n1 : n0;
+        }
+        tc::named_sync(bar, kAtSoft);
+        if (*s_abort) break;
+        if (stage == 0) split = *s_dec;
+        const int i0 = stage ? split : 0, ni = stage ? n0 + n1 - split : split;
+        if (ni == 0) continue;
+        auto load_round = [&](int j0) {
 #pragma unroll
-        for (int u = 0; u < R; ++u)
+          for (int u = 0; u < R; ++u)
 #pragma unroll
-          for (int g = 0; g < G; ++g)
-            if (i0 + u < ntot) num[g] = fmaf(w[g * wcap + i0 + u], v[u][g], num[g]);
+            for (int g = 0; g < G; ++g)
+              v[u][g] = j0 + u < ni
+                            ? __ldcg(pr + (static_cast<size_t>(g) * max_splits + i0 + j0 + u) * (kAtD + 2))
+                            : 0.f;
+        };
+        load_round(0);
+        for (int e = ct; e < G * ni; e += kAtSoft) {
+          const int g = e / ni, i = e - g * ni;
+          const float* pp = part + (pb + static_cast<size_t>(g) * max_splits + i0 + i) * (kAtD + 2) + kAtD;
+          w[g * wcap + i] = __ldcg(pp);
+          lsum[g * wcap + i] = __ldcg(pp + 1);
+        }
+        tc::named_sync(bar, kAtSoft);
+        if (((warp - 2) & 3) < G) {
+          // warp g: the new M, the factor for the earlier terms, the sum,
+          // and the stage's weights 2^(m - M)
+          for (int gg = (warp - 2) & 3; gg < G; gg += 4) {
+            float M = -INFINITY;
+            for (int i = lane; i < ni; i += 32) M = fmaxf(M, w[gg * wcap + i]);
+            const float Mo = mst[gg];
+            M = fmaxf(warp_max(M), Mo);
+            float den = 0.f;
+            for (int i = lane; i < ni; i += 32) {
+              const float e = exp2f(w[gg * wcap + i] - M);
+              den += e * lsum[gg * wcap + i];
+              w[gg * wcap + i] = e;
+            }
+            den = warp_sum(den);
+            __syncwarp();
+            if (lane == 0) {
+              const float sc = Mo == -INFINITY ? 0.f : exp2f(Mo - M);
+              mst[2 * G + gg] = sc;
+              mst[G + gg] = mst[G + gg] * sc + den;
+              mst[gg] = M;
+            }
+          }
+        }
+        tc::named_sync(bar, kAtSoft);
+#pragma unroll
+        for (int g = 0; g < G; ++g) num[g] *= mst[2 * G + g];
+        for (int j0 = 0; j0 < ni; j0 += R) {
+          if (j0 > 0) load_round(j0);
+#pragma unroll
+          for (int u = 0; u < R; ++u)
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+              if (j0 + u < ni) num[g] = fmaf(w[g * wcap + j0 + u], v[u][g], num[g]);
+        }
+        // the scratch is rewritten by the next stage
+        tc::named_sync(bar, kAtSoft);
       }
+      if (*s_abort) break;
 #pragma unroll
       for (int g = 0; g < G; ++g)
-        out[(static_cast<size_t>(pair) * G + g) * kAtD + row] = __float2bfloat16_rn(num[g]);
+        out[(static_cast<size_t>(pair) * G + g) * kAtD + row] = __float2bfloat16_rn(num[g] / mst[G + g]);
       if (ct == 0) ticket[pair] = 0;
       tc::named_sync(bar, kAtSoft);
     }

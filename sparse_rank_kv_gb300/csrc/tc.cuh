@@ -259,13 +259,19 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // Waits until the int at p reaches at least `target`, polling with relaxed
 // loads and a short sleep between them (acquire loads in a tight loop keep
 // invalidating the SM's L1 and flood the counter's L2 line), then issues one
-// acquire fence.  False once `limit_ns` has passed or *abort is set.
-__device__ __forceinline__ bool wait_count(const int* p, int target, uint64_t limit_ns, volatile int* abort) {
+// acquire fence.  False once `limit_ns` has passed or *abort is set.  With
+// a mask, the bits of *p outside it are ignored; *seen (if given) gets the
+// value that ended the wait.
+__device__ __forceinline__ bool wait_count(const int* p, int target, uint64_t limit_ns, volatile int* abort,
+                                           int mask = -1, int* seen = nullptr) {
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     int v;
     asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    if (v >= target) break;
+    if ((v & mask) >= target) {
+      if (seen) *seen = v;
+      break;
+    }
     if ((abort && *abort) || globaltimer_ns() - t0 > limit_ns) return false;
     __nanosleep(64);
   }
