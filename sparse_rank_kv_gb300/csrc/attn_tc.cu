@@ -158,11 +158,24 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
     tc::tmem_alloc(tmem_slot, 64);
     tc::tmem_relinquish();
   } else if (warp == 0) {
-    // item counts per head from its cache hits, as exclusive prefixes
+    // item counts per head from its cache hits, as exclusive prefixes (the
+    // hit counts of up to 512 heads loaded before any is used)
     int b0 = 0, b1 = 0;
+    int hv[16];
     for (int p0 = 0; p0 < npairs; p0 += 32) {
+      const int u = (p0 >> 5) & 15;
+      if (u == 0) {
+#pragma unroll
+        for (int v = 0; v < 16; ++v) {
+          const int pv = p0 + v * 32 + lane;
+          hv[v] = pv < npairs ? hits_in[pv] : 0;
+        }
+      }
       const int p = p0 + lane;
-      int h = p < npairs ? hits_in[p] : 0;
+      int h = 0;
+#pragma unroll
+      for (int v = 0; v < 16; ++v)
+        if (v == u) h = hv[v];
       if (h < 0 || h > k) {
         flag_error(status, DEV_BAD_COUNT);
         h = min(max(h, 0), k);

@@ -188,11 +188,25 @@ __device__ __forceinline__ void rebuild_pipe_body(
   if (REC) tc::grid_dep_launch();
   if constexpr (REC) {
     if (warp == 0) {
-      // exclusive prefix of the heads' tile counts, 32 heads per round
+      // exclusive prefix of the heads' tile counts, 32 heads per round (the
+      // hit counts of up to 512 heads loaded before any is used)
       int base = 0;
+      int hv[16];
       for (int p0 = 0; p0 < npairs; p0 += 32) {
+        const int u = (p0 >> 5) & 15;
+        if (u == 0) {
+#pragma unroll
+          for (int v = 0; v < 16; ++v) {
+            const int pv = p0 + v * 32 + lane;
+            hv[v] = pv < npairs ? hits[pv] : k;
+          }
+        }
+        int hp = k;
+#pragma unroll
+        for (int v = 0; v < 16; ++v)
+          if (v == u) hp = hv[v];
         const int p = p0 + lane;
-        const int mrows = p < npairs ? max(0, k - hits[p]) * c : 0;
+        const int mrows = p < npairs ? max(0, k - hp) * c : 0;
         const int nt = (mrows + kTcRows - 1) / kTcRows;
         int incl = nt;
 #pragma unroll
