@@ -538,7 +538,10 @@ def run_ours(args, cfg):
             "prefill_ms": prefill_ms[0], "prefill_kernels": prefill_kernels,
             "prefill_kernels_ms": sum(v["ms"] for v in prefill_kernels.values()),
             "e2e": {"value": job_tokens_per_s(ws, cfg.b, e2e_s * 1e3 / K / L), "unit": UNIT,
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "path": "shadowkv_decode_step_host per layer on each step's q, k_new, v_new in pinned "
+                            "host memory (a row of one pinned array per step), then a wait for the output "
+                            "in pinned host memory"},
             "gpu_launches": launches,
             "host_max_step_gap_us": host_gap[0] * 1e6,
             "clocks": clk.summary(),
