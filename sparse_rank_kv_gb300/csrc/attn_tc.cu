@@ -21,7 +21,8 @@
 //   warp 1     : tcgen05.mma.  S = K q^T (M = 128 tokens, N = 16, K = d) into
 //                one of two TMEM S buffers; after the softmax warps publish
 //                P, O = V^T P^T (M = d, N = 16, K = 16-token steps) into one
-//                of two TMEM O buffers, polling both queues.
+//                of four TMEM O buffers (two per softmax group), polling both
+//                queues.
 //   warps 2..9 : softmax, two groups of four taking alternate items (each
 //                with its own S, O and P^T buffers); thread = TMEM lane: for S
 //                the token row (scale, mask, head maxima by integer warp
@@ -56,6 +57,11 @@ constexpr int kAtFetchWarps = 4;
 constexpr int kAtSoftGroups = 2;            // softmax warpgroups, taking alternate items
 constexpr int kAtThreads = 64 + 128 * kAtSoftGroups + 32 * kAtFetchWarps;
 constexpr int kAtSoft = 128;                 // softmax threads
+// O accumulators: two per softmax group, so that an item's P V never waits
+// for the group's previous item's partial to be read out of TMEM
+constexpr int kAtOBufs = 4;
+constexpr int kAtTmemCols = 128;             // S: 2 x 16 columns, O: kAtOBufs x 16 (allocated as a power of 2)
+static_assert(32 + 16 * kAtOBufs <= kAtTmemCols, "TMEM columns");
 constexpr int kAtRec = kAtT / 8 * 4096;      // 16 group records (K tile | V^T tile)
 constexpr int kAtQBytes = 16 * kAtD * 2;     // q: 4 x [16 rows][64 B]
 constexpr int kAtStage = kAtRec + kAtQBytes;
@@ -107,8 +113,8 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
   uint64_t* sfull = empty + kAtStages;                    // [2]
   uint64_t* sempty = sfull + 2;                           // [2]
   uint64_t* pfull = sempty + 2;                           // [2]
-  uint64_t* ofull = pfull + 2;                            // [2]
-  uint64_t* oempty = ofull + 2;                           // [2]
+  uint64_t* ofull = pfull + 2;                            // [kAtOBufs]
+  uint64_t* oempty = ofull + kAtOBufs;                    // [kAtOBufs]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 192);
   volatile int* s_abort = reinterpret_cast<volatile int*>(misc + 196);
   volatile int* s_end = reinterpret_cast<volatile int*>(misc + 200);    // items of this CTA, once known
@@ -140,6 +146,8 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
       tc::mbar_init(&sfull[i], 1);
       tc::mbar_init(&sempty[i], kAtSoft / 32);
       tc::mbar_init(&pfull[i], 1);
+    }
+    for (int i = 0; i < kAtOBufs; ++i) {
       tc::mbar_init(&ofull[i], 1);
       tc::mbar_init(&oempty[i], kAtSoft / 32);
     }
@@ -155,7 +163,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
   // the selection's results are read only after its grid has completed
   if (nreb > 0) tc::grid_dep_wait();
   if (warp == 1) {
-    tc::tmem_alloc(tmem_slot, 64);
+    tc::tmem_alloc(tmem_slot, kAtTmemCols);
     tc::tmem_relinquish();
   } else if (warp == 0) {
     // item counts per head from its cache hits, as exclusive prefixes (the
@@ -422,12 +430,12 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
           }
         }
         if (no < ns && tc::mbar_test(&pfull[no & 1], (no >> 1) & 1) &&
-            tc::mbar_test(&oempty[no & 1], ((no >> 1) & 1) ^ 1)) {
-          const int st = no % kAtStages, b = no & 1;
+            tc::mbar_test(&oempty[no % kAtOBufs], ((no / kAtOBufs) & 1) ^ 1)) {
+          const int st = no % kAtStages, b = no % kAtOBufs;
           const int nks = (info[st * 6 + 1] + 15) >> 4;
           tc::fence_after();
           const uint32_t a0 = tc::smem_u32(stages + st * kAtStage + 2048);
-          const uint32_t b0 = tc::smem_u32(pbuf + b * kAtPBytes);
+          const uint32_t b0 = tc::smem_u32(pbuf + (no & 1) * kAtPBytes);   // the item's P^T buffer
           // V^T: core matrices of 8 dims x 8 tokens; dim groups 128 B apart,
           // token groups (records) 4 KB apart.  P^T: 8 heads x 8 tokens; head
           // groups 128 B apart, token groups 256 B apart.  16 tokens per MMA.
@@ -452,7 +460,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
         }
       }
       // every MMA issued has completed before TMEM is released
-      if (no > 0) tc::mbar_wait(&ofull[(no - 1) & 1], ((no - 1) >> 1) & 1, kWaitLimit);
+      if (no > 0) tc::mbar_wait(&ofull[(no - 1) % kAtOBufs], ((no - 1) / kAtOBufs) & 1, kWaitLimit);
     }
     __syncwarp();
   } else if (warp < 2 + 4 * kAtSoftGroups) {
@@ -483,7 +491,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
     float pm[G], pl[G];
     auto finish = [&]() {
       if (!dead) {
-        bool ok = !*s_abort && tc::mbar_wait(&ofull[pj & 1], (pj >> 1) & 1, kWaitLimit);
+        bool ok = !*s_abort && tc::mbar_wait(&ofull[pj % kAtOBufs], (pj / kAtOBufs) & 1, kWaitLimit);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
           if (lane == 0) abort_now();
@@ -493,10 +501,10 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
       if (dead) return;
       tc::fence_after();
       float o[8];
-      load_cols(tmem + tlane + 32 + (pj & 1) * 16, o);
+      load_cols(tmem + tlane + 32 + (pj % kAtOBufs) * 16, o);
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&oempty[pj & 1]);
+      if (lane == 0) tc::mbar_arrive(&oempty[pj % kAtOBufs]);
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         float* pp = part + ((static_cast<size_t>(ppair) * G + g) * max_splits + pli) * (kAtD + 2);
@@ -805,7 +813,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
-  if (warp == 1) tc::tmem_dealloc(tmem, 64);
+  if (warp == 1) tc::tmem_dealloc(tmem, kAtTmemCols);
 }
 
 // ---------------------------------------------------------------- host side
