@@ -76,13 +76,13 @@ struct Sizes {
   size_t A, Bt, L, K_out, V_out, K_loc, V_loc, slot_V, K_sparse, KV_out, KV_loc, KV_slot;
   size_t min_cos, logits, score_part, score_m8, attn_part, basis, rope_tab;
   size_t out_ids, out_mask, sel, sel_slot, slot_chunk, miss_chunk, miss_slot;
-  size_t miss_count, miss_base, att_slot, at_ctr, item_done, sc_ctr, hits, attn_count, counters, status;
+  size_t miss_count, miss_base, att_slot, at_ctr, item_done, sc_ctr, hits, warm_b, attn_count, counters, status;
   size_t q_stage, kv_stage, out_stage;
   size_t total() const {
     const size_t v[] = {A, Bt, L, K_out, V_out, K_loc, V_loc, slot_V, K_sparse, KV_out, KV_loc, KV_slot,
                         min_cos, logits, score_part, score_m8, attn_part, basis, rope_tab, out_ids, out_mask, sel,
                         sel_slot, slot_chunk, miss_chunk, miss_slot, miss_count, miss_base, att_slot,
-                        at_ctr, item_done, sc_ctr, hits, attn_count, counters, status, q_stage, kv_stage,
+                        at_ctr, item_done, sc_ctr, hits, warm_b, attn_count, counters, status, q_stage, kv_stage,
                         out_stage};
     size_t t = 0;
     for (size_t x : v) t += up(x);
@@ -128,7 +128,7 @@ Sizes sizes_of(const shadowkv_params& p) {
   z.out_ids = b * h * o * 4;
   z.out_mask = b * h * nw * 4;
   z.sel = z.sel_slot = z.slot_chunk = z.miss_chunk = z.miss_slot = b * h * k * 4;
-  z.hits = z.attn_count = z.miss_base = b * h * 4;
+  z.hits = z.attn_count = z.miss_base = z.warm_b = b * h * 4;
   z.att_slot = rec ? b * h * k * 4 : 0;
   z.at_ctr = rec ? 8 * 4 : 0;
   z.item_done = rec ? b * h * k * 4 : 0;   // at most k phase-1 attention items per head
@@ -299,6 +299,7 @@ skv_status create(const shadowkv_params* p, cudaStream_t st, shadowkv_ctx** out)
   c.item_done = c.kv_rec ? static_cast<int32_t*>(take(z.item_done)) : nullptr;
   c.sc_ctr = static_cast<int32_t*>(take(z.sc_ctr));
   c.hits = static_cast<int32_t*>(take(z.hits));
+  c.warm_b = static_cast<uint32_t*>(take(z.warm_b));
   c.attn_count = static_cast<int32_t*>(take(z.attn_count));
   c.counters = static_cast<unsigned long long*>(take(z.counters));
   c.status = static_cast<int*>(take(z.status));
@@ -644,6 +645,7 @@ skv_status shadowkv_rewind(shadowkv_ctx* h, void* stream) {
   if (c.item_done)
     CK(cudaMemsetAsync(c.item_done, 0, static_cast<size_t>(c.p.b) * c.p.h_kv * c.p.k * sizeof(int32_t), st));
   CK(cudaMemsetAsync(c.sc_ctr, 0, 2 * sizeof(int32_t), st));
+  CK(cudaMemsetAsync(c.warm_b, 0, static_cast<size_t>(c.p.b) * c.p.h_kv * sizeof(uint32_t), st));
   c.n_app = 0;
   return SKV_OK;
 }

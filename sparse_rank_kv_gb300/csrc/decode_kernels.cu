@@ -17,6 +17,11 @@ namespace skv {
 
 constexpr int kScoreTile = 128;      // landmarks per score tile (one per thread)
 constexpr int kSelectThreads = 1024;
+// How far below the previous step's k-th largest S2 (a log softmax weight)
+// the selection's first threshold try sits: the k-th S2 moved by at most
+// 0.05 per step on the synthetic queries of the headline workload and by
+// 0.24 at a hit rate of about 0.6
+constexpr float kWarmMargin = 0.25f;
 constexpr int kFetchWarps = 32;
 
 // ------------------------------------------------------------------ score
@@ -85,7 +90,7 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
          int32_t* __restrict__ hits, unsigned long long* __restrict__ counters,
          const T* __restrict__ k_new, const T* __restrict__ v_new, T* __restrict__ K_loc,
          T* __restrict__ V_loc, T* __restrict__ KV_loc, int loc_row, int loc_cap,
-         int* __restrict__ status) {
+         uint32_t* __restrict__ warm_b, int* __restrict__ status) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int nw = (n + 31) >> 5;
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
@@ -124,6 +129,9 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
   // this head's cache slots (written by the previous step's selection)
   int32_t* sc_row = slot_chunk + static_cast<size_t>(pair) * k;
   const int my_slot_chunk = cache_on && tid < k ? sc_row[tid] : -1;
+  // the previous step's k-th largest S2 minus a margin, as a key (0: none)
+  const uint32_t b_warm = warm_b != nullptr ? warm_b[pair] : 0u;
+  uint32_t b_next = 0u;
   const int n8 = (n + 7) >> 3;
   const bool bounded = m8 != nullptr && group_reduce == 0 && 2 * n8 <= n && n8 <= 4 * nthr;
   // the bounded path's shared state (below); its counters and the bitmap of
@@ -242,15 +250,35 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
       atomicMin(bmin_slot, kmin);
     }
     __syncthreads();
+    // The threshold B: first, when the previous step left one, its k-th
+    // largest S2 minus a margin (that value moves little from step to step).
+    // The chunks with S2 >= B are exactly the survivors below, so with at
+    // least k of them the top k is among them; else (the first step, a
+    // larger move) B is taken from the bounds as follows.
+    const bool warm = b_warm != 0u && *nnz_slot >= k;
+    for (int attempt = warm ? 0 : 1; attempt < 2 && !topk_done; ++attempt) {
     uint32_t B = 1u;    // fewer than k groups with a valid chunk: all of them are candidates
-    if (*nnz_slot >= k) {
-      // two 8-bit digits: B is the lower edge of the range that holds the
-      // k-th largest bound, still a lower bound of the k-th largest S2 (the
-      // bounds' range is known)
-      if (n8 <= 2048) block_kth_256<8>(bkey, n8, k, ks, 2, *bmin_slot, *bmax_slot);
-      else block_kth_256<16>(bkey, n8, k, ks, 2, *bmin_slot, *bmax_slot);
-      __syncthreads();
-      B = static_cast<uint32_t>(ks[kKth8T]);
+    if (attempt == 0) {
+      B = b_warm;
+    } else {
+      if (warm) {
+        // start over: every thread has read the first try's counts
+        __syncthreads();
+        if (tid == 0) {
+          *cnt_slot = *ncand_slot = 0;
+          *smax_slot = 0u;
+        }
+        __syncthreads();
+      }
+      if (*nnz_slot >= k) {
+        // two 8-bit digits: B is the lower edge of the range that holds the
+        // k-th largest bound, still a lower bound of the k-th largest S2
+        // (the bounds' range is known)
+        if (n8 <= 2048) block_kth_256<8>(bkey, n8, k, ks, 2, *bmin_slot, *bmax_slot);
+        else block_kth_256<16>(bkey, n8, k, ks, 2, *bmin_slot, *bmax_slot);
+        __syncthreads();
+        B = static_cast<uint32_t>(ks[kKth8T]);
+      }
     }
     // candidate groups, compacted by warps of 32 groups
     for (int w0 = warp * 32; w0 < n8; w0 += nthr) {
@@ -326,6 +354,7 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
         __syncthreads();
         const uint32_t Tk = static_cast<uint32_t>(ks[kKth8T]);
         const int need = ks[kKth8Need];
+        b_next = max(order_key(from_order_key(Tk) - kWarmMargin), 1u);
         if (ks[kKth8Eq] == need) {
           for (int i = tid; i < nsurv; i += nthr)
             if (vals[i] >= Tk) atomicOr(&words[vidx[i] >> 5], 1u << (vidx[i] & 31));
@@ -348,6 +377,7 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
         topk_done = true;
       }
     }
+    }   // attempts
   }
   // selection keys: S2 per chunk, 0 for outliers
   auto key_of = [&](float sc_max, float sc_sum, bool excluded) -> uint32_t {
@@ -475,6 +505,7 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
     sel_slot[static_cast<size_t>(pair) * k + tid] = slot;
   }
   if (tid == 0) {
+    if (warm_b != nullptr) warm_b[pair] = b_next;
     hits[pair] = k - nmiss;
     atomicAdd(&counters[0], static_cast<unsigned long long>(k - nmiss));
     atomicAdd(&counters[1], static_cast<unsigned long long>(nmiss));
@@ -663,7 +694,7 @@ static cudaError_t select_t(Ctx& c, const void* k_new, const void* v_new, int lo
       c.miss_count, c.miss_base, c.att_slot, static_cast<int>(c.t & 1), c.hits, c.counters, static_cast<const T*>(k_new),
       static_cast<const T*>(v_new),
       static_cast<T*>(c.K_loc), static_cast<T*>(c.V_loc), static_cast<T*>(c.KV_loc), loc_row, c.loc_cap,
-      c.status);
+      c.warm_b, c.status);
 }
 
 template <typename T, int D>

@@ -104,6 +104,7 @@ struct Ctx {
   int32_t* at_ctr = nullptr;      // attention work counters, 4 per step parity
   int32_t* item_done = nullptr;   // per phase-1 attention item: its value groups fetched this step
   long long at_last = -2;         // step of the last tensor-core attention launch
+  uint32_t* warm_b = nullptr;     // per head: the next selection's first threshold try (0: none)
   int32_t* sc_ctr = nullptr;      // landmark-score tail tile counters, one per step parity
   long long sc_last = -2;         // step of the last tensor-core score launch
   float* score_m8 = nullptr;      // per (batch, query head, 8 chunks): max logit (tensor-core score)

@@ -254,6 +254,39 @@ def test_rebuild_inside_the_attention_launch_full_size():
     assert ctx.layout()["rebuild_in_attention"] == 1
 
 
+@pytest.mark.parametrize("q_sigma", [2.0, 0.02], ids=["large_moves", "small_moves"])
+def test_selection_threshold_carried_between_steps(q_sigma):
+    """The selection's first threshold try is the previous step's k-th
+    largest S2 minus a margin; a try that leaves fewer than k chunks at or
+    above it falls back to the threshold from the bounds.  With large query
+    moves most tries fail, with small ones most succeed: every selection is
+    checked against the oracle either way."""
+    run_parity(SMALL.with_(q_sigma=q_sigma, steps=6, seed=60))
+
+
+def test_selections_repeat_after_a_rewind():
+    """A rewind empties the cache and drops the carried threshold: the same
+    steps again give the same selections (the carried threshold changes how
+    the top k is found, never which chunks it holds)."""
+    cfg = SMALL.with_(steps=5, seed=61)
+    st = synth.make_state(cfg, device="cuda")
+    ctx = binding.load_state(binding.make_params(cfg), st)
+    dt = synth.torch_dtype(cfg.dtype)
+    runs = []
+    for _ in range(2):
+        sels = []
+        for t in range(cfg.steps):
+            out = torch.empty(cfg.b, cfg.h_q, cfg.d, dtype=dt, device="cuda")
+            ctx.decode_step(st["q"][t].contiguous(), st["k_new"][t].contiguous(), st["v_new"][t].contiguous(), out)
+            torch.cuda.synchronize()
+            sels.append(ctx.export("SEL").clone())
+        runs.append(sels)
+        ctx.rewind()
+    ctx.check()
+    for t in range(cfg.steps):
+        assert torch.equal(runs[0][t], runs[1][t]), f"step {t}: selections differ after the rewind"
+
+
 def test_max_new_is_enforced():
     cfg = SMALL.with_(steps=2, seed=40)
     st = synth.make_state(cfg, device="cuda")
