@@ -449,12 +449,17 @@ __device__ __forceinline__ void block_kth(const uint32_t* v, int cnt, int kth, i
 // and scratch[kKth8Need] is not meaningful.  After a complete select
 // scratch[kKth8Eq] is the number of values equal to the k-th largest.  A
 // caller that knows a range [rlo, rhi] (rhi != 0) holding every non-zero
-// value passes it, and the select skips its min/max reduction.
+// value passes it, and the select skips its min/max reduction.  With
+// whole_bucket, the select stops as soon as every value of the digit range
+// holding the k-th largest is among the kth largest: scratch[kKth8T] is then
+// that range's lower edge, and the values at or above it are exactly the kth
+// largest (scratch[kKth8Eq] == scratch[kKth8Need]).
 constexpr int kKth8T = 8 * 256 + 256 + 4, kKth8Need = kKth8T + 1, kKth8Eq = kKth8T + 2,
               kKth8Ints = 8 * 256 + 256 + 8;
 template <int V = 4>
 __device__ __forceinline__ void block_kth_256(const uint32_t* v, int cnt, int kth, int* scratch,
-                                              int max_passes = 4, uint32_t rlo = 0u, uint32_t rhi = 0u) {
+                                              int max_passes = 4, uint32_t rlo = 0u, uint32_t rhi = 0u,
+                                              bool whole_bucket = false) {
   const int tid = threadIdx.x;
   if (tid >= 256) return;
   const int lane = tid & 31, warp = tid >> 5;
@@ -550,6 +555,7 @@ __device__ __forceinline__ void block_kth_256(const uint32_t* v, int cnt, int kt
     pmask |= dmask << shift;
     need = bc[1];
     hb = shift;
+    if (whole_bucket && bc[6] == need) break;   // the whole range is taken
   }
   if (tid == 0) {
     bc[4] = static_cast<int>(vmin + prefix);

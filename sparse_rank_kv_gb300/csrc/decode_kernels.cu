@@ -348,9 +348,9 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
         // largest key]); `need` of the survivors equal to Tk are taken
         // (every chunk equal to Tk is a survivor)
         const uint32_t shi = *smax_slot;
-        if (nsurv <= 1024) block_kth_256<4>(vals, nsurv, k, ks, 4, B, shi);
-        else if (nsurv <= 2048) block_kth_256<8>(vals, nsurv, k, ks, 4, B, shi);
-        else block_kth_256<16>(vals, nsurv, k, ks, 4, B, shi);
+        if (nsurv <= 1024) block_kth_256<4>(vals, nsurv, k, ks, 4, B, shi, true);
+        else if (nsurv <= 2048) block_kth_256<8>(vals, nsurv, k, ks, 4, B, shi, true);
+        else block_kth_256<16>(vals, nsurv, k, ks, 4, B, shi, true);
         __syncthreads();
         const uint32_t Tk = static_cast<uint32_t>(ks[kKth8T]);
         const int need = ks[kKth8Need];
