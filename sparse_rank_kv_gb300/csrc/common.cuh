@@ -591,7 +591,7 @@ __device__ __forceinline__ void bitmap_list(const uint32_t* bits, int nw, int* o
   int cnt = 0;
   for (int w = w0; w < w1; ++w) cnt += __popc(bits[w]);
   int tot;
-  int ex = block_exclusive_scan(cnt, tmp, &tot);
+  int ex = block_exclusive_scan(cnt, tmp, &tot, true);   // tmp is not written again here
   for (int w = w0; w < w1; ++w) {
     wpref[w] = ex;
     uint32_t b = bits[w];
