@@ -213,31 +213,44 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
   if (bounded) {
     int nz = 0;
     uint32_t kmax = 0u, kmin = 0xffffffffu;
+    // with a carried threshold (below) the groups that reach it are
+    // compacted as candidates while the bounds are formed
+    const bool warm = b_warm != 0u;
     auto put_bound = [&](int w, float bnd) {
-      const uint32_t kb = bnd == -INFINITY ? 0u : order_key(bnd);
-      bkey[w] = kb;
+      const uint32_t kb = w < n8 && bnd != -INFINITY ? order_key(bnd) : 0u;
+      if (w < n8) bkey[w] = kb;
       if (kb != 0u) {
         ++nz;
         kmax = max(kmax, kb);
         kmin = min(kmin, kb);
+      }
+      if (warm) {
+        const bool isc = kb != 0u && kb >= b_warm;
+        const unsigned m = __ballot_sync(0xffffffffu, isc);
+        int base = 0;
+        if (lane == 0 && m) base = atomicAdd(ncand_slot, __popc(m));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        if (isc) cand[base + __popc(m & ((1u << lane) - 1u))] = w;
       }
     };
     if (pre) {
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int w = tid + u * nthr;
-        if (w >= n8) continue;
         float bnd = -INFINITY;
 #pragma unroll
         for (int g = 0; g < G; ++g) bnd = fmaxf(bnd, gm[u][g] - lse[g]);
         put_bound(w, bnd);
       }
     } else {
-      for (int w = tid; w < n8; w += nthr) {
+      for (int w0 = 0; w0 < n8; w0 += nthr) {
+        const int w = w0 + tid;
         float bnd = -INFINITY;
+        if (w < n8) {
 #pragma unroll
-        for (int g = 0; g < G; ++g)
-          bnd = fmaxf(bnd, __ldcg(m8 + (static_cast<size_t>(pair) * G + g) * n8 + w) - lse[g]);
+          for (int g = 0; g < G; ++g)
+            bnd = fmaxf(bnd, __ldcg(m8 + (static_cast<size_t>(pair) * G + g) * n8 + w) - lse[g]);
+        }
         put_bound(w, bnd);
       }
     }
@@ -255,7 +268,6 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
     // The chunks with S2 >= B are exactly the survivors below, so with at
     // least k of them the top k is among them; else (the first step, a
     // larger move) B is taken from the bounds as follows.
-    const bool warm = b_warm != 0u && *nnz_slot >= k;
     for (int attempt = warm ? 0 : 1; attempt < 2 && !topk_done; ++attempt) {
     uint32_t B = 1u;    // fewer than k groups with a valid chunk: all of them are candidates
     if (attempt == 0) {
@@ -280,7 +292,9 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
         B = static_cast<uint32_t>(ks[kKth8T]);
       }
     }
-    // candidate groups, compacted by warps of 32 groups
+    // candidate groups, compacted by warps of 32 groups (the first try's
+    // were compacted with the bounds)
+    if (attempt == 1) {
     for (int w0 = warp * 32; w0 < n8; w0 += nthr) {
       const int w = w0 + lane;
       const bool isc = w < n8 && bkey[w] != 0u && bkey[w] >= B;
@@ -291,6 +305,7 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
       if (isc) cand[base + __popc(m & ((1u << lane) - 1u))] = w;
     }
     __syncthreads();
+    }
     const int ne = *ncand_slot * 8;
     if (ne <= 2 * cap) {
       // the candidates' chunks, in rounds of 4 per thread: all loads of a
