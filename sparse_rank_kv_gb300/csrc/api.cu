@@ -609,9 +609,11 @@ skv_status shadowkv_decode_step_host(shadowkv_ctx* h, const void* q, const void*
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t qb = static_cast<size_t>(c.p.b) * c.p.h_q * c.p.d * c.E;
   const size_t kb = static_cast<size_t>(c.p.b) * c.p.h_kv * c.p.d * c.E;
-  // q goes to the staging buffer (the tensor maps stay cached on its address);
-  // k_new, v_new and out are used through their device mapping when they
-  // are pinned host memory, else staged
+  // q goes to the staging buffer (the tensor maps stay cached on its address),
+  // copied first so that the copy's start overlaps the lookups below; k_new,
+  // v_new and out are used through their device mapping when they are
+  // pinned host memory, else staged
+  CK(cudaMemcpyAsync(c.q_stage, q, qb, cudaMemcpyHostToDevice, st));
   const void* kd = nullptr;
   const void* vd = nullptr;
   const void* oview = nullptr;
@@ -619,7 +621,6 @@ skv_status shadowkv_decode_step_host(shadowkv_ctx* h, const void* q, const void*
   CK(mapped_view(c, v_new, &vd));
   CK(mapped_view(c, out, &oview));
   void* od = const_cast<void*>(oview);
-  CK(cudaMemcpyAsync(c.q_stage, q, qb, cudaMemcpyHostToDevice, st));
   if (k_new && !kd) {
     CK(cudaMemcpyAsync(c.kv_stage, k_new, kb, cudaMemcpyHostToDevice, st));
     kd = c.kv_stage;
