@@ -274,15 +274,16 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
     int lastA[kAtStages];
 #pragma unroll
     for (int i = 0; i < kAtStages; ++i) lastA[i] = -1;
-    // phase-0 item numbers are requested two items ahead, so the atomics'
-    // round trips overlap the copies; in phase 1 (about one item per CTA)
-    // the next number is requested only once the current item's copies are
-    // issued, so that every CTA has taken its first item before any takes a
-    // second
-    int phase = 0, x = 0, x1 = 0;
+    // phase-0 item numbers come two at a time, the next pair requested as
+    // the current pair starts, so that no atomic's round trip stalls the
+    // loop; in phase 1 (about one item per CTA) the next number is requested
+    // only once the current item's copies are issued, so that every CTA has
+    // taken its first item before any takes a second
+    int phase = 0, x = 0, pcur = 0, pnext = 0, pidx = 0;
     if (lane == 0) {
-      x = atomicAdd(&ctr[0], 1);
-      x1 = atomicAdd(&ctr[0], 1);
+      pcur = atomicAdd(&ctr[0], 2);
+      pnext = atomicAdd(&ctr[0], 2);
+      x = pcur;
     }
     for (int it = 0;; ++it) {
       x = __shfl_sync(0xffffffffu, x, 0);
@@ -303,9 +304,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
       // cache slots of the item's chunks (lane = chunk), loaded before the wait
       const int nch = t.seg >= 2 ? t.cnt / c : 0;
       const int slot = lane < nch ? att_slot[static_cast<size_t>(t.pair) * k + t.t0 + lane] : 0;
-      // the number after the next one, requested before this item's copies
       int xn = 0;
-      if (lane == 0 && !done && phase == 0) xn = atomicAdd(&ctr[0], 1);
       bool ok = true;
       if (lane == 0) ok = !*s_abort && tc::mbar_wait(&empty[st], (use & 1) ^ 1, kWaitLimit);
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -368,21 +367,33 @@ k_attn_tc(const __grid_constant__ CUtensorMap mapQ, const bf16* __restrict__ KV_
                         static_cast<uint32_t>(groups * 4096), &full[st]);
       }
       __syncwarp();
-      if (lane < nch) {
-        if (slot < 0 || slot >= k) {
-          flag_error(status, DEV_BAD_SLOT);
-        } else {
+      {
+        // one bulk copy per run of consecutive slots (adjacent records):
+        // lane l starts a run unless its slot follows lane l - 1's
+        const bool good = lane < nch && slot >= 0 && slot < k;
+        const int sprev = __shfl_up_sync(0xffffffffu, slot, 1);
+        const bool gprev = __shfl_up_sync(0xffffffffu, good ? 1 : 0, 1) != 0;
+        const bool cont = lane > 0 && good && gprev && slot == sprev + 1;
+        const unsigned long long cm = __ballot_sync(0xffffffffu, cont);
+        if (lane < nch && !good) flag_error(status, DEV_BAD_SLOT);
+        if (good && !cont) {
+          const int len = __ffsll(~(cm >> (lane + 1)));
           tc::bulk_load(sR + lane * c * 512, KV_slot + (static_cast<size_t>(t.pair) * k + slot) * c * 2 * kAtD,
-                        static_cast<uint32_t>(c * 512), &full[st]);
+                        static_cast<uint32_t>(len * c * 512), &full[st]);
         }
       }
       lastA[st] = use;
       if (phase == 1) {
         if (lane == 0) xn = atomicAdd(&ctr[1], 1);
         x = xn;
+      } else if (pidx == 0) {
+        pidx = 1;
+        x = pcur + 1;
       } else {
-        x = x1;
-        x1 = xn;
+        pidx = 0;
+        pcur = pnext;
+        if (lane == 0) pnext = atomicAdd(&ctr[0], 2);
+        x = pcur;
       }
     }
     // no copy may still be landing in this CTA's shared memory at exit

@@ -494,10 +494,11 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
   const int mrank = ranks & 0xffff, frank = ranks >> 16;
   const int nmiss = both & 0xffff, nfree = both >> 16;
   if (is_free) s_free[frank] = tid;
-  // the attention's order of the selected chunks' slots: hits first (each
-  // after the hits before it), then misses
-  if (att_slot != nullptr && tid < k && !is_miss)
-    att_slot[static_cast<size_t>(pair) * k + tid - mrank] = s_slot[tid];
+  // the attention's list of the selected chunks' slots: the kept slots in
+  // ascending order (slot tid after the kept slots below it), then the
+  // misses' slots (ascending too); consecutive slots hold adjacent records
+  if (att_slot != nullptr && tid < k && !is_free)
+    att_slot[static_cast<size_t>(pair) * k + tid - frank] = tid;
   // the reserved range's start (the atomic issued before the scan)
   __shared__ int s_base;
   if (tid == 0) {
