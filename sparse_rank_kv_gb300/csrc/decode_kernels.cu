@@ -173,25 +173,28 @@ k_select(const float* __restrict__ P, const float2* __restrict__ part, const flo
   }
   // log-sum-exp of each query head over the candidate chunks (4 partials
   // of 32 landmarks per 128-landmark score tile): a warp per head, one pass
-  // (each lane's partials in rounds of 8 loads, merged as (max, sum))
+  // (each lane's partials two per 16-byte load, in rounds of 8 loads: one
+  // round up to 128K tokens at 8 per chunk; merged as (max, sum))
   for (int g = warp; g < G; g += nthr / 32) {
-    const float2* pp = part + (static_cast<size_t>(pair) * G + g) * ntile * 4;
-    const int lim = 4 * ntile;
+    const float4* pp = reinterpret_cast<const float4*>(part + (static_cast<size_t>(pair) * G + g) * ntile * 4);
+    const int lim = 2 * ntile;
     float m = -INFINITY, z = 0.f;
     for (int t0 = 0; t0 < lim; t0 += 32 * 8) {
-      float2 v[8];
+      float4 v[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int t = t0 + u * 32 + lane;
-        v[u] = t < lim ? __ldcg(pp + t) : make_float2(-INFINITY, 0.f);
+        v[u] = t < lim ? __ldcg(pp + t) : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
       }
       float mc = m;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) mc = fmaxf(mc, v[u].x);
+      for (int u = 0; u < 8; ++u) mc = fmaxf(mc, fmaxf(v[u].x, v[u].z));
       float zc = z > 0.f ? z * __expf(m - mc) : 0.f;
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
+      for (int u = 0; u < 8; ++u) {
         if (v[u].y > 0.f) zc += v[u].y * __expf(v[u].x - mc);
+        if (v[u].w > 0.f) zc += v[u].w * __expf(v[u].z - mc);
+      }
       m = mc;
       z = zc;
     }
