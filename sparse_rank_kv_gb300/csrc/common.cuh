@@ -128,9 +128,10 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// Block-wide exclusive scan of one int per thread.  `tmp` holds >= 33 ints of
+// Block-wide exclusive scan of one int per thread.  `tmp` holds >= 32 ints of
 // shared memory.  Returns the exclusive prefix; *total gets the block sum.
-// Every thread of the block must call it.
+// Every thread of the block must call it.  One barrier: every warp scans the
+// per-warp totals itself.
 // With last_use, tmp is not written again before the block's next barrier,
 // and the scan skips its closing barrier.
 __device__ __forceinline__ int block_exclusive_scan(int v, int* tmp, int* total, bool last_use = false) {
@@ -144,19 +145,16 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* tmp, int* total,
   }
   if (lane == 31) tmp[warp] = x;
   __syncthreads();
-  if (warp == 0) {
-    int w = lane < nwarps ? tmp[lane] : 0;
+  int w = lane < nwarps ? tmp[lane] : 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    if (lane < nwarps) tmp[lane] = w;  // inclusive warp totals
-    if (lane == nwarps - 1) tmp[32] = w;
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, w, o);
+    if (lane >= o) w += y;
   }
-  __syncthreads();
-  const int excl = (warp ? tmp[warp - 1] : 0) + x - v;
-  *total = tmp[32];
+  // w: inclusive totals of warps 0..lane
+  const int before = __shfl_sync(0xffffffffu, w, warp > 0 ? warp - 1 : 0);
+  const int excl = (warp ? before : 0) + x - v;
+  *total = __shfl_sync(0xffffffffu, w, nwarps - 1);
   if (!last_use) __syncthreads();
   return excl;
 }
