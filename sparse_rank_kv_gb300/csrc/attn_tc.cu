@@ -14,10 +14,12 @@
 // group in 4 KB records laid out as the tensor core's no-swizzle K-major
 // tiles: K ([d/8][token%8][d%8], 2 KB), then V^T ([d/8][d%8][token%8], 2 KB).
 //   warp 0     : producer -- per item the keys and values by bulk copies
-//                (one per selected chunk from its cache slot, one for a piece
-//                of the outliers or local window) and the head's q (TMA, 16
-//                rows of which the rows past G read as zeros) into a 3-stage
-//                ring, with the item's description in the stage.
+//                (one per run of adjacent cache-slot records among the item's
+//                selected chunks, one for a piece of the outliers or local
+//                window) and the head's q (TMA, 16 rows of which the rows past
+//                G read as zeros) into a 3-stage ring, with the item's
+//                description in the stage; phase-0 item numbers come two at
+//                a time.
 //   warp 1     : tcgen05.mma.  S = K q^T (M = 128 tokens, N = 16, K = d) into
 //                one of two TMEM S buffers; after the softmax warps publish
 //                P, O = V^T P^T (M = d, N = 16, K = 16-token steps) into one
